@@ -1,0 +1,36 @@
+import os
+import re
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    config.addinivalue_line("markers", "slow: full-size workload, minutes")
+
+
+def load_golden(name):
+    """Parses a ``key = value`` fixture under tests/golden/ ('#' starts a comment)."""
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            k, v = [s.strip() for s in line.split("=", 1)]
+            if re.fullmatch(r"[\[\]\d,.\-\s]+", v):
+                v = eval(v, {"__builtins__": {}})  # numbers and nested lists only
+            out[k] = v
+    return out
+
+
+@pytest.fixture(scope="session")
+def golden():
+    return load_golden
