@@ -1,0 +1,291 @@
+/*
+ * shmm.h -- C-ABI of libshmm: the sharded matmul A[I,J] . B[J,K] -> C[I,K]
+ * with partial-sum reduction, for virtual ranks held on one GPU.
+ *
+ * The operation.  A mesh is a grid of ranks with named axes, e.g. {X:4,Y:2}
+ * for 8 ranks; a sharding says which mesh axes split which array dims
+ * ("Sharded matmuls and collectives on a torus", Notation).  A sharded matmul
+ * is a local GEMM per rank plus the collectives the sharding implies
+ * ("Sharding Matrix Multiply", Cases 1-4 and Summary):
+ *   case 1  no operand sharded on J: local GEMM only;
+ *   case 2  one operand sharded on J: all-gather it along J, then GEMM;
+ *   case 3  both sharded on J along the same axes: each rank's GEMM yields a
+ *           partial sum C{U}; a reduce-scatter (disjoint output shards) or an
+ *           all-reduce (replicated output) finishes it;
+ *   case 4  a mesh axis shards both A's I and B's K: all-gather B along K,
+ *           then case 1.
+ * Which collective runs is fixed by the ownership the consumer asks for
+ * ("Sharded matrix multiplication and result ownership", The mechanism,
+ * steps 1-5): all-reduce for a replicated C, reduce-scatter for row- (or
+ * column-) owned C, all-gather only when the consumer needs the whole tensor.
+ *
+ * Virtual ranks.  Rank r's data lives in device buffers of its own; every
+ * call takes a host array of N device pointers, one per rank, indexed by rank
+ * id.  Rank ids are row-major over the mesh axes, first axis major; a dim
+ * split by several axes (I_XY) flattens them with the first listed major.
+ * Each buffer holds exactly that rank's box (shmm_plan_rank_box) as a dense
+ * row-major matrix (leading dimension = box width).  Buffers of different
+ * ranks must not overlap.  They may be slices of one allocation.
+ *
+ * Ownership of memory.  The caller allocates and frees every device buffer
+ * (operands, results, partials, workspace).  The library allocates no device
+ * memory; it owns only shmm_plan_t objects (host memory), freed by
+ * shmm_plan_destroy.
+ *
+ * Execution.  Device work is enqueued asynchronously on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and the call returns once
+ * it is enqueued.  Arguments are validated before anything is enqueued; a
+ * call that returns an error has enqueued nothing, except SHMM_ERR_CUDA from
+ * a launch in a multi-kernel call, after which the outputs are undefined.
+ *
+ * Errors.  Every entry point returns shmm_status_t (SHMM_OK = 0).  Errors are
+ * not sticky: each call validates its own arguments.  shmm_last_error()
+ * returns a human-readable message for the calling thread's last failure.
+ * Device-side faults that kernels detect without trapping (a pipeline wait
+ * that exceeded its time limit) are recorded in a device status word read by
+ * shmm_sync_status().
+ *
+ * Numerics.  Inputs are bf16 or fp32.  Products accumulate in fp32; partial
+ * sums are stored in fp32 (unless SHMM_FLAG_PARTIAL_OUT_DTYPE); the sum over a
+ * reduction group is formed in fp32 in ascending rank order, one rounding per
+ * addition, then rounded once to the output type (bf16: round to nearest
+ * even).  The fused path (SHMM_FLAG_FUSED) keeps each rank's partial in its
+ * own fp32 accumulator and sums them in the same order, so it matches the
+ * standalone reduction bit for bit.  SHMM_FLAG_TREE sums with a balanced
+ * pairwise tree over the ranks in ascending order instead.
+ */
+#ifndef SHMM_H
+#define SHMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SHMM_OK = 0,
+    SHMM_ERR_INVALID_SPEC = 1,   /* unknown axis, an axis splitting two dims of
+                                    one array, or an ownership change that is
+                                    neither a reduction nor an all-gather */
+    SHMM_ERR_ILLEGAL_OUTPUT = 2, /* the requested C sharding is itself illegal,
+                                    e.g. C[I_X,K_X] (cheat-sheet, Case 4) */
+    SHMM_ERR_SHAPE = 3,          /* a dim does not split evenly, a size is
+                                    <= 0, a buffer would exceed 2^62 bytes, or
+                                    too many ranks/axes */
+    SHMM_ERR_DTYPE = 4,          /* unsupported dtype combination */
+    SHMM_ERR_NULL = 5,           /* a required pointer is NULL */
+    SHMM_ERR_ALIGN = 6,          /* a device pointer is not 16-byte aligned */
+    SHMM_ERR_CUDA = 7,           /* a CUDA runtime/driver call failed */
+    SHMM_ERR_TIMEOUT = 8,        /* a kernel's bounded wait expired (device
+                                    status word; see shmm_sync_status) */
+    SHMM_ERR_NOMEM = 9,          /* host allocation failed, or the workspace
+                                    passed is smaller than required */
+    SHMM_ERR_UNSUPPORTED = 10,   /* valid request the plan does not need or
+                                    this operation cannot serve (e.g. a
+                                    reduce-scatter on a plan with no
+                                    contracted-axis split) */
+    SHMM_ERR_INJECTED = 11       /* failure forced by SHMM_INJECT_FAIL (tests) */
+} shmm_status_t;
+
+typedef enum { SHMM_F32 = 0, SHMM_BF16 = 1 } shmm_dtype_t;
+
+#define SHMM_MAX_AXES 8
+#define SHMM_AXIS_NAME_LEN 8
+#define SHMM_MAX_RANKS 256
+
+/* A device mesh: `naxes` named axes, rank count = product of sizes. */
+typedef struct {
+    int naxes;
+    char name[SHMM_MAX_AXES][SHMM_AXIS_NAME_LEN]; /* NUL-terminated */
+    int size[SHMM_MAX_AXES];                      /* each >= 1 */
+} shmm_mesh_t;
+
+/* A sharding of a 2-D array: for dim d (0 = rows, 1 = cols), the mesh axis
+ * indices that split it, first = major.  naxes[d] == 0 means the dim is not
+ * split (replicated over every axis not named anywhere). */
+typedef struct {
+    int naxes[2];
+    int axes[2][SHMM_MAX_AXES];
+} shmm_spec_t;
+
+/* Plan flags */
+#define SHMM_FLAG_FUSED 0x1u   /* shmm_run: reduce in the GEMM epilogue; each
+                                  output tile is summed over its reduction
+                                  group in ascending rank order and written
+                                  once to its owner(s) */
+#define SHMM_FLAG_GELU 0x2u    /* apply GeLU (tanh form) to the finished result
+                                  before the output rounding (the column-
+                                  parallel first matmul of an MLP pair) */
+#define SHMM_FLAG_TREE 0x4u    /* standalone reduction: warp-shuffle pairwise
+                                  tree over the ranks instead of the sequential
+                                  rank-order sum */
+#define SHMM_FLAG_PARTIAL_OUT_DTYPE 0x8u /* partial buffers are stored in the
+                                  output dtype instead of fp32 */
+#define SHMM_FLAG_SIMT 0x10u   /* local GEMM on CUDA cores even for bf16 (the
+                                  tensor-core path is used otherwise whenever
+                                  the shapes allow TMA: J_r, K_r multiples of
+                                  8) */
+
+/* Boxes a plan defines for each rank (shmm_plan_rank_box `tensor`). */
+typedef enum {
+    SHMM_TENSOR_A = 0,         /* rank's shard of A, as given */
+    SHMM_TENSOR_B = 1,         /* rank's shard of B, as given */
+    SHMM_TENSOR_C = 2,         /* rank's block of C, as requested */
+    SHMM_TENSOR_P = 3,         /* rank's local product / partial C{U} */
+    SHMM_TENSOR_A_LOCAL = 4,   /* A as the local GEMM reads it (after the
+                                  case 2/4 all-gather) */
+    SHMM_TENSOR_B_LOCAL = 5,
+    SHMM_TENSOR_C_REDUCED = 6  /* rank's block after the reduction (the owner
+                                  block of a reduce-scatter), before any
+                                  all-gather of the result */
+} shmm_tensor_t;
+
+typedef enum {
+    SHMM_COLL_NONE = 0,
+    SHMM_COLL_REDUCE_SCATTER = 1,
+    SHMM_COLL_ALL_REDUCE = 2
+} shmm_collective_t;
+
+typedef struct {
+    int case_id;           /* 1..4 (cheat-sheet numbering) */
+    int collective;        /* shmm_collective_t of the partial-sum reduction */
+    int scatter_dim;       /* reduce-scatter dim: 0 = I, 1 = K; -1 if none */
+    int nranks;
+    int group_size;        /* ranks per reduction group (1 = none) */
+    int ngroups;           /* number of reduction groups */
+    int gather_A_size;     /* ranks per all-gather group of A (1 = none) */
+    int gather_B_size;
+    int gather_C_size;     /* ranks per all-gather group of the result */
+    int in_dtype, out_dtype, partial_dtype;
+    uint32_t flags;
+    int tensor_core;       /* 1 if the local GEMM runs on tcgen05 */
+    int fused;             /* 1 if shmm_run reduces in the GEMM epilogue
+                              (SHMM_FLAG_FUSED honoured: on tensor cores, at
+                              most 8 ranks per group; otherwise shmm_run
+                              reduces with the standalone kernel) */
+    int64_t local_I, local_J, local_K;   /* per-rank GEMM M, K, N */
+    int64_t flops_per_rank;              /* 2 * local_I * local_J * local_K */
+    int64_t payload_operand_ag;          /* bytes each rank sends, counted once
+                                            at the sender (ownership page,
+                                            step 6) */
+    int64_t payload_reduce_scatter;
+    int64_t payload_result_ag;
+    size_t workspace_bytes;              /* shmm_run's workspace requirement */
+} shmm_plan_info_t;
+
+typedef struct shmm_plan shmm_plan_t;
+
+/* Builds a plan: validates the shardings (a mesh axis splits at most one dim
+ * of an array: cheat-sheet Notation, Rule), classifies the case, derives the
+ * operand gathers, the reduction groups (ranks that differ only on the
+ * contracted axes), the owner of every output block and the collective the
+ * requested C sharding needs (ownership page, steps 1-5).  Host only.
+ *   mesh, spec_A, spec_B, spec_C  in: the mesh and the three shardings
+ *                                     (spec_C = the consumer's ownership)
+ *   I, J, K                       in: global sizes; every split must be even
+ *   in_dtype                      in: dtype of A and B
+ *   out_dtype                     in: dtype of C
+ *   flags                         in: SHMM_FLAG_*
+ *   plan                          out: new plan, owned by the caller
+ * Errors: NULL, SHAPE, INVALID_SPEC, ILLEGAL_OUTPUT, DTYPE, NOMEM. */
+shmm_status_t shmm_plan(const shmm_mesh_t *mesh, const shmm_spec_t *spec_A,
+                        const shmm_spec_t *spec_B, const shmm_spec_t *spec_C,
+                        int64_t I, int64_t J, int64_t K, shmm_dtype_t in_dtype,
+                        shmm_dtype_t out_dtype, uint32_t flags, shmm_plan_t **plan);
+
+/* Frees a plan (NULL is accepted). */
+shmm_status_t shmm_plan_destroy(shmm_plan_t *plan);
+
+/* Fills `info` with the plan's classification, shapes and byte counts. */
+shmm_status_t shmm_plan_query(const shmm_plan_t *plan, shmm_plan_info_t *info);
+
+/* Offsets and extents (rows, cols) of `rank`'s box of `tensor` in the global
+ * array: the "completed values with explicit per-rank coordinates" of the
+ * ownership page (Interfaces).  Errors: NULL, SHAPE (rank out of range),
+ * UNSUPPORTED (unknown tensor). */
+shmm_status_t shmm_plan_rank_box(const shmm_plan_t *plan, int tensor, int rank,
+                                 int64_t off[2], int64_t ext[2]);
+
+/* Ranks of `rank`'s reduction group in ascending order (the summation
+ * order); `ranks` must hold info.group_size entries. */
+shmm_status_t shmm_plan_group(const shmm_plan_t *plan, int rank, int *ranks);
+
+/* shmm_run's workspace requirement in bytes (0 if none). */
+shmm_status_t shmm_workspace_size(const shmm_plan_t *plan, size_t *bytes);
+
+/* Local GEMM of every rank (ownership page, step 3; Row Parallelism,
+ * Z_i = X_i A_i): P_r = A_r . B_r over the rank's slice of J.
+ *   A_r[N]  in: box SHMM_TENSOR_A_LOCAL, in_dtype
+ *   B_r[N]  in: box SHMM_TENSOR_B_LOCAL, in_dtype
+ *   P_r[N]  out: box SHMM_TENSOR_P; fp32 partials if the plan reduces (or
+ *           out_dtype with SHMM_FLAG_PARTIAL_OUT_DTYPE), else out_dtype with
+ *           GeLU applied if SHMM_FLAG_GELU.
+ * Errors: NULL, ALIGN, CUDA. */
+shmm_status_t shmm_local_matmul(const shmm_plan_t *plan, const void *const *A_r,
+                                const void *const *B_r, void *const *P_r, void *stream);
+
+/* Reduce-scatter of the partials over each reduction group ("Sharding Matrix
+ * Multiply", Communication primitives; ownership page, step 4): for each
+ * element, the fp32 sum over the group's partials in ascending rank order
+ * (pairwise tree with SHMM_FLAG_TREE), GeLU if flagged, rounded to out_dtype,
+ * written only to the rank that owns it.
+ *   P_r[N]  in: box SHMM_TENSOR_P, partial dtype
+ *   C_r[N]  out: box SHMM_TENSOR_C_REDUCED of a reduce-scatter plan; for an
+ *           all-reduce plan, row block q (rows / group_size rows, dim 0) of
+ *           the partial goes to the group's q-th rank in ascending rank id
+ * Errors: NULL, ALIGN, UNSUPPORTED (plan has no contracted-axis split), CUDA. */
+shmm_status_t shmm_reduce_scatter(const shmm_plan_t *plan, const void *const *P_r,
+                                  void *const *C_r, void *stream);
+
+/* All-reduce of the partials: every rank of a group receives the whole sum
+ * (same arithmetic as shmm_reduce_scatter).
+ *   P_r[N]  in: box SHMM_TENSOR_P
+ *   C_r[N]  out: box SHMM_TENSOR_P, out_dtype
+ * Errors: NULL, ALIGN, UNSUPPORTED, CUDA. */
+shmm_status_t shmm_all_reduce(const shmm_plan_t *plan, const void *const *P_r,
+                              void *const *C_r, void *stream);
+
+/* All-gather ("Sharding Matrix Multiply", AllGather): every rank of a gather
+ * group receives the concatenation of the group's blocks.
+ *   tensor = SHMM_TENSOR_A: shards (box A) -> full (box A_LOCAL), in_dtype
+ *   tensor = SHMM_TENSOR_B: shards (box B) -> full (box B_LOCAL), in_dtype
+ *   tensor = SHMM_TENSOR_C: owner blocks (box C_REDUCED) -> requested blocks
+ *                           (box C), out_dtype
+ * Errors: NULL, ALIGN, UNSUPPORTED (the plan gathers nothing for `tensor`),
+ * CUDA. */
+shmm_status_t shmm_all_gather(const shmm_plan_t *plan, int tensor, const void *const *shard_r,
+                              void *const *full_r, void *stream);
+
+/* The whole sharded matmul: operand all-gathers (cases 2, 4), local GEMMs,
+ * the reduction (fused into the GEMM epilogue with SHMM_FLAG_FUSED, else a
+ * standalone kernel over fp32 partials in the workspace) and the result
+ * all-gather the requested ownership needs.
+ *   A_r[N], B_r[N]  in: boxes SHMM_TENSOR_A / SHMM_TENSOR_B
+ *   C_r[N]          out: box SHMM_TENSOR_C
+ *   workspace       device memory of >= shmm_workspace_size() bytes, 256-byte
+ *                   aligned (may be NULL when the size is 0)
+ * Errors: NULL, ALIGN, NOMEM (workspace too small), CUDA. */
+shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const void *const *B_r,
+                       void *const *C_r, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word that
+ * kernels set when a bounded wait expires.  Returns SHMM_OK, SHMM_ERR_TIMEOUT
+ * or SHMM_ERR_CUDA. */
+shmm_status_t shmm_sync_status(void *stream);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char *shmm_last_error(void);
+
+/* Static name of a status code. */
+const char *shmm_status_string(shmm_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int shmm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SHMM_H */

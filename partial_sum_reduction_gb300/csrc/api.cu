@@ -1,0 +1,395 @@
+// C-ABI entry points of libshmm that enqueue device work: argument checks,
+// workspace carving and dispatch to the kernels.  The plan itself is built
+// by planner.cpp.
+
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "shmm_internal.h"
+
+using shmm::fail;
+
+// Status word written by kernels whose bounded waits expire (0 = fine).
+__device__ int g_shmm_status_word;
+
+namespace {
+
+int *status_ptr(std::string *err) {
+    static int *cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = "no CUDA device";
+        return nullptr;
+    }
+    if (!cached[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_shmm_status_word);
+        if (e != cudaSuccess) {
+            *err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
+            return nullptr;
+        }
+        cached[dev] = static_cast<int *>(p);
+    }
+    return cached[dev];
+}
+
+// SHMM_INJECT_FAIL="name1,name2": those entry points fail before enqueuing.
+bool injected(const char *fn) {
+    const char *env = getenv("SHMM_INJECT_FAIL");
+    if (!env || !*env) return false;
+    const std::string list = std::string(",") + env + ",";
+    return list.find(std::string(",") + fn + ",") != std::string::npos;
+}
+
+shmm_status_t cuda_fail(const char *fn, int e, const std::string &extra = "") {
+    std::string m = std::string(fn) + ": " + cudaGetErrorString((cudaError_t)e);
+    if (!extra.empty()) m += " (" + extra + ")";
+    return fail(SHMM_ERR_CUDA, m);
+}
+
+// Per-rank pointer array: non-NULL, 16-byte aligned (NULL allowed for empty
+// boxes).
+shmm_status_t check_ptrs(const shmm_plan_t *p, const void *const *arr, int tensor, const char *fn,
+                         const char *what) {
+    if (!arr) return fail(SHMM_ERR_NULL, std::string(fn) + ": " + what + " array is NULL");
+    for (int r = 0; r < p->nranks; ++r) {
+        if (p->boxes[tensor][r].numel() == 0) continue;
+        if (!arr[r])
+            return fail(SHMM_ERR_NULL, std::string(fn) + ": " + what + "[" + std::to_string(r) + "] is NULL");
+        if (reinterpret_cast<uintptr_t>(arr[r]) % 16)
+            return fail(SHMM_ERR_ALIGN, std::string(fn) + ": " + what + "[" + std::to_string(r) +
+                                            "] is not 16-byte aligned");
+    }
+    return SHMM_OK;
+}
+
+shmm::GemmArgs gemm_args(const shmm_plan_t *p) {
+    shmm::GemmArgs g;
+    const shmm::Box &al = p->boxes[SHMM_TENSOR_A_LOCAL][0];
+    const shmm::Box &bl = p->boxes[SHMM_TENSOR_B_LOCAL][0];
+    g.M = al.ext[0];
+    g.Kd = al.ext[1];
+    g.N = bl.ext[1];
+    g.in_dt = p->in_dt;
+    return g;
+}
+
+int run_gemm(const shmm_plan_t *p, const shmm::GemmArgs &g, int *status, void *stream, std::string *msg) {
+    if (p->tensor_core && shmm::tcgen05_supported(g)) return shmm::launch_gemm_tcgen05(g, status, stream, msg);
+    return shmm::launch_gemm_simt(g, status, stream);
+}
+
+// Unfused local GEMMs of all ranks: out[r] = A[r] . B[r].
+int gemm_unfused(const shmm_plan_t *p, const void *const *A, const void *const *B, void *const *out,
+                 shmm_dtype_t out_dt, bool gelu, int *status, void *stream, std::string *msg) {
+    shmm::GemmArgs g = gemm_args(p);
+    g.units = p->nranks;
+    g.G = 1;
+    g.out_dt = out_dt;
+    g.gelu = gelu;
+    g.A = A;
+    g.B = B;
+    g.out = out;
+    return run_gemm(p, g, status, stream, msg);
+}
+
+// Reduction (standalone) from partial buffers to destinations.
+int reduce(const shmm_plan_t *p, const void *const *P, void *const *dst, int mode, int *status,
+           void *stream) {
+    const shmm::Groups &g = p->red_groups;
+    std::vector<const void *> src(g.members.size());
+    std::vector<void *> out(g.members.size());
+    for (size_t i = 0; i < g.members.size(); ++i) {
+        src[i] = P[g.members[i]];
+        out[i] = (mode == 2 || p->scatter_dim < 0) ? dst[g.members[i]] : dst[g.by_block[i]];
+    }
+    shmm::ReduceArgs a;
+    a.G = g.size;
+    a.ngroups = g.count;
+    a.rows = p->boxes[SHMM_TENSOR_P][0].ext[0];
+    a.cols = p->boxes[SHMM_TENSOR_P][0].ext[1];
+    a.mode = mode;
+    a.tree = (p->flags & SHMM_FLAG_TREE) != 0;
+    a.gelu = (p->flags & SHMM_FLAG_GELU) != 0;
+    a.pt = p->part_dt;
+    a.ot = p->out_dt;
+    a.src = src.data();
+    a.dst = out.data();
+    return shmm::launch_reduce(a, status, stream);
+}
+
+int gather(const shmm_plan_t *p, const shmm::Groups &g, int src_tensor, int64_t elem,
+           const void *const *shard, void *const *full, int *status, void *stream) {
+    std::vector<const void *> src(g.members.size());
+    std::vector<void *> dst(g.members.size());
+    for (size_t i = 0; i < g.members.size(); ++i) {
+        src[i] = shard[g.by_block[i]];
+        dst[i] = full[g.members[i]];
+    }
+    shmm::GatherArgs a;
+    a.G = g.size;
+    a.ngroups = g.count;
+    a.blocks0 = g.blocks0;
+    a.blocks1 = g.blocks1;
+    a.brows = p->boxes[src_tensor][0].ext[0];
+    a.bcols = p->boxes[src_tensor][0].ext[1];
+    a.elem = elem;
+    a.src = src.data();
+    a.dst = dst.data();
+    return shmm::launch_gather(a, status, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+shmm_status_t shmm_local_matmul(const shmm_plan_t *p, const void *const *A_r, const void *const *B_r,
+                                void *const *P_r, void *stream) {
+    static const char *fn = "shmm_local_matmul";
+    shmm::clear_error();
+    if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    shmm_status_t st;
+    if ((st = check_ptrs(p, A_r, SHMM_TENSOR_A_LOCAL, fn, "A_r")) != SHMM_OK) return st;
+    if ((st = check_ptrs(p, B_r, SHMM_TENSOR_B_LOCAL, fn, "B_r")) != SHMM_OK) return st;
+    if ((st = check_ptrs(p, (const void *const *)P_r, SHMM_TENSOR_P, fn, "P_r")) != SHMM_OK) return st;
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    const bool reduces = p->U.n > 0;
+    const shmm_dtype_t odt = reduces ? p->part_dt : p->out_dt;
+    const bool gelu = !reduces && (p->flags & SHMM_FLAG_GELU);
+    const int e = gemm_unfused(p, A_r, B_r, P_r, odt, gelu, status, stream, &err);
+    if (e) return cuda_fail(fn, e, err);
+    return SHMM_OK;
+}
+
+static shmm_status_t reduce_entry(const char *fn, const shmm_plan_t *p, const void *const *P_r,
+                                  void *const *C_r, void *stream, bool all_reduce) {
+    shmm::clear_error();
+    if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    if (p->U.n == 0)
+        return fail(SHMM_ERR_UNSUPPORTED, std::string(fn) + ": the plan has no partial sums to reduce");
+    if (p->flags & SHMM_FLAG_TREE && p->red_groups.size > 32)
+        return fail(SHMM_ERR_UNSUPPORTED, std::string(fn) + ": tree order supports groups of <= 32 ranks");
+    shmm_status_t st;
+    if ((st = check_ptrs(p, P_r, SHMM_TENSOR_P, fn, "P_r")) != SHMM_OK) return st;
+    int mode = 2;
+    int out_tensor = SHMM_TENSOR_P;
+    if (!all_reduce) {
+        if (p->scatter_dim >= 0) {
+            mode = p->scatter_dim;
+            out_tensor = SHMM_TENSOR_C_REDUCED;
+        } else {
+            mode = 0;  // all-reduce plan: rank q of the group takes row block q
+            if (p->boxes[SHMM_TENSOR_P][0].ext[0] % p->red_groups.size)
+                return fail(SHMM_ERR_SHAPE, std::string(fn) + ": rows do not split over the group");
+        }
+    }
+    if (!C_r) return fail(SHMM_ERR_NULL, std::string(fn) + ": C_r array is NULL");
+    for (int r = 0; r < p->nranks; ++r) {
+        if (p->boxes[out_tensor][r].numel() == 0) continue;
+        if (!C_r[r]) return fail(SHMM_ERR_NULL, std::string(fn) + ": C_r[" + std::to_string(r) + "] is NULL");
+        if (reinterpret_cast<uintptr_t>(C_r[r]) % 16)
+            return fail(SHMM_ERR_ALIGN, std::string(fn) + ": C_r[" + std::to_string(r) + "] is not 16-byte aligned");
+    }
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    // An all-reduce plan reduce-scattered by rows: owners in member order.
+    if (!all_reduce && p->scatter_dim < 0) {
+        const shmm::Groups &g = p->red_groups;
+        std::vector<const void *> src(g.members.size());
+        std::vector<void *> out(g.members.size());
+        for (size_t i = 0; i < g.members.size(); ++i) {
+            src[i] = P_r[g.members[i]];
+            out[i] = C_r[g.members[i]];
+        }
+        shmm::ReduceArgs a;
+        a.G = g.size;
+        a.ngroups = g.count;
+        a.rows = p->boxes[SHMM_TENSOR_P][0].ext[0];
+        a.cols = p->boxes[SHMM_TENSOR_P][0].ext[1];
+        a.mode = 0;
+        a.tree = (p->flags & SHMM_FLAG_TREE) != 0;
+        a.gelu = (p->flags & SHMM_FLAG_GELU) != 0;
+        a.pt = p->part_dt;
+        a.ot = p->out_dt;
+        a.src = src.data();
+        a.dst = out.data();
+        const int e = shmm::launch_reduce(a, status, stream);
+        if (e) return cuda_fail(fn, e);
+        return SHMM_OK;
+    }
+    const int e = reduce(p, P_r, C_r, mode, status, stream);
+    if (e) return cuda_fail(fn, e);
+    return SHMM_OK;
+}
+
+shmm_status_t shmm_reduce_scatter(const shmm_plan_t *p, const void *const *P_r, void *const *C_r,
+                                  void *stream) {
+    return reduce_entry("shmm_reduce_scatter", p, P_r, C_r, stream, false);
+}
+
+shmm_status_t shmm_all_reduce(const shmm_plan_t *p, const void *const *P_r, void *const *C_r,
+                              void *stream) {
+    return reduce_entry("shmm_all_reduce", p, P_r, C_r, stream, true);
+}
+
+shmm_status_t shmm_all_gather(const shmm_plan_t *p, int tensor, const void *const *shard_r,
+                              void *const *full_r, void *stream) {
+    static const char *fn = "shmm_all_gather";
+    shmm::clear_error();
+    if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    const shmm::Groups *g;
+    int src_t, dst_t;
+    int64_t elem;
+    if (tensor == SHMM_TENSOR_A) {
+        g = &p->gA_groups; src_t = SHMM_TENSOR_A; dst_t = SHMM_TENSOR_A_LOCAL;
+        elem = shmm::elem_bytes(p->in_dt);
+    } else if (tensor == SHMM_TENSOR_B) {
+        g = &p->gB_groups; src_t = SHMM_TENSOR_B; dst_t = SHMM_TENSOR_B_LOCAL;
+        elem = shmm::elem_bytes(p->in_dt);
+    } else if (tensor == SHMM_TENSOR_C) {
+        g = &p->gC_groups; src_t = SHMM_TENSOR_C_REDUCED; dst_t = SHMM_TENSOR_C;
+        elem = shmm::elem_bytes(p->out_dt);
+    } else {
+        return fail(SHMM_ERR_UNSUPPORTED, std::string(fn) + ": tensor must be A, B or C");
+    }
+    if (g->size == 1)
+        return fail(SHMM_ERR_UNSUPPORTED, std::string(fn) + ": the plan gathers nothing for this tensor");
+    shmm_status_t st;
+    if ((st = check_ptrs(p, shard_r, src_t, fn, "shard_r")) != SHMM_OK) return st;
+    if ((st = check_ptrs(p, (const void *const *)full_r, dst_t, fn, "full_r")) != SHMM_OK) return st;
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    const int e = gather(p, *g, src_t, elem, shard_r, full_r, status, stream);
+    if (e) return cuda_fail(fn, e);
+    return SHMM_OK;
+}
+
+shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void *const *B_r,
+                       void *const *C_r, void *workspace, size_t workspace_bytes, void *stream) {
+    static const char *fn = "shmm_run";
+    shmm::clear_error();
+    if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    shmm_status_t st;
+    if ((st = check_ptrs(p, A_r, SHMM_TENSOR_A, fn, "A_r")) != SHMM_OK) return st;
+    if ((st = check_ptrs(p, B_r, SHMM_TENSOR_B, fn, "B_r")) != SHMM_OK) return st;
+    if ((st = check_ptrs(p, (const void *const *)C_r, SHMM_TENSOR_C, fn, "C_r")) != SHMM_OK) return st;
+    size_t need = 0;
+    shmm_workspace_size(p, &need);
+    if (workspace_bytes < need)
+        return fail(SHMM_ERR_NOMEM, std::string(fn) + ": workspace of " + std::to_string(workspace_bytes) +
+                                        " bytes, " + std::to_string(need) + " needed");
+    if (need && !workspace) return fail(SHMM_ERR_NULL, std::string(fn) + ": workspace is NULL");
+    if (need && reinterpret_cast<uintptr_t>(workspace) % 256)
+        return fail(SHMM_ERR_ALIGN, std::string(fn) + ": workspace is not 256-byte aligned");
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+
+    // Carve the workspace: per-rank 256-byte-aligned slots.
+    char *ws = static_cast<char *>(workspace);
+    auto carve = [&](int tensor, int64_t elem, std::vector<void *> *slots) {
+        const size_t slot = (size_t)((p->boxes[tensor][0].numel() * elem + 255) / 256 * 256);
+        slots->resize(p->nranks);
+        for (int r = 0; r < p->nranks; ++r) {
+            (*slots)[r] = ws;
+            ws += slot;
+        }
+    };
+    const int64_t in_b = shmm::elem_bytes(p->in_dt), out_b = shmm::elem_bytes(p->out_dt);
+    std::vector<const void *> A_loc(A_r, A_r + p->nranks), B_loc(B_r, B_r + p->nranks);
+    std::vector<void *> wa, wb, wp, wc;
+    int e = 0;
+    if (p->gA.n) {
+        carve(SHMM_TENSOR_A_LOCAL, in_b, &wa);
+        e = gather(p, p->gA_groups, SHMM_TENSOR_A, in_b, A_r, wa.data(), status, stream);
+        if (e) return cuda_fail(fn, e, "gather A");
+        for (int r = 0; r < p->nranks; ++r) A_loc[r] = wa[r];
+    }
+    if (p->gB.n) {
+        carve(SHMM_TENSOR_B_LOCAL, in_b, &wb);
+        e = gather(p, p->gB_groups, SHMM_TENSOR_B, in_b, B_r, wb.data(), status, stream);
+        if (e) return cuda_fail(fn, e, "gather B");
+        for (int r = 0; r < p->nranks; ++r) B_loc[r] = wb[r];
+    }
+    const bool fused = p->fused;
+    if (p->U.n && !fused) carve(SHMM_TENSOR_P, shmm::elem_bytes(p->part_dt), &wp);
+    std::vector<void *> dst(C_r, C_r + p->nranks);
+    if (p->gC.n) {
+        carve(SHMM_TENSOR_C_REDUCED, out_b, &wc);
+        dst = wc;
+    }
+    const bool gelu = (p->flags & SHMM_FLAG_GELU) != 0;
+    if (!p->U.n) {
+        e = gemm_unfused(p, A_loc.data(), B_loc.data(), dst.data(), p->out_dt, gelu, status, stream, &err);
+        if (e) return cuda_fail(fn, e, err);
+    } else if (fused) {
+        const shmm::Groups &g = p->red_groups;
+        std::vector<const void *> fa(g.members.size()), fb(g.members.size());
+        std::vector<void *> fo(g.members.size());
+        for (size_t i = 0; i < g.members.size(); ++i) {
+            fa[i] = A_loc[g.members[i]];
+            fb[i] = B_loc[g.members[i]];
+            fo[i] = p->collective == SHMM_COLL_REDUCE_SCATTER ? dst[g.by_block[i]] : dst[g.members[i]];
+        }
+        shmm::GemmArgs ga = gemm_args(p);
+        ga.units = g.count;
+        ga.G = g.size;
+        ga.fused = true;
+        ga.mode = p->collective == SHMM_COLL_REDUCE_SCATTER ? p->scatter_dim : 2;
+        ga.gelu = gelu;
+        ga.out_dt = p->out_dt;
+        ga.A = fa.data();
+        ga.B = fb.data();
+        ga.out = fo.data();
+        e = run_gemm(p, ga, status, stream, &err);
+        if (e) return cuda_fail(fn, e, err);
+    } else {
+        e = gemm_unfused(p, A_loc.data(), B_loc.data(), wp.data(), p->part_dt, false, status, stream, &err);
+        if (e) return cuda_fail(fn, e, err);
+        const int mode = p->collective == SHMM_COLL_REDUCE_SCATTER ? p->scatter_dim : 2;
+        e = reduce(p, (const void *const *)wp.data(), dst.data(), mode, status, stream);
+        if (e) return cuda_fail(fn, e, "reduce");
+    }
+    if (p->gC.n) {
+        e = gather(p, p->gC_groups, SHMM_TENSOR_C_REDUCED, out_b, (const void *const *)wc.data(), C_r,
+                   status, stream);
+        if (e) return cuda_fail(fn, e, "gather C");
+    }
+    return SHMM_OK;
+}
+
+shmm_status_t shmm_sync_status(void *stream) {
+    shmm::clear_error();
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail("shmm_sync_status", e);
+    std::string err;
+    if (!status_ptr(&err)) return fail(SHMM_ERR_CUDA, "shmm_sync_status: " + err);
+    int v = 0;
+    e = cudaMemcpyFromSymbolAsync(&v, g_shmm_status_word, sizeof v, 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail("shmm_sync_status", e);
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_shmm_status_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail("shmm_sync_status", e);
+        return fail((shmm_status_t)v, "shmm_sync_status: a kernel reported " +
+                                          std::string(shmm_status_string((shmm_status_t)v)));
+    }
+    return SHMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,569 @@
+// Tensor-core local GEMM for sm_103a: every virtual rank's product
+// P_r = A_r . B_r over its slice of the contracted dim ("Sharded matrix
+// multiplication and result ownership", step 3; "Row Parallelism",
+// Z_i = X_i A_i), bf16 inputs, fp32 accumulation, optionally with the
+// partial-sum reduction fused into the epilogue (same page, step 4).
+//
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: per k-block, one 128x64 tile of A (K-major,
+//               128-byte swizzle) and BN/64 tiles of 64x64 of B (B is
+//               row-major [J,K], i.e. MN-major for the MMA: no transpose)
+//               into an S-stage shared-memory ring guarded by mbarriers;
+//   warp 1      allocates the 512 TMEM columns and issues tcgen05.mma
+//               (M=128, N=BN, K=16) from one thread, committing each stage
+//               back to the producer and each finished tile to the epilogue;
+//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator (warp w reads
+//               TMEM lanes 32*(w%4)..+31, one output row per thread), then
+//               GeLU / conversion / store.
+// Work units are (rank, m-tile, n-tile) or, fused, (group, m-tile, n-tile):
+// the G ranks of a reduction group are multiplied one after another into G
+// separate TMEM accumulators and the epilogue adds them in ascending rank
+// order in fp32, so the fused result equals the unfused partials summed by
+// the standalone reduction bit for bit.  Each output tile is written once,
+// to its owner (reduce-scatter) or to every member (all-reduce).
+//
+// Every mbarrier wait is bounded (~2 s of SM clock); on expiry the kernel
+// raises an abort flag, records SHMM_ERR_TIMEOUT in the device status word,
+// drains its own TMA loads and MMAs, frees TMEM and returns.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "shmm_internal.h"
+
+namespace {
+
+constexpr int BM = 128;          // rows per tile (TMEM lanes)
+constexpr int BK = 64;           // bf16 per k-block: one 128-byte swizzle row
+constexpr int UMMA_K = 16;       // K of one tcgen05.mma kind::f16
+constexpr int kMaxMaps = 16;     // rank operand pairs per launch
+constexpr int kThreads = 192;
+constexpr long long kWaitLimit = 4000000000LL;  // SM cycles (~2 s)
+
+struct TcK {
+    CUtensorMap tmA[kMaxMaps];
+    CUtensorMap tmB[kMaxMaps];
+    void *out[kMaxMaps];
+    int *status;
+    int units, G, mode;
+    int fused, gelu, out_f32;
+    int64_t M, N, Kd;
+    int m_tiles, n_tiles, k_blocks;
+};
+
+// ---- PTX wrappers ------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait.  Returns false if the abort flag is raised (by this or
+// another thread) or the wait outlives kWaitLimit, which raises it.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int *status, bool honour_abort = true) {
+    long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if (it == 0) t0 = clock64();
+        if ((it & 31) == 31) {
+            if (honour_abort && *abort_flag) return false;
+            if (clock64() - t0 > kWaitLimit) {
+                *abort_flag = 1;
+                atomicExch(status, (int)SHMM_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2),
+// descriptor version 1, base offset 0 (tiles are 1024-byte aligned).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A
+// K-major, B MN-major, N = bn, M = 128.
+__host__ __device__ constexpr uint32_t instr_desc(int bn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+        " [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float inner = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.0f + tanhf(inner));
+}
+
+// Stores n (<= 32) consecutive values of one row starting at `p` (element
+// pointer of type fp32 or bf16).  vec: whole 16-byte vectors are legal.
+__device__ __forceinline__ void store_run(void *p, const float *v, int n, bool f32, bool vec) {
+    if (f32) {
+        float *d = static_cast<float *>(p);
+        if (vec && n == 32) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4 *>(d + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+            for (int i = 0; i < n; ++i) d[i] = v[i];
+        }
+    } else {
+        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(p);
+        if (vec && n == 32) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[i + 2 * j], v[i + 2 * j + 1]);
+                    w[j] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+                *reinterpret_cast<uint4 *>(d + i) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        } else {
+            for (int i = 0; i < n; ++i) d[i] = __float2bfloat16_rn(v[i]);
+        }
+    }
+}
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;           // 16 KB
+    static constexpr int B_BYTES = BK * BN * 2;           // BN * 128
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcK k) {
+    using C = Cfg<BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *tiles = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::STAGE);
+    // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int Gq = k.fused ? k.G : 1;
+    const int nsets = (512 / (Gq * BN)) >= 2 ? 2 : 1;
+    const int tiles_per_unit = k.m_tiles * k.n_tiles;
+    const int total = k.units * tiles_per_unit;
+
+    auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+    auto empty_bar = [&](int s) { return smem_u32(&bars[S + s]); };
+    auto accf_bar = [&](int s) { return smem_u32(&bars[2 * S + s]); };
+    auto acce_bar = [&](int s) { return smem_u32(&bars[2 * S + 2 + s]); };
+    const uint32_t drain_bar = smem_u32(&bars[2 * S + 4]);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(accf_bar(s), 1);
+            mbar_init(acce_bar(s), 4 * 32);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_u32(tmem_holder))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    auto decode = [&](int t, int *unit, int *mt, int *nt) {
+        *unit = t / tiles_per_unit;
+        const int r = t - *unit * tiles_per_unit;
+        *mt = r % k.m_tiles;  // m fastest: neighbouring CTAs share a B column block
+        *nt = r / k.m_tiles;
+    };
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            for (int i = 0; i < k.units * Gq && i < kMaxMaps; ++i) {
+                prefetch_map(&k.tmA[i]);
+                prefetch_map(&k.tmB[i]);
+            }
+            uint32_t it = 0;
+            int last_parity[8];
+            for (int s = 0; s < 8; ++s) last_parity[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                int unit, mt, nt;
+                decode(t, &unit, &mt, &nt);
+                for (int q = 0; q < Gq && ok; ++q) {
+                    const int ri = unit * Gq + q;
+                    for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
+                        const int s = it % S;
+                        const uint32_t ph = (it / S) & 1;
+                        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, k.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(full_bar(s), C::STAGE);
+                        const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
+                        const uint32_t b_dst = a_dst + C::A_BYTES;
+                        tma_load_2d(a_dst, &k.tmA[ri], full_bar(s), kb * BK, mt * BM);
+#pragma unroll
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_2d(b_dst + c * 8192, &k.tmB[ri], full_bar(s), nt * BN + c * 64,
+                                        kb * BK);
+                        last_parity[s] = (int)ph;
+                    }
+                }
+            }
+            // Never leave a TMA write to shared memory in flight at exit.
+            for (int s = 0; s < S; ++s)
+                if (last_parity[s] >= 0)
+                    mbar_wait(full_bar(s), (uint32_t)last_parity[s], abort_flag, k.status, false);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = instr_desc(BN);
+            uint32_t it = 0;
+            int tile_iter = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_iter) {
+                const int set = tile_iter % nsets;
+                const uint32_t aph = (tile_iter / nsets) & 1;
+                if (!mbar_wait(acce_bar(set), aph ^ 1, abort_flag, k.status)) break;
+                fence_after();
+                for (int q = 0; q < Gq && ok; ++q) {
+                    const uint32_t d_tmem = tmem_base + (uint32_t)((set * Gq + q) * BN);
+                    for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
+                        const int s = it % S;
+                        const uint32_t ph = (it / S) & 1;
+                        if (!mbar_wait(full_bar(s), ph, abort_flag, k.status)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+                        const uint32_t a_addr = smem_u32(tiles + s * C::STAGE);
+                        const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            // A: K-major, advance 32 bytes per 16 k inside the
+                            // swizzle row.  B: MN-major, 16 k rows = 2 atoms.
+                            const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
+                            const uint64_t bd = smem_desc(b_addr + kk * 2048, 8192, 1024);
+                            umma_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(empty_bar(s));
+                    }
+                }
+                if (ok) umma_commit(accf_bar(set));
+            }
+            // Drain: every MMA issued by this thread has completed.
+            umma_commit(drain_bar);
+            mbar_wait(drain_bar, 0, abort_flag, k.status, false);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quad = warp % 4;
+        const int row_in_tile = quad * 32 + lane;
+        const bool f32 = k.out_f32 != 0;
+        const int64_t es = f32 ? 4 : 2;
+        int tile_iter = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_iter) {
+            int unit, mt, nt;
+            decode(t, &unit, &mt, &nt);
+            const int set = tile_iter % nsets;
+            const uint32_t aph = (tile_iter / nsets) & 1;
+            // One lane waits; the warp reconverges before the .sync.aligned
+            // TMEM loads.
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(accf_bar(set), aph, abort_flag, k.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            fence_after();
+            const int64_t row = (int64_t)mt * BM + row_in_tile;
+            const bool row_ok = row < k.M;
+            const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                tmem_ld32(lane_base + (uint32_t)(set * Gq * BN + c * 32), v);
+                for (int q = 1; q < Gq; ++q) {
+                    float w[32];
+                    tmem_ld32(lane_base + (uint32_t)((set * Gq + q) * BN + c * 32), w);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = v[i] + w[i];
+                }
+                if (k.gelu) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                }
+                const int64_t col0 = (int64_t)nt * BN + c * 32;
+                if (!row_ok || col0 >= k.N) continue;
+                const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
+                if (!k.fused) {
+                    char *p = (char *)k.out[unit] + (row * k.N + col0) * es;
+                    store_run(p, v, n, f32, true);
+                } else if (k.mode == 0) {
+                    const int64_t per = k.M / Gq;
+                    const int b = (int)(row / per);
+                    char *p = (char *)k.out[unit * Gq + b] + ((row - b * per) * k.N + col0) * es;
+                    store_run(p, v, n, f32, true);
+                } else if (k.mode == 1) {
+                    const int64_t per = k.N / Gq;
+                    const bool vec = (per % 32) == 0;
+                    if (vec) {
+                        const int b = (int)(col0 / per);
+                        char *p = (char *)k.out[unit * Gq + b] + (row * per + (col0 - b * per)) * es;
+                        store_run(p, v, n, f32, true);
+                    } else {
+                        for (int i = 0; i < n; ++i) {
+                            const int64_t col = col0 + i;
+                            const int b = (int)(col / per);
+                            char *p = (char *)k.out[unit * Gq + b] + (row * per + (col - b * per)) * es;
+                            store_run(p, v + i, 1, f32, false);
+                        }
+                    }
+                } else {
+                    for (int b = 0; b < Gq; ++b) {
+                        char *p = (char *)k.out[unit * Gq + b] + (row * k.N + col0) * es;
+                        store_run(p, v, n, f32, true);
+                    }
+                }
+            }
+            fence_before();
+            mbar_arrive(acce_bar(set));
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
+                     : "memory");
+    }
+}
+
+// ---- host side ----------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(std::string *msg) {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    static std::string err;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e =
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+            err = "cuTensorMapEncodeTiled not available from the driver";
+        else
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!fn && msg) *msg = err;
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major rows x cols matrix, box (bx inner, by).
+bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+              uint32_t bx, uint32_t by) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+    const cuuint32_t box[2] = {bx, by};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    return n;
+}
+
+template <int BN>
+cudaError_t launch_bn(TcK &k, cudaStream_t s) {
+    using C = Cfg<BN>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    k.n_tiles = (int)((k.N + BN - 1) / BN);
+    const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
+    const int grid = (int)(total < num_sms() ? total : num_sms());
+    gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, s>>>(k);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace shmm {
+
+bool tcgen05_supported(const GemmArgs &a) {
+    const int G = a.fused ? a.G : 1;
+    return a.in_dt == SHMM_BF16 && a.M > 0 && a.N > 0 && a.Kd > 0 && a.Kd % 8 == 0 &&
+           a.N % 8 == 0 && G <= 8 && a.M <= ((int64_t)1 << 31) && a.N <= ((int64_t)1 << 31) &&
+           a.Kd <= ((int64_t)1 << 31);
+}
+
+int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::string *msg) {
+    EncodeTiledFn fn = encode_fn(msg);
+    if (!fn) return (int)cudaErrorNotSupported;
+    const int G = a.fused ? a.G : 1;
+    const int bn = G == 1 ? 256 : (G == 2 ? 256 : (G <= 4 ? 128 : 64));
+    const int per_launch = kMaxMaps / G;  // units per launch
+    cudaStream_t s = (cudaStream_t)stream;
+    for (int u0 = 0; u0 < a.units; u0 += per_launch) {
+        const int nu = (a.units - u0) < per_launch ? (a.units - u0) : per_launch;
+        TcK k;
+        memset(&k, 0, sizeof k);
+        for (int i = 0; i < nu * G; ++i) {
+            const int gi = u0 * G + i;
+            if (!make_map(fn, &k.tmA[i], a.A[gi], a.M, a.Kd, BK, BM) ||
+                !make_map(fn, &k.tmB[i], a.B[gi], a.Kd, a.N, 64, BK)) {
+                if (msg) *msg = "cuTensorMapEncodeTiled rejected an operand";
+                return (int)cudaErrorInvalidValue;
+            }
+        }
+        const int nout = a.fused ? nu * G : nu;
+        for (int i = 0; i < nout; ++i) k.out[i] = a.out[(a.fused ? u0 * G : u0) + i];
+        k.status = status;
+        k.units = nu;
+        k.G = G;
+        k.mode = a.mode;
+        k.fused = a.fused ? 1 : 0;
+        k.gelu = a.gelu ? 1 : 0;
+        k.out_f32 = a.out_dt == SHMM_F32 ? 1 : 0;
+        k.M = a.M;
+        k.N = a.N;
+        k.Kd = a.Kd;
+        k.m_tiles = (int)((a.M + BM - 1) / BM);
+        k.k_blocks = (int)((a.Kd + BK - 1) / BK);
+        cudaError_t e;
+        switch (bn) {
+            case 256: e = launch_bn<256>(k, s); break;
+            case 128: e = launch_bn<128>(k, s); break;
+            default: e = launch_bn<64>(k, s); break;
+        }
+        if (e != cudaSuccess) return (int)e;
+    }
+    return 0;
+}
+
+}  // namespace shmm

@@ -1,0 +1,143 @@
+// Internal declarations shared by the host planner, the C-ABI glue and the
+// kernel launchers of libshmm.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/shmm.h"
+
+namespace shmm {
+
+// Ordered list of mesh axis indices splitting one array dim (first = major).
+struct AxisList {
+    int n = 0;
+    int ax[SHMM_MAX_AXES] = {};
+    bool contains(int a) const {
+        for (int i = 0; i < n; ++i)
+            if (ax[i] == a) return true;
+        return false;
+    }
+    void push(int a) { ax[n++] = a; }
+    bool operator==(const AxisList &o) const {
+        if (n != o.n) return false;
+        for (int i = 0; i < n; ++i)
+            if (ax[i] != o.ax[i]) return false;
+        return true;
+    }
+};
+
+struct Spec2 {
+    AxisList d[2];
+};
+
+// A box: offsets and extents of a rank's block in a global 2-D array.
+struct Box {
+    int64_t off[2];
+    int64_t ext[2];
+    int64_t numel() const { return ext[0] * ext[1]; }
+};
+
+// Ranks that exchange data in one collective, grouped.  Group g's members
+// are members[g*size .. g*size+size) in ascending rank id.
+struct Groups {
+    int size = 1;
+    int count = 0;
+    std::vector<int> members;
+    // Reduction: owner[g*size + b] = rank owning block b of the scattered dim.
+    // Gather: src_at[g*size + p] = rank whose block sits at grid position p
+    // (row-major over a blocks0 x blocks1 grid) of the gathered box.
+    std::vector<int> by_block;
+    int blocks0 = 1, blocks1 = 1;
+};
+
+}  // namespace shmm
+
+struct shmm_plan {
+    int naxes = 0;
+    int size[SHMM_MAX_AXES] = {};
+    int nranks = 1;
+    int64_t I = 0, J = 0, K = 0;
+    shmm_dtype_t in_dt = SHMM_BF16, out_dt = SHMM_BF16, part_dt = SHMM_F32;
+    uint32_t flags = 0;
+    shmm::Spec2 A, B, C;                      // as given
+    shmm::Spec2 A_loc, B_loc, nat, red, out;  // derived
+    shmm::AxisList U, gA, gB, gC;             // unreduced / gathered axes
+    int case_id = 1;
+    int collective = SHMM_COLL_NONE;
+    int scatter_dim = -1;
+    bool tensor_core = false;
+    // Reduction runs in the GEMM epilogue: SHMM_FLAG_FUSED, partial sums to
+    // reduce, and (on tensor cores) at most 8 ranks per group, the number of
+    // fp32 accumulators TMEM holds side by side.
+    bool fused = false;
+    std::vector<shmm::Box> boxes[7];          // [shmm_tensor_t][rank]
+    shmm::Groups red_groups, gA_groups, gB_groups, gC_groups;
+};
+
+namespace shmm {
+
+int64_t elem_bytes(shmm_dtype_t t);
+// Sets the calling thread's last-error message and returns `st`.
+shmm_status_t fail(shmm_status_t st, const std::string &msg);
+void clear_error();
+
+// ---- kernel launchers (device code in the .cu files) -------------------
+
+// Partial-sum reduction over groups of `G` ranks.  src[g*G+q]: group g's
+// q-th rank in ascending rank order, a rows x cols row-major buffer of
+// dtype `pt`.  mode 0 = reduce-scatter along dim 0, 1 = along dim 1, 2 =
+// all-reduce.  dst[g*G+b]: owner of block b (RS) or any member (AR), dtype
+// `ot`.  Returns a cudaError_t value (0 = success).
+struct ReduceArgs {
+    int G = 1, ngroups = 0;
+    int64_t rows = 0, cols = 0;
+    int mode = 2;
+    bool tree = false, gelu = false;
+    shmm_dtype_t pt = SHMM_F32, ot = SHMM_F32;
+    const void *const *src = nullptr;
+    void *const *dst = nullptr;
+};
+int launch_reduce(const ReduceArgs &a, int *status, void *stream);
+
+// All-gather over groups of G ranks: each member's dst buffer (full box,
+// blocks0*brows x blocks1*bcols) receives block p from src[g*G+p] (a brows x
+// bcols buffer).  dst[g*G+m] for every member m.
+struct GatherArgs {
+    int G = 1, ngroups = 0;
+    int blocks0 = 1, blocks1 = 1;
+    int64_t brows = 0, bcols = 0;
+    int64_t elem = 2;
+    const void *const *src = nullptr;
+    void *const *dst = nullptr;
+};
+int launch_gather(const GatherArgs &a, int *status, void *stream);
+
+// Local GEMMs.  For unit u (a rank, or a reduction group when fused), the
+// G operand pairs A[u*G+q] (M x Kd, row-major) and B[u*G+q] (Kd x N,
+// row-major) are multiplied.  Unfused (G == 1 per unit): out[u] = A.B.
+// Fused: the G products are summed in q order; mode 0/1 scatter along dim
+// 0/1 to out[u*G+b], mode 2 writes every out[u*G+b].
+struct GemmArgs {
+    int units = 0;          // ranks (unfused) or groups (fused)
+    int G = 1;              // ranks per unit
+    bool fused = false;
+    int mode = 2;           // fused write mode (0/1 RS dim, 2 AR)
+    bool gelu = false;
+    int64_t M = 0, N = 0, Kd = 0;
+    shmm_dtype_t in_dt = SHMM_BF16, out_dt = SHMM_F32;
+    const void *const *A = nullptr;
+    const void *const *B = nullptr;
+    void *const *out = nullptr;
+};
+int launch_gemm_simt(const GemmArgs &a, int *status, void *stream);
+bool tcgen05_supported(const GemmArgs &a);
+// Returns a cudaError_t value; sets *msg on a failure outside CUDA.
+int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::string *msg);
+
+// Device status word (set by kernels whose bounded waits expire).
+int device_status_ptr(int **ptr);  // cudaError_t value
+int device_status_read_clear(int *value, void *stream);
+
+}  // namespace shmm

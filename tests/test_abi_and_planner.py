@@ -1,0 +1,220 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/shmm.h declares, and its host planner agrees with the oracle's
+independent box logic on every mesh/sharding combination tried.  Argument
+checks and the injected-failure hook are exercised before any device call."""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def shmm():
+    from partial_sum_reduction_gb300 import build
+    build.build()
+    import partial_sum_reduction_gb300 as s
+    return s
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "shmm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(shmm_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(shmm):
+    names = declared_functions()
+    assert len(names) >= 15
+    L = ctypes.CDLL(shmm.shmm.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(shmm.shmm.EXPORTS)
+    assert shmm.shmm_version() == 100
+    assert shmm.lib().shmm_status_string(0) == b"SHMM_OK"
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    import partial_sum_reduction_gb300.shmm as m
+    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m, "LIB_PATH", "/nonexistent/libshmm.so")
+    with pytest.raises(RuntimeError):
+        m.lib()
+
+
+MESHES = {
+    "Y2": [("Y", 2)],
+    "XY22": [("X", 2), ("Y", 2)],
+    "XY42": [("X", 4), ("Y", 2)],
+    "X8": [("X", 8)],
+    "XYZ222": [("X", 2), ("Y", 2), ("Z", 2)],
+}
+
+
+def specs_for(mesh):
+    names = [n for n, _ in mesh]
+    dims = [()] + [(a,) for a in names] + [tuple(p) for p in itertools.permutations(names, 2)]
+    return dims
+
+
+def all_combos():
+    rng = np.random.default_rng(0)
+    out = []
+    for mname, mesh in MESHES.items():
+        dims = specs_for(mesh)
+        for _ in range(60):
+            sA = (dims[rng.integers(len(dims))], dims[rng.integers(len(dims))])
+            sB = (dims[rng.integers(len(dims))], dims[rng.integers(len(dims))])
+            sC = (dims[rng.integers(len(dims))], dims[rng.integers(len(dims))])
+            out.append((mname, sA, sB, sC))
+    # the workloads' own shardings
+    out += [("Y2", ((), ("Y",)), (("Y",), ()), (("Y",), ())),
+            ("XY22", (("X",), ()), ((), ("Y",)), (("X",), ("Y",))),
+            ("XY22", ((), ("X",)), ((), ()), ((), ())),
+            ("XY22", ((), ("Y",)), (("Y",), ()), (("Y",), ())),
+            ("XY22", (("X",), ()), ((), ("X",)), (("X",), ())),
+            ("X8", ((), ()), ((), ("X",)), ((), ("X",))),
+            ("X8", ((), ("X",)), (("X",), ()), ((), ())),
+            ("X8", ((), ("X",)), (("X",), ()), (("X",), ())),
+            ("XY42", (("X",), ("Y",)), (("Y",), ()), (("X",), ()))]
+    return out
+
+
+@pytest.mark.parametrize("mname,sA,sB,sC", all_combos())
+def test_planner_matches_oracle(shmm, mname, sA, sB, sC):
+    mesh = MESHES[mname]
+    I, J, K = 48, 96, 24
+    try:
+        oplan = oracle.plan_matmul(mesh, sA, sB, sC)
+        for spec, shape in ((sA, (I, J)), (sB, (J, K)), (sC, (I, K)), (oplan.reduced_C, (I, K))):
+            oracle.shard_box(mesh, spec, shape, 0)
+        oerr = None
+    except ValueError as e:
+        oerr = e
+    try:
+        p = shmm.Plan(mesh, sA, sB, sC, I, J, K, "bf16", "bf16")
+        perr = None
+    except shmm.ShmmError as e:
+        perr = e
+    assert (oerr is None) == (perr is None), (oerr, perr)
+    if oerr is not None:
+        return
+    info = p.info
+    assert info.case_id == oplan.case
+    assert shmm.shmm.COLLECTIVE_NAMES[info.collective] == oplan.collective
+    assert info.scatter_dim == oplan.scatter_dim
+    N = oracle.mesh_size(mesh)
+    T = shmm
+    for r in range(N):
+        for tensor, spec, shape in ((T.TENSOR_A, sA, (I, J)), (T.TENSOR_B, sB, (J, K)),
+                                    (T.TENSOR_C, sC, (I, K)), (T.TENSOR_P, oplan.natural_C, (I, K)),
+                                    (T.TENSOR_A_LOCAL, oplan.local_A, (I, J)),
+                                    (T.TENSOR_B_LOCAL, oplan.local_B, (J, K)),
+                                    (T.TENSOR_C_REDUCED, oplan.reduced_C, (I, K))):
+            assert p.rank_box(tensor, r) == oracle.shard_box(mesh, spec, shape, r), (tensor, r)
+        if info.group_size > 1:
+            assert p.group(r) == oracle.reduction_group(mesh, oplan, r)
+    pay = oracle.payload_bytes(mesh, sA, sB, sC, I, J, K, "bf16", "bf16")
+    assert info.payload_operand_ag == pay["operand_all_gather"]
+    assert info.payload_reduce_scatter == pay["reduce_scatter"]
+    assert info.payload_result_ag == pay["result_all_gather"]
+    assert info.flops_per_rank == oracle.local_flops(mesh, sA, sB, I, J, K)
+
+
+def test_worked_example_plan(shmm, golden):
+    g = golden("p2_worked_example.txt")
+    p = shmm.Plan("{Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 2, 2, 2, "f32", "f32")
+    assert p.info.payload_reduce_scatter == g["reduce_scatter_payload_bytes_per_rank"]
+    p = shmm.Plan("{Y:2}", "I,J_Y", "J_Y,K", "I,K", 2, 2, 2, "f32", "f32")
+    assert p.info.payload_reduce_scatter + p.info.payload_result_ag == g["payload_bytes_per_rank"]
+    assert (p.info.payload_reduce_scatter + p.info.payload_result_ag) * 2 == g["payload_bytes_total"]
+
+
+def test_down_projection_plan(shmm, golden):
+    g = golden("p4_down_projection.txt")
+    p = shmm.Plan("{X:4,Y:2}", "P('X','Y')", "P('Y',None)", "P('X',None)", 8192, 28672, 8192,
+                  "bf16", "bf16", shmm.FLAG_FUSED)
+    assert list(p.rank_box(shmm.TENSOR_A, 0)[1]) == g["A_shard"]
+    assert round(p.info.flops_per_rank / 1e9) == g["local_matmul_GFLOP"]
+    assert p.info.case_id == 3 and p.info.group_size == 2 and p.info.tensor_core == 1
+    assert p.info.fused == 1 and p.info.workspace_bytes == 0
+    _, ext = p.rank_box(shmm.TENSOR_C, 0)
+    assert round(ext[0] * ext[1] * 2 / 1e6, 1) == g["C_bytes_per_device_MB"]
+
+
+def test_spec_string_forms(shmm):
+    assert shmm.parse_spec("P(('X','Y'),None)") == (("X", "Y"), ())
+    assert shmm.parse_spec("P('X', 'Y')") == (("X",), ("Y",))
+    assert shmm.parse_spec("P()") == ((), ())
+    assert shmm.parse_spec("P(None,'Y')") == ((), ("Y",))
+    assert shmm.parse_spec("I_XY,J") == (("X", "Y"), ())
+    assert shmm.parse_mesh("{X:4,Y:2}") == [("X", 4), ("Y", 2)]
+
+
+@pytest.mark.parametrize("bad,code", [
+    (("{X:2}", "I_X,J_X", "J,K", "I,K", 4, 4, 4), "ERR_INVALID_SPEC"),
+    (("{X:2}", "I_X,J", "J,K_X", "I_X,K_X", 4, 4, 4), "ERR_ILLEGAL_OUTPUT"),
+    (("{X:2}", "I_Z,J", "J,K", "I,K", 4, 4, 4), "ERR_INVALID_SPEC"),
+    (("{X:2}", "I_X,J", "J,K", "I,K", 3, 4, 4), "ERR_SHAPE"),
+    (("{X:2}", "I,J", "J,K", "I,K", -1, 4, 4), "ERR_SHAPE"),
+    (("{X:2}", "I,J_X", "J_X,K", "I_X,K_X", 4, 4, 4), "ERR_ILLEGAL_OUTPUT"),
+    (("{X:2,Y:2}", "I,J_XY", "J_XY,K", "I_X,K_Y", 4, 4, 4), "ERR_INVALID_SPEC"),
+    (("{X:2,Y:2}", "I,J_X", "J_X,K", "I_Y,K", 4, 4, 4), "ERR_INVALID_SPEC"),
+    (("{X:300}", "I,J", "J,K", "I,K", 4, 4, 4), "ERR_SHAPE"),
+])
+def test_plan_rejections(shmm, bad, code):
+    with pytest.raises(shmm.ShmmError) as e:
+        shmm.Plan(*bad)
+    assert e.value.status == getattr(shmm.shmm, code)
+
+
+def test_argument_checks_before_any_device_call(shmm, monkeypatch):
+    """NULL, misaligned and undersized arguments, and the injected failure,
+    return their status without touching the GPU (this runs on CPU)."""
+    p = shmm.Plan("{Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 64, 64, 64, "bf16", "bf16")
+    L = shmm.lib()
+    PP = ctypes.c_void_p * 2
+    good = PP(0x10000, 0x20000)
+    bad_align = PP(0x10000, 0x20008)
+    nulls = PP(0, 0)
+    assert L.shmm_local_matmul(p.handle, None, good, good, None) == shmm.shmm.ERR_NULL
+    assert L.shmm_local_matmul(p.handle, nulls, good, good, None) == shmm.shmm.ERR_NULL
+    assert L.shmm_local_matmul(p.handle, good, bad_align, good, None) == shmm.shmm.ERR_ALIGN
+    assert b"16-byte" in L.shmm_last_error()
+    assert L.shmm_reduce_scatter(p.handle, good, bad_align, None) == shmm.shmm.ERR_ALIGN
+    assert L.shmm_all_gather(p.handle, shmm.TENSOR_A, good, good, None) == shmm.shmm.ERR_UNSUPPORTED
+    assert L.shmm_all_gather(p.handle, 9, good, good, None) == shmm.shmm.ERR_UNSUPPORTED
+    p1 = shmm.Plan("{Y:2}", "I_Y,J", "J,K", "I_Y,K", 64, 64, 64, "bf16", "bf16")
+    assert L.shmm_all_reduce(p1.handle, good, good, None) == shmm.shmm.ERR_UNSUPPORTED
+    pr = shmm.Plan("{Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 64, 64, 64, "bf16", "bf16")
+    assert pr.workspace_size() == 2 * 64 * 64 * 4
+    assert L.shmm_run(pr.handle, good, good, good, None, 0, None) == shmm.shmm.ERR_NOMEM
+    assert L.shmm_run(pr.handle, good, good, good, ctypes.c_void_p(0x100080), 1 << 20, None) == \
+        shmm.shmm.ERR_ALIGN
+    assert L.shmm_run(None, good, good, good, None, 0, None) == shmm.shmm.ERR_NULL
+    monkeypatch.setenv("SHMM_INJECT_FAIL", "shmm_run,shmm_all_reduce")
+    assert L.shmm_run(pr.handle, good, good, good, None, 0, None) == shmm.shmm.ERR_INJECTED
+    assert L.shmm_all_reduce(pr.handle, good, good, None) == shmm.shmm.ERR_INJECTED
+    assert b"injected" in L.shmm_last_error()
+    with pytest.raises(shmm.ShmmError) as e:
+        pr.run([0x10000, 0x20000], [0x10000, 0x20000], [0x10000, 0x20000], stream=0)
+    assert e.value.status == shmm.shmm.ERR_INJECTED
+
+
+def test_workspace_accounting(shmm):
+    # case 2: A gathered per rank; case 3 unfused: fp32 partials; fused: none
+    p = shmm.Plan("{X:2,Y:2}", "I,J_X", "J,K", "I,K", 256, 256, 128, "bf16", "bf16")
+    assert p.workspace_size() == 4 * 256 * 256 * 2
+    p = shmm.Plan("{X:2,Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 256, 256, 128, "bf16", "bf16")
+    assert p.workspace_size() == 4 * 256 * 128 * 4
+    p = shmm.Plan("{X:2,Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 256, 256, 128, "bf16", "bf16", shmm.FLAG_FUSED)
+    assert p.workspace_size() == 0 and p.info.fused == 1
+    # more than 8 ranks per group: the tensor-core path reduces unfused
+    p = shmm.Plan("{X:16}", "I,J_X", "J_X,K", "I,K", 256, 256, 128, "bf16", "bf16", shmm.FLAG_FUSED)
+    assert p.info.fused == 0 and p.workspace_size() == 16 * 256 * 128 * 4

@@ -1,0 +1,382 @@
+"""GPU parity: every step of the sharded matmul through the C-ABI against
+the CPU oracle on the same seeded inputs -- bit-exact for integer-valued
+fp32 and for the standalone reductions of given partials, within
+1e-2 * max|C_ref| for bf16 products."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import shmm_inputs
+from parity_util import BF16_TOL, F32P_TOL, compare, lib, oracle_run, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+Y2 = [("Y", 2)]
+XY22 = [("X", 2), ("Y", 2)]
+XY42 = [("X", 4), ("Y", 2)]
+X8 = [("X", 8)]
+
+
+@pytest.fixture(scope="module")
+def s():
+    assert torch.cuda.is_available()
+    return lib()
+
+
+# ------------------------------------------------- split-K integer, {Y:2}
+
+@pytest.mark.parametrize("flags", [0, "FUSED", "SIMT", "FUSED|SIMT", "TREE"])
+@pytest.mark.parametrize("sC", [(("Y",), ()), ((), ())])
+def test_split_k_integer_fp32_bit_exact(s, flags, sC):
+    fl = 0
+    for f in str(flags).split("|"):
+        fl |= getattr(s, "FLAG_" + f) if f != "0" else 0
+    A, B = shmm_inputs.split_k_integer(64, 64, 64, seed=0)
+    sA, sB = ((), ("Y",)), (("Y",), ())
+    plan, gpu = run_gpu(Y2, sA, sB, sC, A, B, "f32", "f32", fl)
+    _, ores = oracle_run(Y2, sA, sB, sC, A, B, "f32")
+    compare(plan, gpu, ores, exact=True)
+
+
+def test_worked_example_on_gpu(s, golden):
+    g = golden("p2_worked_example.txt")
+    A = torch.tensor(g["A"], dtype=torch.float32)
+    B = torch.tensor(g["B"], dtype=torch.float32)
+    from partial_sum_reduction_gb300 import helpers as H
+    # local partials, reduce-scatter by rows, all-gather back
+    p = s.Plan("{Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 2, 2, 2, "f32", "f32")
+    A_r, B_r = H.shard(p, s.TENSOR_A, A), H.shard(p, s.TENSOR_B, B)
+    P_r = H.alloc(p, s.TENSOR_P, fill=float("nan"))
+    p.local_matmul(A_r, B_r, P_r)
+    C_r = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+    p.reduce_scatter(P_r, C_r)
+    torch.cuda.synchronize()
+    assert P_r[0].cpu().tolist() == g["partial_rank0"]
+    assert P_r[1].cpu().tolist() == g["partial_rank1"]
+    assert C_r[0].cpu().tolist() == g["reduce_scatter_rank0"]
+    assert C_r[1].cpu().tolist() == g["reduce_scatter_rank1"]
+    # all-gather of the finished rows: a plan whose result is row-owned and
+    # requested whole
+    pg = s.Plan("{Y:2}", "I_Y,J", "J,K", "I,K", 2, 2, 2, "f32", "f32")
+    full = H.alloc(pg, s.TENSOR_C, fill=float("nan"))
+    pg.all_gather(s.TENSOR_C, C_r, full)
+    torch.cuda.synchronize()
+    for f in full:
+        assert f.cpu().tolist() == g["all_gather_every_rank"]
+    # all-reduce plan end to end, fused
+    pa = s.Plan("{Y:2}", "I,J_Y", "J_Y,K", "I,K", 2, 2, 2, "f32", "f32", s.FLAG_FUSED)
+    Ca = H.alloc(pa, s.TENSOR_C, fill=float("nan"))
+    pa.run(A_r, B_r, Ca)
+    torch.cuda.synchronize()
+    for c in Ca:
+        assert c.cpu().tolist() == g["all_gather_every_rank"]
+
+
+# --------------------------------------------- local GEMM (tensor cores)
+
+@pytest.mark.parametrize("M,Kd,N", [(128, 64, 256), (300, 200, 328), (520, 1032, 264), (7, 16, 8),
+                                    (256, 4096, 512), (129, 72, 1000)])
+def test_local_gemm_partials(s, M, Kd, N):
+    """Several tiles, ragged tails in all three dims, partial k-blocks."""
+    from partial_sum_reduction_gb300 import helpers as H
+    A, B = shmm_inputs.scaled_normal_pair(M, 2 * Kd, N, "bf16", seed=M + N)
+    p = s.Plan(Y2, ((), ("Y",)), (("Y",), ()), ((), ()), M, 2 * Kd, N, "bf16", "bf16")
+    assert p.info.tensor_core == 1
+    A_r, B_r = H.shard(p, s.TENSOR_A, A), H.shard(p, s.TENSOR_B, B)
+    P_r = H.alloc(p, s.TENSOR_P, fill=float("nan"))
+    p.local_matmul(A_r, B_r, P_r)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    _, parts = oracle.partials(Y2, ((), ("Y",)), (("Y",), ()), A.float().numpy(), B.float().numpy(),
+                               nthreads=8)
+    for r in range(2):
+        ref = parts[r][1]
+        got = P_r[r].cpu().numpy()
+        assert not np.isnan(got).any()
+        err = np.abs(got.astype(np.float64) - ref).max()
+        assert err <= F32P_TOL * np.abs(ref).max(), (r, err)
+
+
+def test_tensor_core_agrees_with_cuda_cores(s):
+    A, B = shmm_inputs.scaled_normal_pair(384, 512, 264, "bf16", seed=9)
+    sA, sB, sC = ((), ("Y",)), (("Y",), ()), (("Y",), ())
+    p1, g1 = run_gpu(Y2, sA, sB, sC, A, B, "bf16", "f32")
+    p2, g2 = run_gpu(Y2, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_SIMT)
+    assert p1.info.tensor_core == 1 and p2.info.tensor_core == 0
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(a.numpy(), b.numpy(), rtol=0, atol=1e-4 * float(b.abs().max()))
+
+
+# ---------------------------------------- four-case sweep, mesh {X:2,Y:2}
+
+FOUR = [
+    (1, (("X",), ()), ((), ("Y",)), (("X",), ("Y",))),
+    (2, ((), ("X",)), ((), ()), ((), ())),
+    (3, ((), ("Y",)), (("Y",), ()), (("Y",), ())),
+    (4, (("X",), ()), ((), ("X",)), (("X",), ())),
+]
+
+
+@pytest.mark.parametrize("case,sA,sB,sC", FOUR)
+@pytest.mark.parametrize("fused", [False, True])
+def test_four_cases(s, case, sA, sB, sC, fused):
+    A, B = shmm_inputs.scaled_normal_pair(512, 384, 640, "bf16", seed=case)
+    plan, gpu = run_gpu(XY22, sA, sB, sC, A, B, "bf16", "bf16", s.FLAG_FUSED if fused else 0)
+    assert plan.info.case_id == case
+    oplan, ores = oracle_run(XY22, sA, sB, sC, A, B, "bf16")
+    compare(plan, gpu, ores, exact=False)
+
+
+@pytest.mark.parametrize("case,sA,sB,sC", FOUR)
+def test_four_cases_full_size_sampled(s, case, sA, sB, sC):
+    """I=J=K=2048, N(0,1)/sqrt(J), bf16: every output row sampled in every
+    rank's block is checked against the oracle."""
+    A, B = shmm_inputs.scaled_normal_pair(2048, 2048, 2048, "bf16", seed=0)
+    plan, gpu = run_gpu(XY22, sA, sB, sC, A, B, "bf16", "bf16", s.FLAG_FUSED)
+    rows = list(range(0, 2048, 97)) + [1023, 1024, 2047]
+    _, ores = oracle_run(XY22, sA, sB, sC, A, B, "bf16", rows=rows)
+    compare(plan, gpu, ores, exact=False, rows=rows)
+
+
+# ------------------------------------------------------- ownership paths
+
+@pytest.mark.parametrize("sC", [(("X", "Y"), ()), (("X",), ()), ((), ()), (("X",), ("Y",))])
+@pytest.mark.parametrize("flags", [0, "FUSED", "TREE"])
+def test_down_projection_layout_small(s, sC, flags):
+    """A[I_X,J_Y].B[J_Y,K] on {X:4,Y:2}: all-reduce, reduce-scatter onto I
+    and K, and all-gather of the result."""
+    fl = 0 if flags == 0 else getattr(s, "FLAG_" + flags)
+    A, B = shmm_inputs.scaled_normal_pair(1024, 1024, 512, "bf16", seed=4)
+    sA, sB = (("X",), ("Y",)), (("Y",), ())
+    plan, gpu = run_gpu(XY42, sA, sB, sC, A, B, "bf16", "bf16", fl)
+    _, ores = oracle_run(XY42, sA, sB, sC, A, B, "bf16", order="pairwise" if flags == "TREE" else "sequential")
+    compare(plan, gpu, ores, exact=False)
+
+
+@pytest.mark.slow
+def test_down_projection_full_size_sampled(s):
+    A, B = shmm_inputs.scaled_normal_pair(8192, 28672, 8192, "bf16", seed=0)
+    sA, sB, sC = (("X",), ("Y",)), (("Y",), ()), (("X",), ())
+    plan, gpu = run_gpu(XY42, sA, sB, sC, A, B, "bf16", "bf16", s.FLAG_FUSED)
+    rows = [0, 1, 2047, 2048, 4100, 6143, 6144, 8191]
+    _, ores = oracle_run(XY42, sA, sB, sC, A, B, "bf16", rows=rows)
+    compare(plan, gpu, ores, exact=False, rows=rows)
+
+
+# ------------------------------------------------- MLP column -> row pair
+
+def _mlp(s, T, D, F, sY, fused, rows=None):
+    from partial_sum_reduction_gb300 import helpers as H
+    X, W1, W2 = shmm_inputs.mlp_pair(T, D, F, seed=0)
+    fl = s.FLAG_FUSED if fused else 0
+    p1 = s.Plan(X8, ((), ()), ((), ("X",)), ((), ("X",)), T, D, F, "bf16", "bf16", s.FLAG_GELU)
+    X_r, W1_r = H.shard(p1, s.TENSOR_A, X), H.shard(p1, s.TENSOR_B, W1)
+    H_r = H.alloc(p1, s.TENSOR_C, fill=float("nan"))
+    p1.run(X_r, W1_r, H_r, H.workspace(p1))
+    p2 = s.Plan(X8, ((), ("X",)), (("X",), ()), sY, T, F, D, "bf16", "bf16", fl)
+    W2_r = H.shard(p2, s.TENSOR_B, W2)
+    Y_r = H.alloc(p2, s.TENSOR_C, fill=float("nan"))
+    p2.run(H_r, W2_r, Y_r, H.workspace(p2))   # H feeds the row-parallel GEMM as is
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    # oracle: same chain on the oracle's own H
+    Xn, W1n, W2n = X.float().numpy(), W1.float().numpy(), W2.float().numpy()
+    _, hres = oracle.sharded_matmul(X8, ((), ()), ((), ("X",)), ((), ("X",)), Xn, W1n, out_dtype="bf16",
+                                    gelu=True, rows=rows, nthreads=8)
+    Hn = np.zeros((T, F), np.float32)
+    for r, v in hres.items():
+        if rows is None:
+            (i0, k0), blk = v
+            Hn[i0:i0 + blk.shape[0], k0:k0 + blk.shape[1]] = blk
+        else:
+            crow, k0, blk = v
+            Hn[np.asarray(crow), k0:k0 + blk.shape[1]] = blk
+    _, yres = oracle.sharded_matmul(X8, ((), ("X",)), (("X",), ()), sY, Hn, W2n, out_dtype="bf16",
+                                    rows=rows, nthreads=8)
+    # H parity (bf16 activations)
+    hmax = float(np.abs(Hn).max())
+    for r in range(8):
+        (i0, k0), ext = p1.rank_box(s.TENSOR_C, r)
+        got = H_r[r].float().cpu().numpy()
+        ref = Hn[i0:i0 + ext[0], k0:k0 + ext[1]]
+        if rows is not None:
+            got, ref = got[np.asarray(rows)], ref[np.asarray(rows)]
+        assert np.abs(got - ref).max() <= BF16_TOL * hmax
+    compare(p2, [y.cpu() for y in Y_r], yres, exact=False, rows=rows)
+
+
+@pytest.mark.parametrize("sY", [((), ()), (("X",), ())])
+@pytest.mark.parametrize("fused", [False, True])
+def test_mlp_pair_small(s, sY, fused):
+    _mlp(s, 384, 256, 1024, sY, fused)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("sY", [((), ()), (("X",), ())])
+def test_mlp_pair_full_size_sampled(s, sY):
+    _mlp(s, 8192, 4096, 16384, sY, True, rows=[0, 1, 1023, 1024, 5000, 8191])
+
+
+# -------------------------------------------- collectives on given partials
+
+@pytest.mark.parametrize("G", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("order", ["sequential", "pairwise"])
+@pytest.mark.parametrize("numel", [1 << 16, 4099 * 8])
+def test_collectives_bit_exact(s, G, dtype, order, numel):
+    """Reduce-scatter, all-reduce and all-gather of given partial buffers
+    ({X:G}), bit for bit against the oracle in the same order."""
+    from partial_sum_reduction_gb300 import helpers as H
+    cols = 64 if numel % (64 * G) == 0 else 8
+    rows = numel // cols
+    if rows % G:
+        rows -= rows % G
+    bufs = [b[:rows * cols].reshape(rows, cols) for b in shmm_inputs.partial_buffers(G, numel, dtype, seed=G)]
+    fl = s.FLAG_PARTIAL_OUT_DTYPE | (s.FLAG_TREE if order == "pairwise" else 0)
+    mesh = [("X", G)]
+    p_rs = s.Plan(mesh, ((), ("X",)), (("X",), ()), (("X",), ()), rows, G, cols, dtype, dtype, fl)
+    p_ar = s.Plan(mesh, ((), ("X",)), (("X",), ()), ((), ()), rows, G, cols, dtype, dtype, fl)
+    P_r = [b.cuda() for b in bufs]
+    rs = H.alloc(p_rs, s.TENSOR_C, fill=float("nan"))
+    ar = H.alloc(p_ar, s.TENSOR_C, fill=float("nan"))
+    p_rs.reduce_scatter(P_r, rs)
+    p_ar.all_reduce(P_r, ar)
+    pg = s.Plan(mesh, (("X",), ()), ((), ()), ((), ()), rows, 8, cols, dtype, dtype)
+    ag = H.alloc(pg, s.TENSOR_C, fill=float("nan"))
+    pg.all_gather(s.TENSOR_C, rs, ag)
+    torch.cuda.synchronize()
+    ref_rs = oracle.collective_reduce([b.float().numpy() for b in bufs], "reduce_scatter", dtype, order=order)
+    ref_ar = oracle.collective_reduce([b.float().numpy() for b in bufs], "all_reduce", dtype, order=order)
+    for q in range(G):
+        np.testing.assert_array_equal(rs[q].float().cpu().numpy(), ref_rs[q])
+        np.testing.assert_array_equal(ar[q].float().cpu().numpy(), ref_ar[q])
+        # AllReduce = ReduceScatter + AllGather, bit for bit
+        np.testing.assert_array_equal(ag[q].float().cpu().numpy(), ref_ar[q])
+
+
+@pytest.mark.parametrize("G", [2, 3, 4])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("order", ["sequential", "pairwise"])
+def test_collectives_scalar_path(s, G, dtype, order):
+    """Owner blocks that are not whole 16-byte vectors (odd row width)."""
+    from partial_sum_reduction_gb300 import helpers as H
+    rows, cols = 12, 5
+    bufs = [b.reshape(rows, cols) for b in shmm_inputs.partial_buffers(G, rows * cols, dtype, seed=7)]
+    fl = s.FLAG_PARTIAL_OUT_DTYPE | (s.FLAG_TREE if order == "pairwise" else 0)
+    mesh = [("X", G)]
+    p = s.Plan(mesh, ((), ("X",)), (("X",), ()), (("X",), ()), rows, G, cols, dtype, dtype, fl)
+    pa = s.Plan(mesh, ((), ("X",)), (("X",), ()), ((), ()), rows, G, cols, dtype, dtype, fl)
+    rs = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+    ar = H.alloc(pa, s.TENSOR_C, fill=float("nan"))
+    P_r = [b.cuda() for b in bufs]
+    p.reduce_scatter(P_r, rs)
+    pa.all_reduce(P_r, ar)
+    torch.cuda.synchronize()
+    host = [b.float().numpy() for b in bufs]
+    ref_rs = oracle.collective_reduce(host, "reduce_scatter", dtype, order=order)
+    ref_ar = oracle.collective_reduce(host, "all_reduce", dtype, order=order)
+    for q in range(G):
+        np.testing.assert_array_equal(rs[q].float().cpu().numpy(), ref_rs[q])
+        np.testing.assert_array_equal(ar[q].float().cpu().numpy(), ref_ar[q])
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_reduce_scatter_onto_columns(s, G):
+    from partial_sum_reduction_gb300 import helpers as H
+    rows, cols = 96, 40 * G
+    bufs = [b.reshape(rows, cols) for b in shmm_inputs.partial_buffers(G, rows * cols, "f32", seed=3)]
+    mesh = [("X", G)]
+    p = s.Plan(mesh, ((), ("X",)), (("X",), ()), ((), ("X",)), rows, G, cols, "f32", "bf16")
+    out = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+    p.reduce_scatter([b.cuda() for b in bufs], out)
+    torch.cuda.synchronize()
+    ref = oracle.collective_reduce([b.numpy() for b in bufs], "reduce_scatter", "bf16", scatter_dim=1)
+    for q in range(G):
+        np.testing.assert_array_equal(out[q].float().cpu().numpy(), ref[q])
+
+
+def test_operand_all_gather_bit_exact(s):
+    from partial_sum_reduction_gb300 import helpers as H
+    A, B = shmm_inputs.scaled_normal_pair(256, 512, 264, "bf16", seed=1)
+    # case 2 gathers A along J; case 4 gathers B along K
+    cases = [(((), ("X",)), ((), ()), s.TENSOR_A, s.TENSOR_A_LOCAL, A),
+             ((("X",), ()), ((), ("X",)), s.TENSOR_B, s.TENSOR_B_LOCAL, B)]
+    for sA, sB, t, tloc, full in cases:
+        p = s.Plan(XY22, sA, sB, ((), ()), 256, 512, 264, "bf16", "bf16")
+        shards = H.shard(p, t, full)
+        loc = H.alloc(p, tloc)
+        p.all_gather(t, shards, loc)
+        torch.cuda.synchronize()
+        for r in range(4):
+            (o0, o1), ext = p.rank_box(tloc, r)
+            assert torch.equal(loc[r].cpu(), full[o0:o0 + ext[0], o1:o1 + ext[1]])
+
+
+# -------------------------------------------------------------- invariants
+
+def test_fused_equals_unfused_bitwise(s):
+    A, B = shmm_inputs.scaled_normal_pair(640, 1024, 512, "bf16", seed=12)
+    for mesh, sA, sB, sC in ((Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ())),
+                             (XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ())),
+                             ([("X", 4)], ((), ("X",)), (("X",), ()), ((), ("X",)))):
+        _, g1 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32")
+        p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED)
+        assert p2.info.fused == 1
+        for a, b in zip(g1, g2):
+            assert torch.equal(a, b)
+
+
+def test_all_reduce_replicas_identical(s):
+    A, B = shmm_inputs.scaled_normal_pair(256, 2048, 384, "bf16", seed=2)
+    plan, gpu = run_gpu(X8, ((), ("X",)), (("X",), ()), ((), ()), A, B, "bf16", "bf16", s.FLAG_FUSED)
+    for g in gpu[1:]:
+        assert torch.equal(g, gpu[0])
+
+
+# -------------------------------------------------------------- edge cases
+
+def test_empty_contraction_gives_zero(s):
+    A = torch.zeros(64, 0, dtype=torch.float32)
+    B = torch.zeros(0, 32, dtype=torch.float32)
+    plan, gpu = run_gpu(Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, "f32", "f32")
+    for g in gpu:
+        assert torch.equal(g, torch.zeros_like(g))
+
+
+def test_empty_output_is_a_no_op(s):
+    A = torch.ones(0, 16, dtype=torch.bfloat16)
+    B = torch.ones(16, 8, dtype=torch.bfloat16)
+    plan, gpu = run_gpu(Y2, ((), ("Y",)), (("Y",), ()), ((), ()), A, B, "bf16", "bf16")
+    assert all(g.numel() == 0 for g in gpu)
+
+
+@pytest.mark.parametrize("I,J,K", [(1, 2, 1), (3, 6, 5), (17, 10, 9), (130, 14, 70)])
+def test_ragged_shapes_off_the_tensor_core_path(s, I, J, K):
+    A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=I)
+    plan, gpu = run_gpu(Y2, ((), ("Y",)), (("Y",), ()), ((), ()), A, B, "bf16", "bf16", s.FLAG_FUSED)
+    _, ores = oracle_run(Y2, ((), ("Y",)), (("Y",), ()), ((), ()), A, B, "bf16")
+    compare(plan, gpu, ores, exact=False)
+
+
+def test_outputs_stay_inside_their_boxes(s):
+    """Canary-filled guard regions around every rank's output slice of one
+    allocation stay untouched."""
+    from partial_sum_reduction_gb300 import helpers as H
+    A, B = shmm_inputs.scaled_normal_pair(384, 512, 200, "bf16", seed=5)
+    for flags in (0, s.FLAG_FUSED):
+        p = s.Plan(XY42, (("X",), ("Y",)), (("Y",), ()), (("X", "Y"), ()), 384, 512, 200, "bf16", "bf16",
+                   flags)
+        A_r, B_r = H.shard(p, s.TENSOR_A, A), H.shard(p, s.TENSOR_B, B)
+        _, ext = p.rank_box(s.TENSOR_C, 0)
+        n = ext[0] * ext[1]
+        guard = 4096
+        pool = torch.full((8 * (n + 2 * guard),), -7.0, dtype=torch.bfloat16, device="cuda")
+        C_r = [pool[r * (n + 2 * guard) + guard: r * (n + 2 * guard) + guard + n].view(ext) for r in range(8)]
+        p.run(A_r, B_r, C_r, H.workspace(p))
+        torch.cuda.synchronize()
+        host = pool.cpu()
+        for r in range(8):
+            base = r * (n + 2 * guard)
+            assert torch.all(host[base:base + guard] == -7.0)
+            assert torch.all(host[base + guard + n:base + 2 * guard + n] == -7.0)
