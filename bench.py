@@ -1,0 +1,573 @@
+#!/usr/bin/env python
+"""Throughput of the sharded matmul hot path on GB300.
+
+Default workload: the tensor-parallel down-projection of "Sharded matmuls and
+collectives on a torus" (the sharding sandbox's default case 3): A[8192,28672]
+. B[28672,8192] bf16 on mesh {X:4,Y:2}, A[I_X,J_Y], B[J_Y,K], result C[I_X,K]
+(all-reduce over Y), entries N(0,1)/sqrt(28672).  Each of the 8 virtual ranks
+multiplies a [2048,14336].[14336,8192] shard (481 GFLOP) and the partial sums
+are reduced in the GEMM epilogue.  One step = one shmm_run over the whole
+mesh (plan built once, outside the timed region).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl shmm|reference]
+        [--workload down_projection|four_case|mlp_pair|split_k_integer]
+        python bench.py --sweep collectives     (reduce-scatter / all-reduce /
+                                                 all-gather bandwidth sweep)
+Under torchrun (N > 1) every GPU runs its own replica of the workload (the
+virtual-rank mesh lives on one GPU); the reported value is the work of all
+replicas over the slowest replica's time (weak scaling).
+
+Prints one JSON line (rank 0).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("sharded-matmul TFLOP/s (% bf16 peak) and reduce-scatter GB/s (% HBM) on 1 GB300")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOADS = {
+    "down_projection": dict(
+        mesh=[("X", 4), ("Y", 2)], sA=(("X",), ("Y",)), sB=(("Y",), ()), sC=(("X",), ()),
+        I=8192, J=28672, K=8192, fused=True,
+        text="tensor-parallel down-projection A[8192,28672].B[28672,8192] bf16 on {X:4,Y:2}, "
+             "A[I_X,J_Y], B[J_Y,K] -> C[I_X,K] (all-reduce over Y fused into the GEMM epilogue)"),
+    "four_case": dict(
+        mesh=[("X", 2), ("Y", 2)], I=2048, J=2048, K=2048, fused=True,
+        text="four-case sweep I=J=K=2048 bf16 on {X:2,Y:2} (cases 1-4 back to back)"),
+    "mlp_pair": dict(
+        mesh=[("X", 8)], T=8192, D=4096, F=16384, fused=True,
+        text="MLP column->row pair X[8192,4096].W1[4096,16384] (GeLU) .W2[16384,4096] bf16 on {X:8}, "
+             "all-reduce of Y fused"),
+    "split_k_integer": dict(
+        mesh=[("Y", 2)], I=64, J=64, K=64, fused=True,
+        text="split-K integer fp32 A[64,64].B[64,64] on {Y:2}, reduce-scatter C[I_Y,K]"),
+}
+FOUR_CASES = [
+    ((("X",), ()), ((), ("Y",)), (("X",), ("Y",))),
+    (((), ("X",)), ((), ()), ((), ())),
+    (((), ("Y",)), (("Y",), ()), (("Y",), ())),
+    ((("X",), ()), ((), ("X",)), (("X",), ())),
+]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"]))}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of the SM clock and throttle reasons; only samples
+    stamped inside [mark_start, mark_end] count."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, bus_id=None, interval_ms=50):
+        self.proc = None
+        self.t_start = self.t_end = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", str(interval_ms)]
+        if bus_id:
+            cmd += ["-i", bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    @staticmethod
+    def _ts(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = []
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((self._ts(parts[0]), float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.out.name)
+        inside = [r for r in rows if r[0] is not None and self.t_start is not None and
+                  self.t_start - 0.05 <= r[0] <= self.t_end + 0.05]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "whole run (no sample fell inside the timed region)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        reasons = sorted({self.NAMES[i] for r in inside for i, f in enumerate(r[3]) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------- workloads
+
+class Workload:
+    """Plans, per-rank device buffers and pinned host copies of one workload;
+    ``step()`` enqueues one pass of the hot path."""
+
+    def __init__(self, name, device):
+        import torch
+        import partial_sum_reduction_gb300 as s
+        import shmm_inputs
+        from partial_sum_reduction_gb300 import helpers as H
+        self.name, self.cfg = name, WORKLOADS[name]
+        self.s, self.H, self.torch = s, H, torch
+        c = self.cfg
+        self.steps_spec = []   # (plan, A list, B list, C list, ws)
+        self.flops = 0
+        if name == "down_projection":
+            A, B = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
+            self.host_globals = (A, B)
+            self._add(c["mesh"], c["sA"], c["sB"], c["sC"], A, B, s.FLAG_FUSED if c["fused"] else 0, device)
+        elif name == "four_case":
+            A, B = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
+            self.host_globals = (A, B)
+            for sA, sB, sC in FOUR_CASES:
+                self._add(c["mesh"], sA, sB, sC, A, B, s.FLAG_FUSED, device)
+        elif name == "mlp_pair":
+            X, W1, W2 = shmm_inputs.mlp_pair(c["T"], c["D"], c["F"], seed=0)
+            self.host_globals = (X, W1, W2)
+            p1 = self._add(c["mesh"], ((), ()), ((), ("X",)), ((), ("X",)), X, W1, s.FLAG_GELU, device)
+            H_r = self.steps_spec[0][3]
+            p2 = s.Plan(c["mesh"], ((), ("X",)), (("X",), ()), ((), ()), c["T"], c["F"], c["D"], "bf16", "bf16",
+                        s.FLAG_FUSED)
+            W2_r = H.shard(p2, s.TENSOR_B, W2, device)
+            Y_r = H.alloc(p2, s.TENSOR_C, device)
+            self.steps_spec.append((p2, H_r, W2_r, Y_r, H.workspace(p2, device)))
+            self.flops += p2.info.flops_per_rank * p2.nranks
+        elif name == "split_k_integer":
+            A, B = shmm_inputs.split_k_integer(c["I"], c["J"], c["K"], seed=0)
+            self.host_globals = (A, B)
+            self._add(c["mesh"], ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, s.FLAG_FUSED, device,
+                      dt="f32")
+        torch.cuda.synchronize()
+
+    def _add(self, mesh, sA, sB, sC, A, B, flags, device, dt="bf16"):
+        s, H = self.s, self.H
+        I, J = A.shape
+        K = B.shape[1]
+        p = s.Plan(mesh, sA, sB, sC, I, J, K, dt, dt, flags)
+        A_r, B_r = H.shard(p, s.TENSOR_A, A, device), H.shard(p, s.TENSOR_B, B, device)
+        C_r = H.alloc(p, s.TENSOR_C, device)
+        self.steps_spec.append((p, A_r, B_r, C_r, H.workspace(p, device)))
+        self.flops += p.info.flops_per_rank * p.nranks
+        return p
+
+    def step(self, stream):
+        for p, A_r, B_r, C_r, ws in self.steps_spec:
+            p.run(A_r, B_r, C_r, ws, stream=stream)
+
+    def input_bytes(self):
+        n = 0
+        for i, (p, A_r, B_r, C_r, ws) in enumerate(self.steps_spec):
+            if self.name == "mlp_pair" and i == 1:
+                n += sum(t.numel() * t.element_size() for t in B_r)
+                continue
+            n += sum(t.numel() * t.element_size() for t in A_r + B_r)
+        return n
+
+    def output_tensors(self):
+        if self.name == "mlp_pair":
+            return self.steps_spec[-1][3]
+        out = []
+        for p, A_r, B_r, C_r, ws in self.steps_spec:
+            out += C_r
+        return out
+
+    def input_tensors(self):
+        out = []
+        for i, (p, A_r, B_r, C_r, ws) in enumerate(self.steps_spec):
+            if self.name == "mlp_pair" and i == 1:
+                out += B_r
+            else:
+                out += A_r + B_r
+        return out
+
+
+def time_device(wl, steps, warmup, dist_ctx):
+    """Device-timed loop: CUDA events on the launching stream, one pair per
+    step; inputs (>> L2 for the full-size workloads) stay resident."""
+    import torch
+    s = wl.s
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    s.shmm_sync_status(stream)
+    dist_ctx.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(torch.cuda.current_device()).pci_bus_id
+    except Exception:
+        pass
+    sampler = ClockSampler(bus_id=_smi_bus_id(bus))
+    time.sleep(0.3)
+    launches0 = s.shmm_kernel_launches()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark_start()
+    t0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        wl.step(stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    launches = s.shmm_kernel_launches() - launches0
+    clocks = sampler.stop()
+    s.shmm_sync_status(stream)
+    total_ms = t0.elapsed_time(t1)
+    per_step = [a.elapsed_time(b) for a, b in ev]
+    total_ms = dist_ctx.max(total_ms)
+    return total_ms, per_step, launches, clocks
+
+
+def _smi_bus_id(bus):
+    if not bus:
+        return None
+    # torch reports e.g. "0000:1B:00.0"; nvidia-smi accepts "00000000:1B:00.0"
+    parts = bus.split(":")
+    if len(parts) == 3 and len(parts[0]) == 4:
+        return "0000" + bus
+    return bus
+
+
+def time_e2e(wl, steps, dist_ctx):
+    """End to end through the public API: each step copies every rank's
+    inputs from pinned host memory, runs, and copies every rank's result
+    back to pinned host memory; all inside the timed region."""
+    import torch
+    ins = wl.input_tensors()
+    outs = wl.output_tensors()
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    for _ in range(2):
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        wl.step(stream)
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        wl.step(stream)
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_ctx.max(t0.elapsed_time(t1)) / steps
+    return ms, h2d, d2h
+
+
+def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False):
+    """Bandwidth of one standalone collective on {X:G} partial buffers of
+    ``mib`` MiB per rank (the full logical array V per rank)."""
+    import shmm_inputs
+    eb = 4 if dtype == "f32" else 2
+    numel = mib * (1 << 20) // eb
+    cols = 4096
+    rows = numel // cols
+    mesh = [("X", G)]
+    fl = s.FLAG_PARTIAL_OUT_DTYPE | (s.FLAG_TREE if tree else 0)
+    if op == "all_gather":
+        p = s.Plan(mesh, (("X",), ()), ((), ()), ((), ()), rows, 8, cols, dtype, dtype)
+        src = [torch.empty((rows // G, cols), dtype=H.TORCH_DTYPES[dtype], device="cuda").uniform_(-1, 1)
+               for _ in range(G)]
+        dst = H.alloc(p, s.TENSOR_C)
+        run = lambda: p.all_gather(s.TENSOR_C, src, dst)
+        V = rows * cols * eb
+        nbytes = V + G * V           # read V (each shard once), write G copies of V
+    else:
+        sC = (("X",), ()) if op == "reduce_scatter" else ((), ())
+        p = s.Plan(mesh, ((), ("X",)), (("X",), ()), sC, rows, G, cols, dtype, dtype, fl)
+        src = [torch.empty((rows, cols), dtype=H.TORCH_DTYPES[dtype], device="cuda").uniform_(-1, 1)
+               for _ in range(G)]
+        dst = H.alloc(p, s.TENSOR_C)
+        run = (lambda: p.reduce_scatter(src, dst)) if op == "reduce_scatter" else (lambda: p.all_reduce(src, dst))
+        V = rows * cols * eb
+        nbytes = G * V + (V if op == "reduce_scatter" else G * V)
+    # L2 flush by READING a buffer twice the L2 size: clean lines, so no
+    # write-back of the flush itself lands inside the timed kernel
+    flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    t = statistics.median(times)
+    busbw_factor = (G - 1) / G if op != "all_reduce" else 2 * (G - 1) / G
+    return {"op": op, "ranks": G, "MiB_per_rank": mib, "dtype": dtype, "order": "tree" if tree else "sequential",
+            "ms_median": t, "ms_best": min(times), "GB_s": nbytes / (t * 1e-3) / 1e9,
+            "bytes": nbytes, "busbw_GB_s": (V / (t * 1e-3) / 1e9) * busbw_factor}
+
+
+# --------------------------------------------------------------- oracle
+
+def oracle_sample_step(cfg_name, rows_per_rank, nthreads, host_globals):
+    """One bounded sample of the workload computed by the CPU oracle:
+    ``rows_per_rank`` output rows of every rank's block (local products,
+    rank-order sum, rounding, ownership).  Returns the sample's FLOPs."""
+    import numpy as np
+    import oracle
+    c = WORKLOADS[cfg_name]
+    if cfg_name == "down_projection":
+        A, B = host_globals
+        mesh, sA, sB, sC = c["mesh"], c["sA"], c["sB"], c["sC"]
+        xs = dict(mesh)["X"]
+        blk = c["I"] // xs
+        rows = sorted({x * blk + int(i * blk / rows_per_rank) for x in range(xs) for i in range(rows_per_rank)})
+        oracle.sharded_matmul(mesh, sA, sB, sC, A, B, out_dtype="bf16", rows=rows, nthreads=nthreads)
+        nr = len(rows) // xs  # rows per X block; each is formed by the 2 Y ranks
+        return 2 * nr * (c["J"] // 2) * c["K"] * oracle.mesh_size(mesh)
+    raise ValueError("no oracle sample for %s" % cfg_name)
+
+
+def host_globals_f32(wl):
+    return tuple(t.float().numpy() for t in wl.host_globals)
+
+
+def cpu_baseline(cfg_name, host_globals, target_s=12.0):
+    nthreads = len(os.sched_getaffinity(0))
+    t0 = time.time()
+    fl = oracle_sample_step(cfg_name, 8, nthreads, host_globals)
+    dt = time.time() - t0
+    rows = max(8, min(1024, int(8 * target_s / max(dt, 1e-3))))
+    t0 = time.time()
+    fl = oracle_sample_step(cfg_name, rows, nthreads, host_globals)
+    dt = time.time() - t0
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": "%d output rows of each of the 8 ranks' blocks (%.1f GFLOP of the step's %.0f), "
+                      "%.1f s" % (rows, fl / 1e9, 3848.3, dt)}
+
+
+# ---------------------------------------------------------- distributed
+
+class DistCtx:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = os.environ.get("SHMM_BENCH_BACKEND", "nccl")
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v):
+        if self.pg is None:
+            return v
+        import torch
+        dev = "cuda" if torch.cuda.is_available() and self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, dist_ctx):
+    """The oracle on the host cores as the reference arm."""
+    if dist_ctx.rank != 0:
+        return None
+    import shmm_inputs
+    name = args.workload
+    c = WORKLOADS[name]
+    A, B = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
+    hg = (A.float().numpy(), B.float().numpy())
+    nthreads = len(os.sched_getaffinity(0))
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    t0 = time.time()
+    oracle_sample_step(name, 1, nthreads, hg)
+    one = time.time() - t0
+    rows = max(1, min(256, int(budget / max(one, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_step(name, rows, nthreads, hg)
+    t0 = time.time()
+    fl = 0
+    for _ in range(args.steps):
+        fl += oracle_sample_step(name, rows, nthreads, hg)
+    dt = time.time() - t0
+    value = fl / dt / 1e12
+    sample = ("%d output rows of each rank's block per step (%.2f GFLOP of the step's 3848 GFLOP)"
+              % (rows, fl / args.steps / 1e9))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate",
+            "data": "synthetic", "config": {"workload": c["text"], "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_shmm(args, dist_ctx):
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the shmm arm needs a CUDA device")
+    torch.cuda.set_device(dist_ctx.local)
+    from partial_sum_reduction_gb300 import build
+    if dist_ctx.local == 0:
+        build.build()
+    dist_ctx.barrier()
+    import partial_sum_reduction_gb300 as s
+    from partial_sum_reduction_gb300 import helpers as H
+    peaks, peak_kind = load_peaks()
+    wl = Workload(args.workload, "cuda")
+    total_ms, per_step, launches, clocks = time_device(wl, args.steps, args.warmup, dist_ctx)
+    ms = total_ms / args.steps
+    N = dist_ctx.world
+    value = wl.flops * N / (total_ms / args.steps * 1e-3) / 1e12
+    # roofline of the dominant kernel: in the default workload one step is
+    # one fused GEMM launch, so the per-step event time is its duration
+    launch_ms = statistics.mean(per_step)
+    achieved = wl.flops / (launch_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    e2e_steps = max(3, min(10, args.steps // 10))
+    e2e_ms, h2d, d2h = time_e2e(wl, e2e_steps, dist_ctx)
+    e2e_value = wl.flops * N / (e2e_ms * 1e-3) / 1e12
+    rs = time_collective(s, H, torch, "reduce_scatter", 8, 256, "f32")
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": N, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload]["text"], "name": args.workload,
+                   "l2": "inputs larger than L2 (%.2f GB of per-rank operands per step)" % (wl.input_bytes() / 1e9),
+                   "flop_per_step": wl.flops, "replicas": N},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": "%s bf16 burst (cuBLAS 8192^3)" % peak_kind,
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "kernel": "gemm_tc_kernel<256> fused all-reduce epilogue"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "reduce_scatter": {"value": rs["GB_s"], "unit": "GB/s", "frac": rs["GB_s"] / peaks["hbm_gbs"],
+                           "peak": peaks["hbm_gbs"], "peak_kind": "%s HBM copy" % peak_kind,
+                           "config": "fp32 partials, 8 ranks x 256 MiB, sequential rank order, L2 flushed",
+                           "ms": rs["ms_median"], "busbw_GB_s": rs["busbw_GB_s"]},
+    }
+    if dist_ctx.rank == 0 and N == 1 and not args.no_cpu_baseline and args.workload == "down_projection":
+        out["cpu_baseline"] = cpu_baseline(args.workload, host_globals_f32(wl))
+    return out
+
+
+def run_sweep(args):
+    import torch
+    from partial_sum_reduction_gb300 import build
+    build.build()
+    import partial_sum_reduction_gb300 as s
+    from partial_sum_reduction_gb300 import helpers as H
+    peaks, kind = load_peaks()
+    sizes = [int(x) for x in args.sizes.split(",")]
+    for op in ("reduce_scatter", "all_reduce", "all_gather"):
+        for dtype in ("f32", "bf16"):
+            for G in (2, 4, 8, 16):
+                for mib in sizes:
+                    if G * mib * (2 if op == "all_reduce" else 1) > 40 * 1024:
+                        continue
+                    for tree in ((False, True) if op != "all_gather" else (False,)):
+                        r = time_collective(s, H, torch, op, G, mib, dtype, tree=tree)
+                        r["frac_hbm"] = r["GB_s"] / peaks["hbm_gbs"]
+                        r["peak_kind"] = kind
+                        print(json.dumps(r), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="shmm", choices=["shmm", "reference"])
+    ap.add_argument("--workload", default="down_projection", choices=sorted(WORKLOADS))
+    ap.add_argument("--sweep", default=None, choices=[None, "collectives"])
+    ap.add_argument("--sizes", default="1,16,256,1024")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.sweep:
+        run_sweep(args)
+        return
+    dist_ctx = DistCtx()
+    try:
+        if args.impl == "reference":
+            out = run_reference(args, dist_ctx)
+        else:
+            out = run_shmm(args, dist_ctx)
+        if dist_ctx.rank == 0 and out is not None:
+            print(json.dumps(out), flush=True)
+    finally:
+        dist_ctx.close()
+
+
+if __name__ == "__main__":
+    main()

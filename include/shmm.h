@@ -284,6 +284,10 @@ const char *shmm_status_string(shmm_status_t status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int shmm_version(void);
 
+/* Number of kernels this library has enqueued since it was loaded, over all
+ * threads and devices (a diagnostic for benchmarks and tests). */
+uint64_t shmm_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

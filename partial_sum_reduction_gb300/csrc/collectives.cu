@@ -394,6 +394,7 @@ int launch_reduce(const ReduceArgs &a, int *status, void *stream) {
     k.nvec = vec_ok ? n / V : n;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
+    count_launch();
     if (a.pt == SHMM_F32 && a.ot == SHMM_F32) e = reduce_dispatch<float, float>(k, vec_ok, a.tree, a.gelu, s);
     else if (a.pt == SHMM_F32) e = reduce_dispatch<float, __nv_bfloat16>(k, vec_ok, a.tree, a.gelu, s);
     else if (a.ot == SHMM_BF16) e = reduce_dispatch<__nv_bfloat16, __nv_bfloat16>(k, vec_ok, a.tree, a.gelu, s);
@@ -421,6 +422,7 @@ int launch_gather(const GatherArgs &a, int *status, void *stream) {
     k.nvec = (int64_t)a.G * a.brows * k.bvecs;
     cudaStream_t s = (cudaStream_t)stream;
     const unsigned grid = grid_for(k.nvec * k.ngroups, 256 * 2);
+    count_launch();
     if (vec) gather_kernel<true><<<grid, 256, 0, s>>>(k, a.elem);
     else gather_kernel<false><<<grid, 256, 0, s>>>(k, a.elem);
     return (int)cudaGetLastError();

@@ -156,6 +156,7 @@ int launch_gemm_simt(const GemmArgs &a, int *status, void *stream) {
     if (gy > 65535) return (int)cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)a.units);
     cudaStream_t s = (cudaStream_t)stream;
+    count_launch();
     if (a.in_dt == SHMM_F32 && a.out_dt == SHMM_F32) gemm_simt_kernel<float, float><<<grid, 256, 0, s>>>(k);
     else if (a.in_dt == SHMM_F32) gemm_simt_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(k);
     else if (a.out_dt == SHMM_F32) gemm_simt_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(k);

@@ -507,6 +507,7 @@ cudaError_t launch_bn(TcK &k, cudaStream_t s) {
     k.n_tiles = (int)((k.N + BN - 1) / BN);
     const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
     const int grid = (int)(total < num_sms() ? total : num_sms());
+    shmm::count_launch();
     gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, s>>>(k);
     return cudaGetLastError();
 }

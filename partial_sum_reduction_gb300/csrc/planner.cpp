@@ -8,6 +8,7 @@
 // multiplication and result ownership" (The mechanism, steps 1-5).
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -30,6 +31,9 @@ shmm_status_t fail(shmm_status_t st, const std::string &msg) {
 void clear_error() { g_last_error.clear(); }
 
 int64_t elem_bytes(shmm_dtype_t t) { return t == SHMM_F32 ? 4 : 2; }
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 }  // namespace shmm
 
@@ -423,5 +427,7 @@ const char *shmm_status_string(shmm_status_t s) {
 const char *shmm_last_error(void) { return shmm::g_last_error.c_str(); }
 
 int shmm_version(void) { return 100; }
+
+uint64_t shmm_kernel_launches(void) { return shmm::g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -136,6 +136,9 @@ bool tcgen05_supported(const GemmArgs &a);
 // Returns a cudaError_t value; sets *msg on a failure outside CUDA.
 int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::string *msg);
 
+// Count of kernels enqueued by this library since it was loaded.
+void count_launch(int n = 1);
+
 // Device status word (set by kernels whose bounded waits expire).
 int device_status_ptr(int **ptr);  // cudaError_t value
 int device_status_read_clear(int *value, void *stream);

@@ -69,7 +69,7 @@ class ShmmError(RuntimeError):
 EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_box",
            "shmm_plan_group", "shmm_workspace_size", "shmm_local_matmul", "shmm_reduce_scatter",
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
-           "shmm_status_string", "shmm_version"]
+           "shmm_status_string", "shmm_version", "shmm_kernel_launches"]
 
 _lib = None
 
@@ -104,8 +104,9 @@ def lib():
         L.shmm_last_error.restype = ctypes.c_char_p
         L.shmm_status_string.argtypes = [ctypes.c_int]
         L.shmm_status_string.restype = ctypes.c_char_p
+        L.shmm_kernel_launches.restype = ctypes.c_uint64
         for f in EXPORTS:
-            if f not in ("shmm_last_error", "shmm_status_string"):
+            if f not in ("shmm_last_error", "shmm_status_string", "shmm_kernel_launches"):
                 getattr(L, f).restype = st
         _lib = L
     return _lib
@@ -353,3 +354,7 @@ def shmm_sync_status(stream=None) -> None:
 
 def shmm_version() -> int:
     return lib().shmm_version()
+
+
+def shmm_kernel_launches() -> int:
+    return lib().shmm_kernel_launches()
