@@ -270,6 +270,32 @@ shmm_status_t shmm_all_gather(const shmm_plan_t *plan, int tensor, const void *c
 shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const void *const *B_r,
                        void *const *C_r, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the fixed device workspace behind shmm_run_static_workspace. */
+#define SHMM_STATIC_WORKSPACE_BYTES (64u << 20)
+
+/* shmm_run for callers that cannot allocate device memory: a plugin or host
+ * framework that hands over only input and output buffers and offers no
+ * allocator, or a latency-critical caller that must not call cudaMalloc
+ * (which can synchronise the device) once it is running.  The pages have no
+ * counterpart: this is an interface convenience of this library.
+ * Same arguments and results as shmm_run, without the workspace: the
+ * workspace is a file-scope device array of SHMM_STATIC_WORKSPACE_BYTES
+ * (64 MiB) that every device loading the library holds until the process
+ * exits.  This call allocates nothing.
+ *   - Plans whose shmm_workspace_size() exceeds SHMM_STATIC_WORKSPACE_BYTES
+ *     are rejected with SHMM_ERR_NOMEM before anything is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents; nothing in it needs to start at zero (each use
+ *     writes every byte it later reads).  Calls that overlap on the GPU
+ *     (different streams, or host threads without ordering) race on it:
+ *     order them on one stream.
+ * Errors: those of shmm_run, and NOMEM (workspace need above the limit). */
+shmm_status_t shmm_run_static_workspace(const shmm_plan_t *plan, const void *const *A_r,
+                                        const void *const *B_r, void *const *C_r, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device status word that
  * kernels set when a bounded wait expires.  Returns SHMM_OK, SHMM_ERR_TIMEOUT
  * or SHMM_ERR_CUDA. */

@@ -16,6 +16,12 @@ using shmm::fail;
 // Status word written by kernels whose bounded waits expire (0 = fine).
 __device__ int g_shmm_status_word;
 
+// Fixed workspace for shmm_run_static_workspace, for callers that cannot
+// allocate device memory themselves.  Every device that loads this library
+// holds these SHMM_STATIC_WORKSPACE_BYTES until the process exits, and every
+// call on a device shares them.
+static __device__ __align__(256) unsigned char g_shmm_static_workspace[SHMM_STATIC_WORKSPACE_BYTES];
+
 namespace {
 
 int *status_ptr(std::string *err) {
@@ -33,6 +39,28 @@ int *status_ptr(std::string *err) {
             return nullptr;
         }
         cached[dev] = static_cast<int *>(p);
+    }
+    return cached[dev];
+}
+
+// Device address of g_shmm_static_workspace on the current device.  Host
+// code cannot use the array's name as a device pointer, so the address is
+// looked up once per device (with that device current) and cached.
+void *static_workspace_ptr(std::string *err) {
+    static void *cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = "no CUDA device";
+        return nullptr;
+    }
+    if (!cached[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_shmm_static_workspace);
+        if (e != cudaSuccess) {
+            *err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
+            return nullptr;
+        }
+        cached[dev] = p;
     }
     return cached[dev];
 }
@@ -368,6 +396,28 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         if (e) return cuda_fail(fn, e, "gather C");
     }
     return SHMM_OK;
+}
+
+shmm_status_t shmm_run_static_workspace(const shmm_plan_t *p, const void *const *A_r,
+                                        const void *const *B_r, void *const *C_r, void *stream) {
+    static const char *fn = "shmm_run_static_workspace";
+    shmm::clear_error();
+    if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    size_t need = 0;
+    shmm_workspace_size(p, &need);
+    if (need > (size_t)SHMM_STATIC_WORKSPACE_BYTES)
+        return fail(SHMM_ERR_NOMEM, std::string(fn) + ": the plan needs " + std::to_string(need) +
+                                        " bytes of workspace, more than the " +
+                                        std::to_string((size_t)SHMM_STATIC_WORKSPACE_BYTES) +
+                                        " of the static workspace; use shmm_run with a workspace you allocate");
+    void *ws = nullptr;
+    if (need) {
+        std::string err;
+        ws = static_workspace_ptr(&err);
+        if (!ws) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    }
+    return shmm_run(p, A_r, B_r, C_r, ws, need, stream);
 }
 
 shmm_status_t shmm_sync_status(void *stream) {

@@ -69,7 +69,7 @@ class ShmmError(RuntimeError):
 EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_box",
            "shmm_plan_group", "shmm_workspace_size", "shmm_local_matmul", "shmm_reduce_scatter",
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
-           "shmm_status_string", "shmm_version", "shmm_kernel_launches"]
+           "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace"]
 
 _lib = None
 
@@ -100,6 +100,7 @@ def lib():
         L.shmm_all_reduce.argtypes = [P, PP, PP, P]
         L.shmm_all_gather.argtypes = [P, ctypes.c_int, PP, PP, P]
         L.shmm_run.argtypes = [P, PP, PP, PP, P, ctypes.c_size_t, P]
+        L.shmm_run_static_workspace.argtypes = [P, PP, PP, PP, P]
         L.shmm_sync_status.argtypes = [P]
         L.shmm_last_error.restype = ctypes.c_char_p
         L.shmm_status_string.argtypes = [ctypes.c_int]
@@ -306,6 +307,12 @@ class Plan:
         _check(lib().shmm_run(self._h, _ptr_array(A_r, "A"), _ptr_array(B_r, "B"), _ptr_array(C_r, "C"),
                               ws_ptr, ws_bytes, _stream_handle(stream)))
 
+    def run_static_workspace(self, A_r, B_r, C_r, stream=None):
+        """shmm_run on the library's fixed 64 MiB device workspace, for
+        callers that cannot allocate device memory (see include/shmm.h)."""
+        _check(lib().shmm_run_static_workspace(self._h, _ptr_array(A_r, "A"), _ptr_array(B_r, "B"),
+                                               _ptr_array(C_r, "C"), _stream_handle(stream)))
+
 
 # Same names as the C-ABI, for callers that prefer the flat interface.
 def shmm_plan(mesh, spec_A, spec_B, spec_C, I, J, K, in_dtype="bf16", out_dtype="bf16", flags=0) -> Plan:
@@ -346,6 +353,13 @@ def shmm_all_gather(plan: Plan, tensor: int, shard_r, full_r, stream=None):
 
 def shmm_run(plan: Plan, A_r, B_r, C_r, workspace=None, stream=None):
     plan.run(A_r, B_r, C_r, workspace, stream)
+
+
+def shmm_run_static_workspace(plan: Plan, A_r, B_r, C_r, stream=None):
+    plan.run_static_workspace(A_r, B_r, C_r, stream)
+
+
+STATIC_WORKSPACE_BYTES = 64 << 20
 
 
 def shmm_sync_status(stream=None) -> None:

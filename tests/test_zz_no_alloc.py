@@ -1,0 +1,69 @@
+"""shmm_run_static_workspace: the variant of shmm_run for callers that cannot
+allocate device memory (a host framework or plugin interface that passes in
+only the input and output buffers, or a caller that must not call cudaMalloc
+once running).  It takes its scratch from the library's fixed 64 MiB device
+array instead of a caller-supplied workspace.
+
+Each test calls the entry point through the C-ABI twice in a row and checks
+both results against shmm_run with a workspace the test allocates.  This file
+sorts last so that a run stopping at its first failure has already run every
+other test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import shmm_inputs
+from parity_util import BF16_TOL, lib
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # unfused reduce-scatter: fp32 partials in the scratch array
+    ("{Y:2}", ((), ("Y",)), (("Y",), ()), (("Y",), ()), 512, 1024, 384),
+    # case 2: the all-gathered operand in the scratch array
+    ("{X:2,Y:2}", ((), ("X",)), ((), ()), ((), ()), 256, 512, 264),
+    # all-reduce then all-gather of the result: partials + owner blocks
+    ("{X:4,Y:2}", (("X",), ("Y",)), (("Y",), ()), ((), ()), 512, 1024, 256),
+]
+
+
+def _ptrs(ts):
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+@pytest.mark.parametrize("mesh,sA,sB,sC,I,J,K", CASES)
+def test_static_workspace_matches_shmm_run_on_two_calls(mesh, sA, sB, sC, I, J, K):
+    s = lib()
+    from partial_sum_reduction_gb300 import helpers as H
+    A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=I + K)
+    plan = s.Plan(mesh, sA, sB, sC, I, J, K, "bf16", "bf16")
+    need = plan.workspace_size()
+    assert 0 < need <= s.shmm.STATIC_WORKSPACE_BYTES
+    A_r, B_r = H.shard(plan, s.TENSOR_A, A), H.shard(plan, s.TENSOR_B, B)
+    ref = H.alloc(plan, s.TENSOR_C, fill=float("nan"))
+    plan.run(A_r, B_r, ref, H.workspace(plan))
+    torch.cuda.synchronize()
+    L = s.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        out = H.alloc(plan, s.TENSOR_C, fill=float("nan"))
+        st = L.shmm_run_static_workspace(plan.handle, _ptrs(A_r), _ptrs(B_r), _ptrs(out), stream)
+        assert st == 0, L.shmm_last_error()
+        assert L.shmm_sync_status(stream) == 0
+        ref_max = max(float(r.float().abs().max()) for r in ref)
+        for r, o in zip(ref, out):
+            got = o.float().cpu().numpy()
+            assert not np.isnan(got).any(), "call %d left output unwritten" % call
+            assert np.abs(got - r.float().cpu().numpy()).max() <= BF16_TOL * ref_max
+
+
+def test_static_workspace_rejects_plans_above_its_size():
+    s = lib()
+    plan = s.Plan("{X:2,Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 4096, 4096, 4096, "bf16", "bf16")
+    assert plan.workspace_size() > s.shmm.STATIC_WORKSPACE_BYTES
+    dummy = (ctypes.c_void_p * 4)(*([0x10000] * 4))
+    L = s.lib()
+    assert L.shmm_run_static_workspace(plan.handle, dummy, dummy, dummy, None) == s.shmm.ERR_NOMEM
+    assert b"static workspace" in L.shmm_last_error()
