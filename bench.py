@@ -41,6 +41,10 @@ WORKLOADS = {
         I=8192, J=28672, K=8192, fused=True,
         text="tensor-parallel down-projection A[8192,28672].B[28672,8192] bf16 on {X:4,Y:2}, "
              "A[I_X,J_Y], B[J_Y,K] -> C[I_X,K] (all-reduce over Y fused into the GEMM epilogue)"),
+    "down_projection_quarter": dict(
+        mesh=[("X", 4), ("Y", 2)], sA=(("X",), ("Y",)), sB=(("Y",), ()), sC=(("X",), ()),
+        I=4096, J=14336, K=4096, fused=True,
+        text="quarter-size down-projection A[4096,14336].B[14336,4096] bf16 on {X:4,Y:2} (profiling case)"),
     "four_case": dict(
         mesh=[("X", 2), ("Y", 2)], I=2048, J=2048, K=2048, fused=True,
         text="four-case sweep I=J=K=2048 bf16 on {X:2,Y:2} (cases 1-4 back to back)"),
@@ -157,7 +161,7 @@ class Workload:
         c = self.cfg
         self.steps_spec = []   # (plan, A list, B list, C list, ws)
         self.flops = 0
-        if name == "down_projection":
+        if name in ("down_projection", "down_projection_quarter"):
             A, B = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
             self.host_globals = (A, B)
             self._add(c["mesh"], c["sA"], c["sB"], c["sC"], A, B, s.FLAG_FUSED if c["fused"] else 0, device)
