@@ -374,7 +374,7 @@ def oracle_sample_step(cfg_name, rows_per_rank, nthreads, host_globals):
     import numpy as np
     import oracle
     c = WORKLOADS[cfg_name]
-    if cfg_name == "down_projection":
+    if cfg_name in ("down_projection", "down_projection_quarter"):
         A, B = host_globals
         mesh, sA, sB, sC = c["mesh"], c["sA"], c["sB"], c["sC"]
         xs = dict(mesh)["X"]
@@ -399,9 +399,10 @@ def cpu_baseline(cfg_name, host_globals, target_s=12.0):
     t0 = time.time()
     fl = oracle_sample_step(cfg_name, rows, nthreads, host_globals)
     dt = time.time() - t0
+    c = WORKLOADS[cfg_name]
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
             "sample": "%d output rows of each of the 8 ranks' blocks (%.1f GFLOP of the step's %.0f), "
-                      "%.1f s" % (rows, fl / 1e9, 3848.3, dt)}
+                      "%.1f s" % (rows, fl / 1e9, 2.0 * c["I"] * c["J"] * c["K"] / 1e9, dt)}
 
 
 # ---------------------------------------------------------- distributed
@@ -413,8 +414,12 @@ class DistCtx:
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
         if self.world > 1:
+            import torch
             import torch.distributed as dist
-            backend = os.environ.get("SHMM_BENCH_BACKEND", "nccl")
+            default = "nccl" if torch.cuda.is_available() else "gloo"
+            backend = os.environ.get("SHMM_BENCH_BACKEND", default)
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
             dist.init_process_group(backend)
             self.pg = dist
 
@@ -448,7 +453,7 @@ def run_reference(args, dist_ctx):
     A, B = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
     hg = (A.float().numpy(), B.float().numpy())
     nthreads = len(os.sched_getaffinity(0))
-    budget = 150.0 / max(1, args.steps + args.warmup)
+    budget = args.reference_budget_s / max(1, args.steps + args.warmup)
     t0 = time.time()
     oracle_sample_step(name, 1, nthreads, hg)
     one = time.time() - t0
@@ -461,8 +466,9 @@ def run_reference(args, dist_ctx):
         fl += oracle_sample_step(name, rows, nthreads, hg)
     dt = time.time() - t0
     value = fl / dt / 1e12
-    sample = ("%d output rows of each rank's block per step (%.2f GFLOP of the step's 3848 GFLOP)"
-              % (rows, fl / args.steps / 1e9))
+    step_gflop = 2.0 * c["I"] * c["J"] * c["K"] / 1e9
+    sample = ("%d output rows of each rank's block per step (%.2f GFLOP of the step's %.0f GFLOP)"
+              % (rows, fl / args.steps / 1e9, step_gflop))
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate",
@@ -555,6 +561,8 @@ def main():
     ap.add_argument("--sweep", default=None, choices=[None, "collectives"])
     ap.add_argument("--sizes", default="1,16,256,1024")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget-s", type=float, default=150.0,
+                    help="--impl reference: seconds of oracle work for the whole run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
