@@ -163,7 +163,7 @@ typedef struct {
     int tensor_core;       /* 1 if the local GEMM runs on tcgen05 */
     int fused;             /* 1 if shmm_run reduces in the GEMM epilogue
                               (SHMM_FLAG_FUSED honoured: on tensor cores, at
-                              most 8 ranks per group; otherwise shmm_run
+                              most 16 ranks per group; otherwise shmm_run
                               reduces with the standalone kernel) */
     int64_t local_I, local_J, local_K;   /* per-rank GEMM M, K, N */
     int64_t flops_per_rank;              /* 2 * local_I * local_J * local_K */

@@ -31,7 +31,7 @@ struct ReduceK {
     void *dst[kMaxPtrs];        // [g*G + b]: owner of block b (RS) / member b (AR)
     int G, ngroups, mode;       // mode: 0 RS rows, 1 RS cols, 2 AR
     int64_t rows, cols, n;      // per-rank partial shape, n = rows*cols
-    int64_t nvec;               // vectors per group
+    int64_t nvec;               // vectors per group (per rank's partial)
 };
 
 struct GatherK {
@@ -112,30 +112,34 @@ __device__ __forceinline__ void store_n(void *p, const float *v) {
     }
 }
 
-// Destination element index and owner for element e of the partial.
-__device__ __forceinline__ void route(const ReduceK &k, int64_t e, int *b, int64_t *off) {
+// Destination owner b and element offset for element e of a partial.  IT is
+// the index type: 32-bit whenever every index of the launch fits, since
+// 64-bit integer division costs many times more instructions.
+template <typename IT>
+__device__ __forceinline__ void route(const ReduceK &k, IT e, int *b, IT *off) {
     if (k.mode == 0) {
-        const int64_t per = k.n / k.G;
+        const IT per = (IT)(k.n / k.G);
         *b = (int)(e / per);
-        *off = e - (int64_t)(*b) * per;
+        *off = e - (IT)(*b) * per;
     } else if (k.mode == 1) {
-        const int64_t row = e / k.cols, col = e - row * k.cols, per = k.cols / k.G;
+        const IT cols = (IT)k.cols, per = (IT)(k.cols / k.G);
+        const IT row = e / cols, col = e - row * cols;
         *b = (int)(col / per);
-        *off = row * per + (col - (int64_t)(*b) * per);
+        *off = row * per + (col - (IT)(*b) * per);
     } else {
         *b = -1;
         *off = e;
     }
 }
 
-template <typename OT, int NV>
-__device__ __forceinline__ void write_out(const ReduceK &k, int g, int64_t e, float *s, bool gelu) {
+template <typename OT, int NV, typename IT>
+__device__ __forceinline__ void write_out(const ReduceK &k, int g, IT e, float *s, bool gelu) {
     if (gelu)
 #pragma unroll
         for (int i = 0; i < NV; ++i) s[i] = gelu_tanh(s[i]);
     int b;
-    int64_t off;
-    route(k, e, &b, &off);
+    IT off;
+    route<IT>(k, e, &b, &off);
     const int q0 = b >= 0 ? b : 0, q1 = b >= 0 ? b + 1 : k.G;
     for (int q = q0; q < q1; ++q) {
         OT *d = (OT *)k.dst[g * k.G + q] + off;
@@ -144,43 +148,58 @@ __device__ __forceinline__ void write_out(const ReduceK &k, int g, int64_t e, fl
     }
 }
 
-// Sequential rank-order sum, 16-byte vectors.  GT > 0: group size known at
-// compile time (all G loads issued before the adds); GT == 0: runtime G.
-template <typename PT, typename OT, int GT, int UNROLL>
+// Rank sum over 16-byte vectors; group g = blockIdx.y.  GT > 0: group size
+// known at compile time (all G loads issued before the adds); GT == 0:
+// runtime G.  TREE (GT a power of two only): the G vectors held in registers
+// are added as a balanced pairwise tree over the ranks in ascending order --
+// the same tree, and the same bits, as the warp-shuffle kernel below, at the
+// memory rate of the sequential order.
+template <typename PT, typename OT, int GT, int UNROLL, typename IT, bool TREE = false>
 __global__ void __launch_bounds__(256) reduce_seq_kernel(const __grid_constant__ ReduceK k, bool gelu) {
+    static_assert(!TREE || (GT > 0 && (GT & (GT - 1)) == 0), "register tree needs a power-of-two G");
     constexpr int V = Vec<PT>::N;
     const int G = GT > 0 ? GT : k.G;
-    const int64_t total = k.nvec * k.ngroups;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x * UNROLL;
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x * UNROLL + threadIdx.x; base < total;
-         base += stride) {
+    const int g = blockIdx.y;
+    const IT total = (IT)k.nvec;
+    const IT stride = (IT)gridDim.x * blockDim.x * UNROLL;
+    const void *const *src = k.src + g * G;
+    for (IT base = (IT)blockIdx.x * blockDim.x * UNROLL + threadIdx.x; base < total; base += stride) {
         float acc[UNROLL][V];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t v = base + (int64_t)u * blockDim.x;
+            const IT v = base + (IT)u * blockDim.x;
             if (v >= total) continue;
-            const int g = (int)(v / k.nvec);
-            const int64_t e = (v - (int64_t)g * k.nvec) * V;
+            const IT e = v * V;
             if constexpr (GT > 0) {
                 float x[GT][V];
 #pragma unroll
-                for (int q = 0; q < GT; ++q)
-                    Vec<PT>::load((const PT *)k.src[g * GT + q] + e, x[q]);
+                for (int q = 0; q < GT; ++q) Vec<PT>::load((const PT *)src[q] + e, x[q]);
+                if constexpr (TREE) {
 #pragma unroll
-                for (int i = 0; i < V; ++i) {
-                    float s = x[0][i];
+                    for (int w = GT; w > 1; w >>= 1)
 #pragma unroll
-                    for (int q = 1; q < GT; ++q) s = s + x[q][i];
-                    acc[u][i] = s;
+                        for (int r = 0; r < w / 2; ++r)
+#pragma unroll
+                            for (int i = 0; i < V; ++i) x[r][i] = x[2 * r][i] + x[2 * r + 1][i];
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[u][i] = x[0][i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < V; ++i) {
+                        float s = x[0][i];
+#pragma unroll
+                        for (int q = 1; q < GT; ++q) s = s + x[q][i];
+                        acc[u][i] = s;
+                    }
                 }
             } else {
-                Vec<PT>::load((const PT *)k.src[g * G] + e, acc[u]);
+                Vec<PT>::load((const PT *)src[0] + e, acc[u]);
                 for (int q = 1; q < G; q += 4) {
                     float x[4][V];
                     const int m = min(4, G - q);
 #pragma unroll
                     for (int t = 0; t < 4; ++t)
-                        if (t < m) Vec<PT>::load((const PT *)k.src[g * G + q + t] + e, x[t]);
+                        if (t < m) Vec<PT>::load((const PT *)src[q + t] + e, x[t]);
 #pragma unroll
                     for (int t = 0; t < 4; ++t)
                         if (t < m)
@@ -191,23 +210,19 @@ __global__ void __launch_bounds__(256) reduce_seq_kernel(const __grid_constant__
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t v = base + (int64_t)u * blockDim.x;
+            const IT v = base + (IT)u * blockDim.x;
             if (v >= total) continue;
-            const int g = (int)(v / k.nvec);
-            const int64_t e = (v - (int64_t)g * k.nvec) * V;
-            write_out<OT, V>(k, g, e, acc[u], gelu);
+            write_out<OT, V, IT>(k, g, v * V, acc[u], gelu);
         }
     }
 }
 
-// Scalar fallback for shapes whose rows/owner blocks are not whole vectors.
-template <typename PT, typename OT, bool TREE>
+// Scalar fallback for shapes whose owner blocks are not whole vectors.
+template <typename PT, typename OT, bool TREE, typename IT>
 __global__ void __launch_bounds__(256) reduce_scalar_kernel(const __grid_constant__ ReduceK k, bool gelu) {
-    const int64_t total = k.n * k.ngroups;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total;
-         v += (int64_t)gridDim.x * blockDim.x) {
-        const int g = (int)(v / k.n);
-        const int64_t e = v - (int64_t)g * k.n;
+    const int g = blockIdx.y;
+    const IT total = (IT)k.n;
+    for (IT e = (IT)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (IT)gridDim.x * blockDim.x) {
         float s;
         if (!TREE) {
             s = Vec<PT>::load1((const PT *)k.src[g * k.G] + e);
@@ -223,7 +238,7 @@ __global__ void __launch_bounds__(256) reduce_scalar_kernel(const __grid_constan
                 for (int q = 0; q < w / 2; ++q) lv[q] = lv[2 * q] + lv[2 * q + 1];
             s = lv[0];
         }
-        write_out<OT, 1>(k, g, e, &s, gelu);
+        write_out<OT, 1, IT>(k, g, e, &s, gelu);
     }
 }
 
@@ -231,25 +246,25 @@ __global__ void __launch_bounds__(256) reduce_scalar_kernel(const __grid_constan
 // >= G) reduces one vector position; lane q loads rank q (q < G) or -0.0.
 // After log2(W) xor-shuffle levels every lane holds the same total (fp32
 // addition is commutative bit for bit), so lane q writes destination q.
-template <typename PT, typename OT, int W, int UNROLL>
+template <typename PT, typename OT, int W, int UNROLL, typename IT>
 __global__ void __launch_bounds__(256) reduce_tree_kernel(const __grid_constant__ ReduceK k, bool gelu) {
     constexpr int V = Vec<PT>::N;
     constexpr int PER_WARP = 32 / W;  // vector positions per warp per step
     const int lane = threadIdx.x & 31;
     const int q = lane % W;
     const int sub = lane / W;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
-    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    const int64_t total = k.nvec * k.ngroups;
-    for (int64_t base = warp * PER_WARP * UNROLL; base < total; base += warps * PER_WARP * UNROLL) {
+    const int g = blockIdx.y;
+    const IT warps = (IT)gridDim.x * (blockDim.x / 32);
+    const IT warp = (IT)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const IT total = (IT)k.nvec;
+    const PT *src = q < k.G ? (const PT *)k.src[g * k.G + q] : nullptr;
+    for (IT base = warp * PER_WARP * UNROLL; base < total; base += warps * PER_WARP * UNROLL) {
         float x[UNROLL][V];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t v = base + (int64_t)u * PER_WARP + sub;
-            if (v < total && q < k.G) {
-                const int g = (int)(v / k.nvec);
-                const int64_t e = (v - (int64_t)g * k.nvec) * V;
-                Vec<PT>::load((const PT *)k.src[g * k.G + q] + e, x[u]);
+            const IT v = base + (IT)u * PER_WARP + sub;
+            if (v < total && src) {
+                Vec<PT>::load(src + v * V, x[u]);
             } else {
 #pragma unroll
                 for (int i = 0; i < V; ++i) x[u][i] = -0.0f;
@@ -263,16 +278,14 @@ __global__ void __launch_bounds__(256) reduce_tree_kernel(const __grid_constant_
                 for (int i = 0; i < V; ++i) x[u][i] = x[u][i] + __shfl_xor_sync(0xffffffffu, x[u][i], off);
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t v = base + (int64_t)u * PER_WARP + sub;
+            const IT v = base + (IT)u * PER_WARP + sub;
             if (v >= total || q >= k.G) continue;
-            const int g = (int)(v / k.nvec);
-            const int64_t e = (v - (int64_t)g * k.nvec) * V;
             float s[V];
 #pragma unroll
             for (int i = 0; i < V; ++i) s[i] = gelu ? gelu_tanh(x[u][i]) : x[u][i];
             int b;
-            int64_t off;
-            route(k, e, &b, &off);
+            IT off;
+            route<IT>(k, v * V, &b, &off);
             if (b >= 0 && b != q) continue;  // RS: only the owner's lane writes
             store_n<OT, V>((OT *)k.dst[g * k.G + q] + off, s);
         }
@@ -293,73 +306,90 @@ int sm_count() {
     return cached[dev];
 }
 
-unsigned grid_for(int64_t work, int per_block) {
+// Grid for `work` items per group, `per_block` items per CTA and `groups`
+// groups along y: about 8 resident CTAs per SM in total.
+dim3 grid_for(int64_t work, int per_block, int groups) {
     const int64_t want = (work + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)sm_count() * 8;
-    return (unsigned)(want < 1 ? 1 : (want > cap ? cap : want));
+    int64_t cap = (int64_t)sm_count() * 8 / (groups > 0 ? groups : 1);
+    if (cap < 1) cap = 1;
+    return dim3((unsigned)(want < 1 ? 1 : (want > cap ? cap : want)), (unsigned)groups, 1);
 }
 
-template <typename PT, typename OT>
+template <typename PT, typename OT, typename IT>
 cudaError_t reduce_dispatch(const ReduceK &k, bool vec_ok, bool tree, bool gelu, cudaStream_t s) {
-    const int64_t total_vec = k.nvec * k.ngroups;
     if (!vec_ok) {
-        const unsigned grid = grid_for(k.n * k.ngroups, 256);
-        if (tree) reduce_scalar_kernel<PT, OT, true><<<grid, 256, 0, s>>>(k, gelu);
-        else reduce_scalar_kernel<PT, OT, false><<<grid, 256, 0, s>>>(k, gelu);
+        const dim3 grid = grid_for(k.n, 256, k.ngroups);
+        if (tree) reduce_scalar_kernel<PT, OT, true, IT><<<grid, 256, 0, s>>>(k, gelu);
+        else reduce_scalar_kernel<PT, OT, false, IT><<<grid, 256, 0, s>>>(k, gelu);
+        return cudaGetLastError();
+    }
+    if (tree && (k.G == 2 || k.G == 4 || k.G == 8 || k.G == 16)) {
+        // power-of-two groups fit in registers: pairwise tree per thread
+        switch (k.G) {
+            case 2: reduce_seq_kernel<PT, OT, 2, 4, IT, true><<<grid_for(k.nvec, 256 * 4, k.ngroups), 256, 0, s>>>(k, gelu); break;
+            case 4: reduce_seq_kernel<PT, OT, 4, 2, IT, true><<<grid_for(k.nvec, 256 * 2, k.ngroups), 256, 0, s>>>(k, gelu); break;
+            case 8: reduce_seq_kernel<PT, OT, 8, 1, IT, true><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
+            default: reduce_seq_kernel<PT, OT, 16, 1, IT, true><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        }
         return cudaGetLastError();
     }
     if (tree) {
+        // other group sizes: one rank per lane, shuffles pad to a power of two
         int W = 1;
         while (W < k.G) W <<= 1;
-        const unsigned grid = grid_for(total_vec, 8 * (32 / W) * 2);  // 8 warps, UNROLL 2
+        constexpr int U = 4;  // vector positions per lane in flight
+        const dim3 grid = grid_for(k.nvec, 8 * (32 / W) * U, k.ngroups);  // 8 warps per CTA
         switch (W) {
-            case 1: reduce_tree_kernel<PT, OT, 1, 2><<<grid, 256, 0, s>>>(k, gelu); break;
-            case 2: reduce_tree_kernel<PT, OT, 2, 2><<<grid, 256, 0, s>>>(k, gelu); break;
-            case 4: reduce_tree_kernel<PT, OT, 4, 2><<<grid, 256, 0, s>>>(k, gelu); break;
-            case 8: reduce_tree_kernel<PT, OT, 8, 2><<<grid, 256, 0, s>>>(k, gelu); break;
-            case 16: reduce_tree_kernel<PT, OT, 16, 2><<<grid, 256, 0, s>>>(k, gelu); break;
-            default: reduce_tree_kernel<PT, OT, 32, 2><<<grid, 256, 0, s>>>(k, gelu); break;
+            case 1: reduce_tree_kernel<PT, OT, 1, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
+            case 2: reduce_tree_kernel<PT, OT, 2, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
+            case 4: reduce_tree_kernel<PT, OT, 4, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
+            case 8: reduce_tree_kernel<PT, OT, 8, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
+            case 16: reduce_tree_kernel<PT, OT, 16, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
+            default: reduce_tree_kernel<PT, OT, 32, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
         }
         return cudaGetLastError();
     }
     switch (k.G) {
-        case 1: reduce_seq_kernel<PT, OT, 1, 4><<<grid_for(total_vec, 256 * 4), 256, 0, s>>>(k, gelu); break;
-        case 2: reduce_seq_kernel<PT, OT, 2, 4><<<grid_for(total_vec, 256 * 4), 256, 0, s>>>(k, gelu); break;
-        case 4: reduce_seq_kernel<PT, OT, 4, 2><<<grid_for(total_vec, 256 * 2), 256, 0, s>>>(k, gelu); break;
-        case 8: reduce_seq_kernel<PT, OT, 8, 1><<<grid_for(total_vec, 256), 256, 0, s>>>(k, gelu); break;
-        case 16: reduce_seq_kernel<PT, OT, 16, 1><<<grid_for(total_vec, 256), 256, 0, s>>>(k, gelu); break;
-        default: reduce_seq_kernel<PT, OT, 0, 1><<<grid_for(total_vec, 256), 256, 0, s>>>(k, gelu); break;
+        case 1: reduce_seq_kernel<PT, OT, 1, 4, IT><<<grid_for(k.nvec, 256 * 4, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        case 2: reduce_seq_kernel<PT, OT, 2, 4, IT><<<grid_for(k.nvec, 256 * 4, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        case 4: reduce_seq_kernel<PT, OT, 4, 2, IT><<<grid_for(k.nvec, 256 * 2, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        case 8: reduce_seq_kernel<PT, OT, 8, 1, IT><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        case 16: reduce_seq_kernel<PT, OT, 16, 1, IT><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        default: reduce_seq_kernel<PT, OT, 0, 1, IT><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
     }
     return cudaGetLastError();
 }
 
-// All-gather: one read of each source vector, G writes.
-template <bool VEC16>
-__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherK k, int64_t elem) {
-    const int64_t total = k.nvec * k.ngroups;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total;
-         v += (int64_t)gridDim.x * blockDim.x) {
-        const int g = (int)(v / k.nvec);
-        int64_t w = v - (int64_t)g * k.nvec;
-        const int64_t per_block = k.brows * k.bvecs;
-        const int p = (int)(w / per_block);
-        w -= (int64_t)p * per_block;
-        const int64_t r = w / k.bvecs, c = w - r * k.bvecs;
+template <typename PT, typename OT>
+cudaError_t reduce_dispatch_idx(const ReduceK &k, bool vec_ok, bool tree, bool gelu, cudaStream_t s) {
+    // every element index of one rank's partial fits in 32 bits?
+    if (k.n < ((int64_t)1 << 32) - 64) return reduce_dispatch<PT, OT, uint32_t>(k, vec_ok, tree, gelu, s);
+    return reduce_dispatch<PT, OT, uint64_t>(k, vec_ok, tree, gelu, s);
+}
+
+// All-gather: one read of each source vector, G writes; group g = blockIdx.y.
+template <bool VEC16, typename IT>
+__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherK k, int elem) {
+    const int g = blockIdx.y;
+    const IT total = (IT)k.nvec;
+    const IT bvecs = (IT)k.bvecs, brows = (IT)k.brows, per_block = brows * bvecs;
+    const IT full_vecs = (IT)k.full_vecs;
+    for (IT v = (IT)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (IT)gridDim.x * blockDim.x) {
+        const int p = (int)(v / per_block);
+        const IT w = v - (IT)p * per_block;
+        const IT r = w / bvecs, c = w - r * bvecs;
         const int p0 = p / k.blocks1, p1 = p - p0 * k.blocks1;
-        const int64_t src_off = r * k.bvecs + c;
-        const int64_t dst_off = ((int64_t)p0 * k.brows + r) * k.full_vecs + (int64_t)p1 * k.bvecs + c;
+        const IT src_off = w;
+        const IT dst_off = ((IT)p0 * brows + r) * full_vecs + (IT)p1 * bvecs + c;
         if (VEC16) {
             const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(k.src[g * k.G + p]) + src_off);
             for (int m = 0; m < k.G; ++m) __stcs(reinterpret_cast<uint4 *>(k.dst[g * k.G + m]) + dst_off, x);
+        } else if (elem == 4) {  // element-wise: "vectors" are single elements
+            const uint32_t x = reinterpret_cast<const uint32_t *>(k.src[g * k.G + p])[src_off];
+            for (int m = 0; m < k.G; ++m) reinterpret_cast<uint32_t *>(k.dst[g * k.G + m])[dst_off] = x;
         } else {
-            // element-wise: "vectors" are single elements of `elem` bytes
-            if (elem == 4) {
-                const uint32_t x = reinterpret_cast<const uint32_t *>(k.src[g * k.G + p])[src_off];
-                for (int m = 0; m < k.G; ++m) reinterpret_cast<uint32_t *>(k.dst[g * k.G + m])[dst_off] = x;
-            } else {
-                const uint16_t x = reinterpret_cast<const uint16_t *>(k.src[g * k.G + p])[src_off];
-                for (int m = 0; m < k.G; ++m) reinterpret_cast<uint16_t *>(k.dst[g * k.G + m])[dst_off] = x;
-            }
+            const uint16_t x = reinterpret_cast<const uint16_t *>(k.src[g * k.G + p])[src_off];
+            for (int m = 0; m < k.G; ++m) reinterpret_cast<uint16_t *>(k.dst[g * k.G + m])[dst_off] = x;
         }
     }
 }
@@ -395,10 +425,10 @@ int launch_reduce(const ReduceArgs &a, int *status, void *stream) {
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
     count_launch();
-    if (a.pt == SHMM_F32 && a.ot == SHMM_F32) e = reduce_dispatch<float, float>(k, vec_ok, a.tree, a.gelu, s);
-    else if (a.pt == SHMM_F32) e = reduce_dispatch<float, __nv_bfloat16>(k, vec_ok, a.tree, a.gelu, s);
-    else if (a.ot == SHMM_BF16) e = reduce_dispatch<__nv_bfloat16, __nv_bfloat16>(k, vec_ok, a.tree, a.gelu, s);
-    else e = reduce_dispatch<__nv_bfloat16, float>(k, vec_ok, a.tree, a.gelu, s);
+    if (a.pt == SHMM_F32 && a.ot == SHMM_F32) e = reduce_dispatch_idx<float, float>(k, vec_ok, a.tree, a.gelu, s);
+    else if (a.pt == SHMM_F32) e = reduce_dispatch_idx<float, __nv_bfloat16>(k, vec_ok, a.tree, a.gelu, s);
+    else if (a.ot == SHMM_BF16) e = reduce_dispatch_idx<__nv_bfloat16, __nv_bfloat16>(k, vec_ok, a.tree, a.gelu, s);
+    else e = reduce_dispatch_idx<__nv_bfloat16, float>(k, vec_ok, a.tree, a.gelu, s);
     return (int)e;
 }
 
@@ -421,10 +451,18 @@ int launch_gather(const GatherArgs &a, int *status, void *stream) {
     k.full_vecs = (int64_t)a.blocks1 * k.bvecs;
     k.nvec = (int64_t)a.G * a.brows * k.bvecs;
     cudaStream_t s = (cudaStream_t)stream;
-    const unsigned grid = grid_for(k.nvec * k.ngroups, 256 * 2);
+    const dim3 grid = grid_for(k.nvec, 256 * 2, k.ngroups);
+    const int elem = (int)a.elem;
+    const bool small = k.nvec < ((int64_t)1 << 32) - 64 &&
+                       (int64_t)a.blocks0 * a.brows * k.full_vecs < ((int64_t)1 << 32) - 64;
     count_launch();
-    if (vec) gather_kernel<true><<<grid, 256, 0, s>>>(k, a.elem);
-    else gather_kernel<false><<<grid, 256, 0, s>>>(k, a.elem);
+    if (vec) {
+        if (small) gather_kernel<true, uint32_t><<<grid, 256, 0, s>>>(k, elem);
+        else gather_kernel<true, uint64_t><<<grid, 256, 0, s>>>(k, elem);
+    } else {
+        if (small) gather_kernel<false, uint32_t><<<grid, 256, 0, s>>>(k, elem);
+        else gather_kernel<false, uint64_t><<<grid, 256, 0, s>>>(k, elem);
+    }
     return (int)cudaGetLastError();
 }
 

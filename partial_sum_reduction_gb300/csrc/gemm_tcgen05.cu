@@ -181,6 +181,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+        " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+        " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
 __device__ __forceinline__ float gelu_tanh(float x) {
     const float inner = 0.7978845608028654f * (x + 0.044715f * x * x * x);
     return 0.5f * x * (1.0f + tanhf(inner));
@@ -241,7 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int Gq = k.fused ? k.G : 1;
-    const int nsets = (512 / (Gq * BN)) >= 2 ? 2 : 1;
     const int tiles_per_unit = k.m_tiles * k.n_tiles;
     const int total = k.units * tiles_per_unit;
 
@@ -325,18 +343,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
+        // Two TMEM buffers of BN columns.  Tile i (this CTA's i-th) keeps its
+        // running sum S in buffer i%2; ranks 1..G-1 of the tile are computed
+        // in the other buffer W.  A buffer is refilled only after the
+        // epilogue released its previous contents.
         if (lane == 0) {
             constexpr uint32_t idesc = instr_desc(BN);
             uint32_t it = 0;
+            uint32_t fills0 = 0, fills1 = 0;
             int tile_iter = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_iter) {
-                const int set = tile_iter % nsets;
-                const uint32_t aph = (tile_iter / nsets) & 1;
-                if (!mbar_wait(acce_bar(set), aph ^ 1, abort_flag, k.status)) break;
-                fence_after();
+                const int bS = tile_iter & 1;
                 for (int q = 0; q < Gq && ok; ++q) {
-                    const uint32_t d_tmem = tmem_base + (uint32_t)((set * Gq + q) * BN);
+                    const int b = (q == 0) ? bS : (bS ^ 1);
+                    const uint32_t nf = b ? fills1 : fills0;
+                    if (!mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
                     for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
@@ -357,8 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         }
                         umma_commit(empty_bar(s));
                     }
+                    if (!ok) break;
+                    umma_commit(accf_bar(b));
+                    if (b) ++fills1;
+                    else ++fills0;
                 }
-                if (ok) umma_commit(accf_bar(set));
             }
             // Drain: every MMA issued by this thread has completed.
             umma_commit(drain_bar);
@@ -370,32 +400,55 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int row_in_tile = quad * 32 + lane;
         const bool f32 = k.out_f32 != 0;
         const int64_t es = f32 ? 4 : 2;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+        uint32_t used0 = 0, used1 = 0;  // finished products consumed per buffer
+        // One lane waits; the warp reconverges before the .sync.aligned TMEM
+        // instructions.
+        auto warp_wait_full = [&](int b) -> bool {
+            const uint32_t n = b ? used1 : used0;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(accf_bar(b), n & 1, abort_flag, k.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (b) ++used1;
+            else ++used0;
+            if (ok) fence_after();
+            return ok != 0;
+        };
         int tile_iter = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_iter) {
             int unit, mt, nt;
             decode(t, &unit, &mt, &nt);
-            const int set = tile_iter % nsets;
-            const uint32_t aph = (tile_iter / nsets) & 1;
-            // One lane waits; the warp reconverges before the .sync.aligned
-            // TMEM loads.
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(accf_bar(set), aph, abort_flag, k.status) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const int bS = tile_iter & 1, bW = bS ^ 1;
+            const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
+            const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
+            if (!warp_wait_full(bS)) break;  // S = product of the group's first rank
+            bool ok = true;
+            for (int q = 1; q < Gq; ++q) {
+                // S = S + P_q in fp32: the ascending-rank sequential sum
+                if (!warp_wait_full(bW)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float a[32], w[32];
+                    tmem_ld32(s_base + (uint32_t)(c * 32), a);
+                    tmem_ld32(w_base + (uint32_t)(c * 32), w);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = a[i] + w[i];
+                    tmem_st32(s_base + (uint32_t)(c * 32), a);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                fence_before();
+                mbar_arrive(acce_bar(bW));  // W may take the next product
+            }
             if (!ok) break;
-            fence_after();
             const int64_t row = (int64_t)mt * BM + row_in_tile;
             const bool row_ok = row < k.M;
-            const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 float v[32];
-                tmem_ld32(lane_base + (uint32_t)(set * Gq * BN + c * 32), v);
-                for (int q = 1; q < Gq; ++q) {
-                    float w[32];
-                    tmem_ld32(lane_base + (uint32_t)((set * Gq + q) * BN + c * 32), w);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = v[i] + w[i];
-                }
+                tmem_ld32(s_base + (uint32_t)(c * 32), v);
                 if (k.gelu) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
@@ -434,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             }
             fence_before();
-            mbar_arrive(acce_bar(set));
+            mbar_arrive(acce_bar(bS));  // S may take the next tile's products
         }
     }
 
@@ -519,7 +572,7 @@ namespace shmm {
 bool tcgen05_supported(const GemmArgs &a) {
     const int G = a.fused ? a.G : 1;
     return a.in_dt == SHMM_BF16 && a.M > 0 && a.N > 0 && a.Kd > 0 && a.Kd % 8 == 0 &&
-           a.N % 8 == 0 && G <= 8 && a.M <= ((int64_t)1 << 31) && a.N <= ((int64_t)1 << 31) &&
+           a.N % 8 == 0 && G <= kMaxMaps && a.M <= ((int64_t)1 << 31) && a.N <= ((int64_t)1 << 31) &&
            a.Kd <= ((int64_t)1 << 31);
 }
 
@@ -527,7 +580,7 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
     EncodeTiledFn fn = encode_fn(msg);
     if (!fn) return (int)cudaErrorNotSupported;
     const int G = a.fused ? a.G : 1;
-    const int bn = G == 1 ? 256 : (G == 2 ? 256 : (G <= 4 ? 128 : 64));
+    constexpr int bn = 256;
     const int per_launch = kMaxMaps / G;  // units per launch
     cudaStream_t s = (cudaStream_t)stream;
     for (int u0 = 0; u0 < a.units; u0 += per_launch) {
@@ -556,12 +609,7 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         k.Kd = a.Kd;
         k.m_tiles = (int)((a.M + BM - 1) / BM);
         k.k_blocks = (int)((a.Kd + BK - 1) / BK);
-        cudaError_t e;
-        switch (bn) {
-            case 256: e = launch_bn<256>(k, s); break;
-            case 128: e = launch_bn<128>(k, s); break;
-            default: e = launch_bn<64>(k, s); break;
-        }
+        const cudaError_t e = launch_bn<bn>(k, s);
         if (e != cudaSuccess) return (int)e;
     }
     return 0;

@@ -312,7 +312,7 @@ shmm_status_t shmm_plan(const shmm_mesh_t *mesh, const shmm_spec_t *spec_A,
                      al.ext[1] > 0 && bl.ext[1] > 0 && al.ext[1] % 8 == 0 && bl.ext[1] % 8 == 0;
 
     p->fused = p->U.n > 0 && (flags & SHMM_FLAG_FUSED) &&
-               (!p->tensor_core || p->red_groups.size <= 8);
+               (!p->tensor_core || p->red_groups.size <= 16);
 
     guard.owned = nullptr;
     *plan_out = p;

@@ -6,7 +6,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/shmm.h"
+#include "shmm.h"
 
 namespace shmm {
 
@@ -69,8 +69,8 @@ struct shmm_plan {
     int scatter_dim = -1;
     bool tensor_core = false;
     // Reduction runs in the GEMM epilogue: SHMM_FLAG_FUSED, partial sums to
-    // reduce, and (on tensor cores) at most 8 ranks per group, the number of
-    // fp32 accumulators TMEM holds side by side.
+    // reduce, and (on tensor cores) at most 16 ranks per group, the operand
+    // descriptors one launch carries.
     bool fused = false;
     std::vector<shmm::Box> boxes[7];          // [shmm_tensor_t][rank]
     shmm::Groups red_groups, gA_groups, gB_groups, gC_groups;

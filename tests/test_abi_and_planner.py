@@ -215,6 +215,8 @@ def test_workspace_accounting(shmm):
     assert p.workspace_size() == 4 * 256 * 128 * 4
     p = shmm.Plan("{X:2,Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 256, 256, 128, "bf16", "bf16", shmm.FLAG_FUSED)
     assert p.workspace_size() == 0 and p.info.fused == 1
-    # more than 8 ranks per group: the tensor-core path reduces unfused
+    # up to 16 ranks per group fuse on the tensor cores; more reduce unfused
     p = shmm.Plan("{X:16}", "I,J_X", "J_X,K", "I,K", 256, 256, 128, "bf16", "bf16", shmm.FLAG_FUSED)
-    assert p.info.fused == 0 and p.workspace_size() == 16 * 256 * 128 * 4
+    assert p.info.fused == 1 and p.workspace_size() == 0
+    p = shmm.Plan("{X:32}", "I,J_X", "J_X,K", "I,K", 256, 256, 128, "bf16", "bf16", shmm.FLAG_FUSED)
+    assert p.info.fused == 0 and p.workspace_size() == 32 * 256 * 128 * 4

@@ -220,7 +220,7 @@ def test_mlp_pair_full_size_sampled(s, sY):
 
 # -------------------------------------------- collectives on given partials
 
-@pytest.mark.parametrize("G", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("G", [2, 3, 4, 5, 8, 12, 16])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("order", ["sequential", "pairwise"])
 @pytest.mark.parametrize("numel", [1 << 16, 4099 * 8])
