@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -200,6 +201,67 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
         : "memory");
 }
 
+
+// ---- CTA-pair (cluster of 2) helpers for the cta_group::2 kernel ---------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (here: the leader's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma2_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at this shared offset in both CTAs of the pair once
+// every cta_group::2 MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma2_commit_both(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
+        : "memory");
+}
+
+// Instruction descriptor for the pair MMA: M = 256 (128 rows per CTA).
+__host__ __device__ constexpr uint32_t instr_desc_pair(int bn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
 __device__ __forceinline__ float gelu_tanh(float x) {
     const float inner = 0.7978845608028654f * (x + 0.044715f * x * x * x);
     return 0.5f * x * (1.0f + tanhf(inner));
@@ -232,6 +294,42 @@ __device__ __forceinline__ void store_run(void *p, const float *v, int n, bool f
             }
         } else {
             for (int i = 0; i < n; ++i) d[i] = __float2bfloat16_rn(v[i]);
+        }
+    }
+}
+
+// Writes n (<= 32) finished values of output row `row`, columns col0.., of
+// unit `unit`: the rank's own block (unfused), the owner's block of a
+// reduce-scatter along rows (mode 0) or columns (mode 1), or every group
+// member's copy (mode 2).
+__device__ __forceinline__ void store_tile_row(const TcK &k, int unit, int Gq, int64_t row, int64_t col0,
+                                               const float *v, int n, bool f32, int64_t es) {
+    if (!k.fused) {
+        char *p = (char *)k.out[unit] + (row * k.N + col0) * es;
+        store_run(p, v, n, f32, true);
+    } else if (k.mode == 0) {
+        const int64_t per = k.M / Gq;
+        const int b = (int)(row / per);
+        char *p = (char *)k.out[unit * Gq + b] + ((row - b * per) * k.N + col0) * es;
+        store_run(p, v, n, f32, true);
+    } else if (k.mode == 1) {
+        const int64_t per = k.N / Gq;
+        if ((per % 32) == 0) {
+            const int b = (int)(col0 / per);
+            char *p = (char *)k.out[unit * Gq + b] + (row * per + (col0 - b * per)) * es;
+            store_run(p, v, n, f32, true);
+        } else {
+            for (int i = 0; i < n; ++i) {
+                const int64_t col = col0 + i;
+                const int b = (int)(col / per);
+                char *p = (char *)k.out[unit * Gq + b] + (row * per + (col - b * per)) * es;
+                store_run(p, v + i, 1, f32, false);
+            }
+        }
+    } else {
+        for (int b = 0; b < Gq; ++b) {
+            char *p = (char *)k.out[unit * Gq + b] + (row * k.N + col0) * es;
+            store_run(p, v, n, f32, true);
         }
     }
 }
@@ -456,35 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const int64_t col0 = (int64_t)nt * BN + c * 32;
                 if (!row_ok || col0 >= k.N) continue;
                 const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
-                if (!k.fused) {
-                    char *p = (char *)k.out[unit] + (row * k.N + col0) * es;
-                    store_run(p, v, n, f32, true);
-                } else if (k.mode == 0) {
-                    const int64_t per = k.M / Gq;
-                    const int b = (int)(row / per);
-                    char *p = (char *)k.out[unit * Gq + b] + ((row - b * per) * k.N + col0) * es;
-                    store_run(p, v, n, f32, true);
-                } else if (k.mode == 1) {
-                    const int64_t per = k.N / Gq;
-                    const bool vec = (per % 32) == 0;
-                    if (vec) {
-                        const int b = (int)(col0 / per);
-                        char *p = (char *)k.out[unit * Gq + b] + (row * per + (col0 - b * per)) * es;
-                        store_run(p, v, n, f32, true);
-                    } else {
-                        for (int i = 0; i < n; ++i) {
-                            const int64_t col = col0 + i;
-                            const int b = (int)(col / per);
-                            char *p = (char *)k.out[unit * Gq + b] + (row * per + (col - b * per)) * es;
-                            store_run(p, v + i, 1, f32, false);
-                        }
-                    }
-                } else {
-                    for (int b = 0; b < Gq; ++b) {
-                        char *p = (char *)k.out[unit * Gq + b] + (row * k.N + col0) * es;
-                        store_run(p, v, n, f32, true);
-                    }
-                }
+                store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
             }
             fence_before();
             mbar_arrive(acce_bar(bS));  // S may take the next tile's products
@@ -496,6 +566,256 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     fence_after();
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
+                     : "memory");
+    }
+}
+
+
+// ---- CTA-pair kernel: 256x256 output tiles on two SMs ---------------------
+//
+// A cluster of two CTAs computes one 256x256 tile with tcgen05.mma
+// cta_group::2 (M = 256, N = 256, K = 16): each CTA stages its own 128 rows of
+// A and its 128 of the tile's 256 columns of B, so a CTA moves 32 KB per
+// k-block instead of the 48 KB of a 128x256 single-CTA tile, and the pair's
+// accumulator is split by rows over the two TMEMs.  The even CTA (the
+// leader) issues the MMAs; both CTAs' TMA loads complete on the leader's
+// full barrier; the leader's commits reach both CTAs' barriers.  Each CTA's
+// epilogue drains its own 128 rows exactly as in the single-CTA kernel.
+
+struct Cfg2 {
+    static constexpr int A_BYTES = BM * BK * 2;   // 16 KB: this CTA's 128 rows
+    static constexpr int B_BYTES = BK * 128 * 2;  // 16 KB: this CTA's 128 columns
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGES = 6;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcK k) {
+    using C = Cfg2;
+    constexpr int S = C::STAGES;
+    constexpr int BN = 256;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *tiles = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::STAGE);
+    // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t cr = cluster_ctarank();  // 0: leader, 1: peer
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int Gq = k.fused ? k.G : 1;
+    const int tiles_per_unit = k.m_tiles * k.n_tiles;  // 256x256 tiles
+    const int total = k.units * tiles_per_unit;
+
+    auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+    auto empty_bar = [&](int s) { return smem_u32(&bars[S + s]); };
+    auto accf_bar = [&](int s) { return smem_u32(&bars[2 * S + s]); };
+    auto acce_bar = [&](int s) { return smem_u32(&bars[2 * S + 2 + s]); };
+    const uint32_t drain_bar = smem_u32(&bars[2 * S + 4]);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(accf_bar(s), 1);
+            mbar_init(acce_bar(s), 2 * 4 * 32);  // both CTAs' epilogue threads
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        // collective over the pair: the same columns in both TMEMs
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_u32(tmem_holder))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any remote use
+    fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    auto decode = [&](int t, int *unit, int *mt, int *nt) {
+        *unit = t / tiles_per_unit;
+        const int r = t - *unit * tiles_per_unit;
+        *mt = r % k.m_tiles;
+        *nt = r / k.m_tiles;
+    };
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs) ----------------
+        if (lane == 0) {
+            for (int i = 0; i < k.units * Gq && i < kMaxMaps; ++i) {
+                prefetch_map(&k.tmA[i]);
+                prefetch_map(&k.tmB[i]);
+            }
+            uint32_t it = 0;
+            int last_parity[8];
+            for (int s = 0; s < 8; ++s) last_parity[s] = -1;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                int unit, mt, nt;
+                decode(t, &unit, &mt, &nt);
+                for (int q = 0; q < Gq && ok; ++q) {
+                    const int ri = unit * Gq + q;
+                    for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
+                        const int s = it % S;
+                        const uint32_t ph = (it / S) & 1;
+                        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, k.status)) {
+                            ok = false;
+                            break;
+                        }
+                        if (cr == 0) mbar_expect_tx(full_bar(s), 2 * C::STAGE);
+                        const uint32_t bar = mapa_shared(full_bar(s), 0);
+                        const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
+                        const uint32_t b_dst = a_dst + C::A_BYTES;
+                        tma_load_2d_pair(a_dst, &k.tmA[ri], bar, kb * BK, mt * 256 + (int)cr * BM);
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_2d_pair(b_dst + c * 8192, &k.tmB[ri], bar,
+                                             nt * BN + (int)cr * 128 + c * 64, kb * BK);
+                        last_parity[s] = (int)ph;
+                    }
+                }
+            }
+            if (cr == 0) {
+                // both CTAs' loads of a stage complete on the leader's barrier
+                for (int s = 0; s < S; ++s)
+                    if (last_parity[s] >= 0)
+                        mbar_wait(full_bar(s), (uint32_t)last_parity[s], abort_flag, k.status, false);
+            } else if (!ok) {
+                // aborted: let this CTA's own loads land before it can exit
+                for (int i = 0; i < 200; ++i) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (leader CTA only) ----------------
+        if (lane == 0 && cr == 0) {
+            constexpr uint32_t idesc = instr_desc_pair(BN);
+            uint32_t it = 0;
+            uint32_t fills0 = 0, fills1 = 0;
+            int tile_iter = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs, ++tile_iter) {
+                const int bS = tile_iter & 1;
+                for (int q = 0; q < Gq && ok; ++q) {
+                    const int b = (q == 0) ? bS : (bS ^ 1);
+                    const uint32_t nf = b ? fills1 : fills0;
+                    if (!mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+                    for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
+                        const int s = it % S;
+                        const uint32_t ph = (it / S) & 1;
+                        if (!mbar_wait(full_bar(s), ph, abort_flag, k.status)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+                        const uint32_t a_addr = smem_u32(tiles + s * C::STAGE);
+                        const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
+                            const uint64_t bd = smem_desc(b_addr + kk * 2048, 8192, 1024);
+                            umma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma2_commit_both(empty_bar(s));
+                    }
+                    if (!ok) break;
+                    umma2_commit_both(accf_bar(b));
+                    if (b) ++fills1;
+                    else ++fills0;
+                }
+            }
+            umma2_commit_both(drain_bar);
+            mbar_wait(drain_bar, 0, abort_flag, k.status, false);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        const int quad = warp % 4;
+        const int row_in_tile = (int)cr * BM + quad * 32 + lane;
+        const bool f32 = k.out_f32 != 0;
+        const int64_t es = f32 ? 4 : 2;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+        uint32_t used0 = 0, used1 = 0;
+        auto warp_wait_full = [&](int b) -> bool {
+            const uint32_t n = b ? used1 : used0;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(accf_bar(b), n & 1, abort_flag, k.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (b) ++used1;
+            else ++used0;
+            if (ok) fence_after();
+            return ok != 0;
+        };
+        auto release = [&](int b) {
+            fence_before();
+            mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));  // the leader's barrier
+        };
+        int tile_iter = 0;
+        for (int t = pair; t < total; t += npairs, ++tile_iter) {
+            int unit, mt, nt;
+            decode(t, &unit, &mt, &nt);
+            const int bS = tile_iter & 1, bW = bS ^ 1;
+            const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
+            const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
+            if (!warp_wait_full(bS)) break;
+            bool ok = true;
+            for (int q = 1; q < Gq; ++q) {
+                if (!warp_wait_full(bW)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float a[32], w[32];
+                    tmem_ld32(s_base + (uint32_t)(c * 32), a);
+                    tmem_ld32(w_base + (uint32_t)(c * 32), w);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = a[i] + w[i];
+                    tmem_st32(s_base + (uint32_t)(c * 32), a);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                release(bW);
+            }
+            if (!ok) break;
+            const int64_t row = (int64_t)mt * 256 + row_in_tile;
+            const bool row_ok = row < k.M;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                tmem_ld32(s_base + (uint32_t)(c * 32), v);
+                if (k.gelu) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                }
+                const int64_t col0 = (int64_t)nt * BN + c * 32;
+                if (!row_ok || col0 >= k.N) continue;
+                const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
+                store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
+            }
+            release(bS);
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while its peer may still signal it
+    fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
                      : "memory");
     }
 }
@@ -565,6 +885,63 @@ cudaError_t launch_bn(TcK &k, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Launches the CTA-pair kernel: clusters of two, at most as many pairs as can
+// be resident at once (one CTA per SM).
+cudaError_t launch_pair(TcK &k, cudaStream_t s) {
+    using C = Cfg2;
+    static bool attr_set[64] = {};
+    static int max_pairs[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool cache = dev >= 0 && dev < 64;
+    if (!cache || !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t q = {};
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = 2;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.gridDim = dim3((unsigned)(num_sms() & ~1));
+        q.blockDim = dim3(kThreads);
+        q.dynamicSmemBytes = C::SMEM;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &q);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorNotSupported;
+        if (!cache) return cudaErrorInvalidDevice;
+        max_pairs[dev] = n;
+        attr_set[dev] = true;
+    }
+    const int cap = max_pairs[dev];
+    k.m_tiles = (int)((k.M + 255) / 256);
+    k.n_tiles = (int)((k.N + 255) / 256);
+    const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
+    const int npairs = (int)(total < cap ? total : cap);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * npairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    shmm::count_launch();
+    return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, k);
+}
+
+bool pair_kernel_enabled() {
+    const char *e = getenv("SHMM_TC_PAIR");
+    return !(e && e[0] == '0');
+}
+
 }  // namespace
 
 namespace shmm {
@@ -609,7 +986,8 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         k.Kd = a.Kd;
         k.m_tiles = (int)((a.M + BM - 1) / BM);
         k.k_blocks = (int)((a.Kd + BK - 1) / BK);
-        const cudaError_t e = launch_bn<bn>(k, s);
+        // 256-row tiles on CTA pairs unless the local M fits one 128-row tile
+        const cudaError_t e = (a.M > BM && pair_kernel_enabled()) ? launch_pair(k, s) : launch_bn<bn>(k, s);
         if (e != cudaSuccess) return (int)e;
     }
     return 0;

@@ -75,10 +75,13 @@ def test_worked_example_on_gpu(s, golden):
 
 # --------------------------------------------- local GEMM (tensor cores)
 
+@pytest.mark.parametrize("pair", ["1", "0"])
 @pytest.mark.parametrize("M,Kd,N", [(128, 64, 256), (300, 200, 328), (520, 1032, 264), (7, 16, 8),
-                                    (256, 4096, 512), (129, 72, 1000)])
-def test_local_gemm_partials(s, M, Kd, N):
-    """Several tiles, ragged tails in all three dims, partial k-blocks."""
+                                    (256, 4096, 512), (129, 72, 1000), (700, 136, 600)])
+def test_local_gemm_partials(s, M, Kd, N, pair, monkeypatch):
+    """Several tiles, ragged tails in all three dims, partial k-blocks; the
+    CTA-pair kernel (256-row tiles, for M > 128) and the single-CTA kernel."""
+    monkeypatch.setenv("SHMM_TC_PAIR", pair)
     from partial_sum_reduction_gb300 import helpers as H
     A, B = shmm_inputs.scaled_normal_pair(M, 2 * Kd, N, "bf16", seed=M + N)
     p = s.Plan(Y2, ((), ("Y",)), (("Y",), ()), ((), ()), M, 2 * Kd, N, "bf16", "bf16")
@@ -120,7 +123,9 @@ FOUR = [
 
 @pytest.mark.parametrize("case,sA,sB,sC", FOUR)
 @pytest.mark.parametrize("fused", [False, True])
-def test_four_cases(s, case, sA, sB, sC, fused):
+@pytest.mark.parametrize("pair", ["1", "0"])
+def test_four_cases(s, case, sA, sB, sC, fused, pair, monkeypatch):
+    monkeypatch.setenv("SHMM_TC_PAIR", pair)
     A, B = shmm_inputs.scaled_normal_pair(512, 384, 640, "bf16", seed=case)
     plan, gpu = run_gpu(XY22, sA, sB, sC, A, B, "bf16", "bf16", s.FLAG_FUSED if fused else 0)
     assert plan.info.case_id == case
@@ -315,7 +320,9 @@ def test_operand_all_gather_bit_exact(s):
 
 # -------------------------------------------------------------- invariants
 
-def test_fused_equals_unfused_bitwise(s):
+@pytest.mark.parametrize("pair", ["1", "0"])
+def test_fused_equals_unfused_bitwise(s, pair, monkeypatch):
+    monkeypatch.setenv("SHMM_TC_PAIR", pair)
     A, B = shmm_inputs.scaled_normal_pair(640, 1024, 512, "bf16", seed=12)
     for mesh, sA, sB, sC in ((Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ())),
                              (XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ())),
