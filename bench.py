@@ -64,6 +64,29 @@ FOUR_CASES = [
 ]
 
 
+# DRAM bytes per launch of the dominant kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, one pass, full-size launch;
+# profiles/gemm_tc2_fused_down_projection_quarter.md gives the command), valid
+# only for the kernel source it was taken on.
+NCU_TRAFFIC = {
+    "down_projection": {"kernel_sha256_16": "29a33455fe55b903", "bytes": 8.75e9 + 0.29659e9,
+                        "kernel": "gemm_tc2_kernel"},
+}
+
+
+def kernel_traffic(workload):
+    import hashlib
+    rec = NCU_TRAFFIC.get(workload)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for name in ("gemm_tcgen05.cu", "device_wait.cuh"):
+        with open(os.path.join(ROOT, "partial_sum_reduction_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()[:16]
+    return rec["bytes"] if sha == rec["kernel_sha256_16"] else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -281,38 +304,59 @@ def _smi_bus_id(bus):
     return bus
 
 
-def time_e2e(wl, steps, dist_ctx):
-    """End to end through the public API: each step copies every rank's
-    inputs from pinned host memory, runs, and copies every rank's result
-    back to pinned host memory; all inside the timed region."""
+def _pool_views(tensors, device, pin=False):
+    """Lays ``tensors`` out back to back (256-byte aligned) in one byte pool;
+    returns the pool and a view of it per tensor."""
     import torch
-    ins = wl.input_tensors()
-    outs = wl.output_tensors()
-    h_in = [t.cpu().pin_memory() for t in ins]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    offs, off = [], 0
+    for t in tensors:
+        offs.append(off)
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    pool = torch.empty(max(off, 1), dtype=torch.uint8, device=device, pin_memory=pin)
+    views = [pool[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+    return pool, views
+
+
+def time_e2e(wl, steps, dist_ctx):
+    """End to end through the public API: every step copies all ranks'
+    inputs from one pinned host buffer to the device (one copy), runs the
+    sharded matmul, and copies all ranks' results back to pinned host memory
+    (one copy), all inside the timed region.  The per-rank buffers are
+    256-byte-aligned slices of one device allocation per direction."""
+    import torch
+    ins, outs = wl.input_tensors(), wl.output_tensors()
+    d_in, v_in = _pool_views(ins, "cuda")
+    d_out, v_out = _pool_views(outs, "cuda")
+    for v, t in zip(v_in, ins):
+        v.copy_(t)
+    h_in = torch.empty(d_in.numel(), dtype=torch.uint8, pin_memory=True)
+    h_in.copy_(d_in)
+    h_out = torch.empty(d_out.numel(), dtype=torch.uint8, pin_memory=True)
+    remap = {id(t): v for t, v in zip(ins + outs, v_in + v_out)}
+    specs = [(p, [remap.get(id(t), t) for t in A_r], [remap.get(id(t), t) for t in B_r],
+              [remap.get(id(t), t) for t in C_r], ws) for p, A_r, B_r, C_r, ws in wl.steps_spec]
     stream = torch.cuda.current_stream()
-    h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def one_step():
+        d_in.copy_(h_in, non_blocking=True)
+        for p, A_r, B_r, C_r, ws in specs:
+            p.run(A_r, B_r, C_r, ws, stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
+
     for _ in range(2):
-        for d, h in zip(ins, h_in):
-            d.copy_(h, non_blocking=True)
-        wl.step(stream)
-        for h, d in zip(h_out, outs):
-            h.copy_(d, non_blocking=True)
+        one_step()
     torch.cuda.synchronize()
     dist_ctx.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(steps):
-        for d, h in zip(ins, h_in):
-            d.copy_(h, non_blocking=True)
-        wl.step(stream)
-        for h, d in zip(h_out, outs):
-            h.copy_(d, non_blocking=True)
+        one_step()
     t1.record(stream)
     torch.cuda.synchronize()
     ms = dist_ctx.max(t0.elapsed_time(t1)) / steps
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
     return ms, h2d, d2h
 
 
@@ -512,12 +556,18 @@ def run_shmm(args, dist_ctx):
                    "l2": "inputs larger than L2 (%.2f GB of per-rank operands per step)" % (wl.input_bytes() / 1e9),
                    "flop_per_step": wl.flops, "replicas": N},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": kernel_traffic(args.workload),
+                     "traffic_unit": "DRAM bytes per launch (ncu)",
+                     "algorithmic_bytes": wl.input_bytes() + sum(t.numel() * t.element_size()
+                                                                 for t in wl.output_tensors()),
                      "peak_kind": "%s bf16 burst (cuBLAS 8192^3)" % peak_kind,
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                     "kernel": "gemm_tc_kernel<256> fused all-reduce epilogue"},
+                     "kernel": ("gemm_tc2_kernel (CTA pair) with fused reduction epilogue"
+                                if os.environ.get("SHMM_TC_PAIR", "1") != "0"
+                                else "gemm_tc_kernel<256> with fused reduction epilogue")},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms, "host_link_GB_s": (h2d + d2h) / (e2e_ms * 1e-3) / 1e9,
+                "note": "one pinned H2D copy of all ranks' operands, shmm_run, one D2H copy of all results"},
         "gpu_launches": launches,
         "clocks": clocks,
         "reduce_scatter": {"value": rs["GB_s"], "unit": "GB/s", "frac": rs["GB_s"] / peaks["hbm_gbs"],

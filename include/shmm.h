@@ -301,6 +301,16 @@ shmm_status_t shmm_run_static_workspace(const shmm_plan_t *plan, const void *con
  * or SHMM_ERR_CUDA. */
 shmm_status_t shmm_sync_status(void *stream);
 
+/* Failure-detection self-test: enqueues one kernel that waits on a barrier
+ * nothing arrives at, through the same bounded wait every pipeline wait of
+ * this library uses, with a limit of `limit_cycles` SM clock cycles
+ * (1e3..4e9; the pipelines use ~4e9, about 2 s).  The wait gives up, records
+ * SHMM_ERR_TIMEOUT in the device status word and the kernel returns: the next
+ * shmm_sync_status() reports SHMM_ERR_TIMEOUT and clears it, and the context
+ * stays usable.  No counterpart on the pages: a test of this library's own
+ * fault handling.  Errors: SHAPE (limit out of range), CUDA. */
+shmm_status_t shmm_selftest_wait_timeout(uint64_t limit_cycles, void *stream);
+
 /* Message for the calling thread's last failed call ("" if none). */
 const char *shmm_last_error(void);
 

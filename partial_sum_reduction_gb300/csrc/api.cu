@@ -9,6 +9,7 @@
 #include <string>
 #include <vector>
 
+#include "device_wait.cuh"
 #include "shmm_internal.h"
 
 using shmm::fail;
@@ -63,6 +64,20 @@ void *static_workspace_ptr(std::string *err) {
         cached[dev] = p;
     }
     return cached[dev];
+}
+
+// A wait on an mbarrier that nothing ever arrives at, through the same
+// bounded wait the pipelines use: it gives up after `limit` cycles and
+// records SHMM_ERR_TIMEOUT.
+__global__ void selftest_wait_kernel(int *status, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        shmm_dev::mbar_init(shmm_dev::smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        shmm_dev::mbar_wait(shmm_dev::smem_u32(&bar), 0, &abort_flag, status, true, limit);
+    }
 }
 
 // SHMM_INJECT_FAIL="name1,name2": those entry points fail before enqueuing.
@@ -418,6 +433,21 @@ shmm_status_t shmm_run_static_workspace(const shmm_plan_t *p, const void *const 
         if (!ws) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
     }
     return shmm_run(p, A_r, B_r, C_r, ws, need, stream);
+}
+
+shmm_status_t shmm_selftest_wait_timeout(uint64_t limit_cycles, void *stream) {
+    static const char *fn = "shmm_selftest_wait_timeout";
+    shmm::clear_error();
+    if (limit_cycles < 1000 || limit_cycles > 4000000000ull)
+        return fail(SHMM_ERR_SHAPE, std::string(fn) + ": limit must be in [1e3, 4e9] cycles");
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    shmm::count_launch();
+    selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status, (long long)limit_cycles);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(fn, e);
+    return SHMM_OK;
 }
 
 shmm_status_t shmm_sync_status(void *stream) {

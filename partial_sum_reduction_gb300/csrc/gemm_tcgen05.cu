@@ -36,6 +36,7 @@
 #include <mutex>
 #include <string>
 
+#include "device_wait.cuh"
 #include "shmm_internal.h"
 
 namespace {
@@ -45,7 +46,6 @@ constexpr int BK = 64;           // bf16 per k-block: one 128-byte swizzle row
 constexpr int UMMA_K = 16;       // K of one tcgen05.mma kind::f16
 constexpr int kMaxMaps = 16;     // rank operand pairs per launch
 constexpr int kThreads = 192;
-constexpr long long kWaitLimit = 4000000000LL;  // SM cycles (~2 s)
 
 struct TcK {
     CUtensorMap tmA[kMaxMaps];
@@ -60,53 +60,7 @@ struct TcK {
 
 // ---- PTX wrappers ------------------------------------------------------
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait.  Returns false if the abort flag is raised (by this or
-// another thread) or the wait outlives kWaitLimit, which raises it.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int *status, bool honour_abort = true) {
-    long long t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if (it == 0) t0 = clock64();
-        if ((it & 31) == 31) {
-            if (honour_abort && *abort_flag) return false;
-            if (clock64() - t0 > kWaitLimit) {
-                *abort_flag = 1;
-                atomicExch(status, (int)SHMM_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
+using namespace shmm_dev;
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int32_t c0, int32_t c1) {

@@ -69,7 +69,8 @@ class ShmmError(RuntimeError):
 EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_box",
            "shmm_plan_group", "shmm_workspace_size", "shmm_local_matmul", "shmm_reduce_scatter",
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
-           "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace"]
+           "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace",
+           "shmm_selftest_wait_timeout"]
 
 _lib = None
 
@@ -102,6 +103,7 @@ def lib():
         L.shmm_run.argtypes = [P, PP, PP, PP, P, ctypes.c_size_t, P]
         L.shmm_run_static_workspace.argtypes = [P, PP, PP, PP, P]
         L.shmm_sync_status.argtypes = [P]
+        L.shmm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
         L.shmm_last_error.restype = ctypes.c_char_p
         L.shmm_status_string.argtypes = [ctypes.c_int]
         L.shmm_status_string.restype = ctypes.c_char_p
@@ -364,6 +366,10 @@ STATIC_WORKSPACE_BYTES = 64 << 20
 
 def shmm_sync_status(stream=None) -> None:
     _check(lib().shmm_sync_status(_stream_handle(stream)))
+
+
+def shmm_selftest_wait_timeout(limit_cycles: int, stream=None) -> None:
+    _check(lib().shmm_selftest_wait_timeout(int(limit_cycles), _stream_handle(stream)))
 
 
 def shmm_version() -> int:

@@ -387,3 +387,21 @@ def test_outputs_stay_inside_their_boxes(s):
             base = r * (n + 2 * guard)
             assert torch.all(host[base:base + guard] == -7.0)
             assert torch.all(host[base + guard + n:base + 2 * guard + n] == -7.0)
+
+
+# ------------------------------------------------------- failure detection
+
+def test_bounded_wait_reports_timeout_and_context_survives(s):
+    """A wait that runs out (a barrier nothing arrives at, ~10 ms limit) is
+    reported through the device status word; the next read is clean and the
+    context still computes correctly."""
+    s.shmm_sync_status()
+    s.shmm_selftest_wait_timeout(20_000_000)
+    with pytest.raises(s.ShmmError) as e:
+        s.shmm_sync_status()
+    assert e.value.status == s.shmm.ERR_TIMEOUT
+    s.shmm_sync_status()  # cleared
+    A, B = shmm_inputs.split_k_integer(64, 64, 64, seed=1)
+    plan, gpu = run_gpu(Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, "f32", "f32", s.FLAG_FUSED)
+    _, ores = oracle_run(Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, "f32")
+    compare(plan, gpu, ores, exact=True)
