@@ -111,10 +111,15 @@ typedef struct {
 } shmm_spec_t;
 
 /* Plan flags */
-#define SHMM_FLAG_FUSED 0x1u   /* shmm_run: reduce in the GEMM epilogue; each
-                                  output tile is summed over its reduction
-                                  group in ascending rank order and written
-                                  once to its owner(s) */
+#define SHMM_FLAG_FUSED 0x1u   /* shmm_run: fuse the collectives into the GEMM.
+                                  Partial sums are reduced in the epilogue:
+                                  each output tile is summed over its
+                                  reduction group in ascending rank order and
+                                  written once to its owner(s).  Operand
+                                  all-gathers (cases 2, 4) become in-place
+                                  reads of the owners' shards by the GEMM's
+                                  loads, where shard edges allow
+                                  (info.fused_gather) */
 #define SHMM_FLAG_GELU 0x2u    /* apply GeLU (tanh form) to the finished result
                                   before the output rounding (the column-
                                   parallel first matmul of an MLP pair) */
@@ -173,6 +178,11 @@ typedef struct {
     int64_t payload_reduce_scatter;
     int64_t payload_result_ag;
     size_t workspace_bytes;              /* shmm_run's workspace requirement */
+    int fused_gather;      /* 1 if shmm_run reads the case 2/4 operands in
+                              place from their owners' shards inside the GEMM
+                              (SHMM_FLAG_FUSED, tensor cores, shard edges on
+                              64-column / 128-row boundaries, <= 16 ranks)
+                              instead of all-gathering them first */
 } shmm_plan_info_t;
 
 typedef struct shmm_plan shmm_plan_t;

@@ -123,6 +123,10 @@ shmm::GemmArgs gemm_args(const shmm_plan_t *p) {
 
 int run_gemm(const shmm_plan_t *p, const shmm::GemmArgs &g, int *status, void *stream, std::string *msg) {
     if (p->tensor_core && shmm::tcgen05_supported(g)) return shmm::launch_gemm_tcgen05(g, status, stream, msg);
+    if (g.A_src || g.B_src) {  // in-place gathers exist only on the tensor-core path
+        *msg = "in-place operand gather needs the tensor-core GEMM";
+        return (int)cudaErrorNotSupported;
+    }
     return shmm::launch_gemm_simt(g, status, stream);
 }
 
@@ -354,18 +358,50 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
     std::vector<const void *> A_loc(A_r, A_r + p->nranks), B_loc(B_r, B_r + p->nranks);
     std::vector<void *> wa, wb, wp, wc;
     int e = 0;
-    if (p->gA.n) {
+    if (p->gA.n && !p->fused_gather) {
         carve(SHMM_TENSOR_A_LOCAL, in_b, &wa);
         e = gather(p, p->gA_groups, SHMM_TENSOR_A, in_b, A_r, wa.data(), status, stream);
         if (e) return cuda_fail(fn, e, "gather A");
         for (int r = 0; r < p->nranks; ++r) A_loc[r] = wa[r];
     }
-    if (p->gB.n) {
+    if (p->gB.n && !p->fused_gather) {
         carve(SHMM_TENSOR_B_LOCAL, in_b, &wb);
         e = gather(p, p->gB_groups, SHMM_TENSOR_B, in_b, B_r, wb.data(), status, stream);
         if (e) return cuda_fail(fn, e, "gather B");
         for (int r = 0; r < p->nranks; ++r) B_loc[r] = wb[r];
     }
+    // In-place gather: per GEMM operand slot (a rank), the shard of each
+    // block of its all-gather group, in grid order.
+    std::vector<const void *> a_src, b_src;
+    auto shard_table = [&](const shmm::Groups &g, const void *const *shards, const std::vector<int> &slot_rank,
+                           std::vector<const void *> *out) {
+        out->assign(slot_rank.size() * g.size, nullptr);
+        for (size_t i = 0; i < slot_rank.size(); ++i) {
+            int gi = 0;
+            for (size_t j = 0; j < g.members.size(); ++j)
+                if (g.members[j] == slot_rank[i]) gi = (int)j / g.size;
+            for (int q = 0; q < g.size; ++q) (*out)[i * g.size + q] = shards[g.by_block[gi * g.size + q]];
+        }
+    };
+    auto attach_gather = [&](shmm::GemmArgs *ga, const std::vector<int> &slot_rank) {
+        if (!p->fused_gather) return;
+        if (p->gA.n) {
+            shard_table(p->gA_groups, A_r, slot_rank, &a_src);
+            ga->A_src = a_src.data();
+            ga->a_b0 = p->gA_groups.blocks0;
+            ga->a_b1 = p->gA_groups.blocks1;
+            ga->a_brows = p->boxes[SHMM_TENSOR_A][0].ext[0];
+            ga->a_bcols = p->boxes[SHMM_TENSOR_A][0].ext[1];
+        }
+        if (p->gB.n) {
+            shard_table(p->gB_groups, B_r, slot_rank, &b_src);
+            ga->B_src = b_src.data();
+            ga->b_b0 = p->gB_groups.blocks0;
+            ga->b_b1 = p->gB_groups.blocks1;
+            ga->b_brows = p->boxes[SHMM_TENSOR_B][0].ext[0];
+            ga->b_bcols = p->boxes[SHMM_TENSOR_B][0].ext[1];
+        }
+    };
     const bool fused = p->fused;
     if (p->U.n && !fused) carve(SHMM_TENSOR_P, shmm::elem_bytes(p->part_dt), &wp);
     std::vector<void *> dst(C_r, C_r + p->nranks);
@@ -374,8 +410,19 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         dst = wc;
     }
     const bool gelu = (p->flags & SHMM_FLAG_GELU) != 0;
+    std::vector<int> by_rank(p->nranks);
+    for (int r = 0; r < p->nranks; ++r) by_rank[r] = r;
     if (!p->U.n) {
-        e = gemm_unfused(p, A_loc.data(), B_loc.data(), dst.data(), p->out_dt, gelu, status, stream, &err);
+        shmm::GemmArgs ga = gemm_args(p);
+        ga.units = p->nranks;
+        ga.G = 1;
+        ga.out_dt = p->out_dt;
+        ga.gelu = gelu;
+        ga.A = A_loc.data();
+        ga.B = B_loc.data();
+        ga.out = dst.data();
+        attach_gather(&ga, by_rank);
+        e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
     } else if (fused) {
         const shmm::Groups &g = p->red_groups;
@@ -396,10 +443,19 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         ga.A = fa.data();
         ga.B = fb.data();
         ga.out = fo.data();
+        attach_gather(&ga, g.members);
         e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
     } else {
-        e = gemm_unfused(p, A_loc.data(), B_loc.data(), wp.data(), p->part_dt, false, status, stream, &err);
+        shmm::GemmArgs ga = gemm_args(p);
+        ga.units = p->nranks;
+        ga.G = 1;
+        ga.out_dt = p->part_dt;
+        ga.A = A_loc.data();
+        ga.B = B_loc.data();
+        ga.out = wp.data();
+        attach_gather(&ga, by_rank);
+        e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
         const int mode = p->collective == SHMM_COLL_REDUCE_SCATTER ? p->scatter_dim : 2;
         e = reduce(p, (const void *const *)wp.data(), dst.data(), mode, status, stream);

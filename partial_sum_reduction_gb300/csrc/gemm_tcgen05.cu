@@ -48,7 +48,7 @@ constexpr int kMaxMaps = 16;     // rank operand pairs per launch
 constexpr int kThreads = 192;
 
 struct TcK {
-    CUtensorMap tmA[kMaxMaps];
+    CUtensorMap tmA[kMaxMaps];   // one map per distinct A shard of the launch
     CUtensorMap tmB[kMaxMaps];
     void *out[kMaxMaps];
     int *status;
@@ -56,7 +56,30 @@ struct TcK {
     int fused, gelu, out_f32;
     int64_t M, N, Kd;
     int m_tiles, n_tiles, k_blocks;
+    // operand slot i's block p (row-major over a b0 x b1 grid of brows x bcols
+    // shards) is map a_idx[i][p]; an operand read whole has one 1x1 block
+    uint8_t a_idx[kMaxMaps][kMaxMaps];
+    uint8_t b_idx[kMaxMaps][kMaxMaps];
+    int a_b0, a_b1, b_b0, b_b1;
+    int64_t a_brows, a_bcols, b_brows, b_bcols;
+    int n_maps_a, n_maps_b;
 };
+
+// Which shard map holds element (row, col) of an operand read in place from
+// an all-gather group's shards, and its coordinates there.  Boxes never
+// straddle a shard (the planner only fuses when shard edges fall on box
+// edges); coordinates past the operand's end stay past the last shard's end,
+// where TMA fills zeros.
+__device__ __forceinline__ int shard_of(const uint8_t *idx, int b0, int b1, int64_t brows, int64_t bcols,
+                                        int64_t row, int64_t col, int32_t *srow, int32_t *scol) {
+    int p0 = b0 > 1 ? (int)(row / brows) : 0;
+    int p1 = b1 > 1 ? (int)(col / bcols) : 0;
+    if (p0 > b0 - 1) p0 = b0 - 1;
+    if (p1 > b1 - 1) p1 = b1 - 1;
+    *srow = (int32_t)(row - (int64_t)p0 * brows);
+    *scol = (int32_t)(col - (int64_t)p1 * bcols);
+    return idx[p0 * b1 + p1];
+}
 
 // ---- PTX wrappers ------------------------------------------------------
 
@@ -356,10 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            for (int i = 0; i < k.units * Gq && i < kMaxMaps; ++i) {
-                prefetch_map(&k.tmA[i]);
-                prefetch_map(&k.tmB[i]);
-            }
+            for (int i = 0; i < k.n_maps_a; ++i) prefetch_map(&k.tmA[i]);
+            for (int i = 0; i < k.n_maps_b; ++i) prefetch_map(&k.tmB[i]);
             uint32_t it = 0;
             int last_parity[8];
             for (int s = 0; s < 8; ++s) last_parity[s] = -1;
@@ -379,11 +400,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         mbar_expect_tx(full_bar(s), C::STAGE);
                         const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
                         const uint32_t b_dst = a_dst + C::A_BYTES;
-                        tma_load_2d(a_dst, &k.tmA[ri], full_bar(s), kb * BK, mt * BM);
+                        int32_t r0, c0;
+                        int m = shard_of(k.a_idx[ri], k.a_b0, k.a_b1, k.a_brows, k.a_bcols,
+                                         (int64_t)mt * BM, (int64_t)kb * BK, &r0, &c0);
+                        tma_load_2d(a_dst, &k.tmA[m], full_bar(s), c0, r0);
 #pragma unroll
-                        for (int c = 0; c < BN / 64; ++c)
-                            tma_load_2d(b_dst + c * 8192, &k.tmB[ri], full_bar(s), nt * BN + c * 64,
-                                        kb * BK);
+                        for (int c = 0; c < BN / 64; ++c) {
+                            m = shard_of(k.b_idx[ri], k.b_b0, k.b_b1, k.b_brows, k.b_bcols, (int64_t)kb * BK,
+                                         (int64_t)nt * BN + c * 64, &r0, &c0);
+                            tma_load_2d(b_dst + c * 8192, &k.tmB[m], full_bar(s), c0, r0);
+                        }
                         last_parity[s] = (int)ph;
                     }
                 }
@@ -607,10 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
         if (lane == 0) {
-            for (int i = 0; i < k.units * Gq && i < kMaxMaps; ++i) {
-                prefetch_map(&k.tmA[i]);
-                prefetch_map(&k.tmB[i]);
-            }
+            for (int i = 0; i < k.n_maps_a; ++i) prefetch_map(&k.tmA[i]);
+            for (int i = 0; i < k.n_maps_b; ++i) prefetch_map(&k.tmB[i]);
             uint32_t it = 0;
             int last_parity[8];
             for (int s = 0; s < 8; ++s) last_parity[s] = -1;
@@ -631,11 +655,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
                         const uint32_t bar = mapa_shared(full_bar(s), 0);
                         const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
                         const uint32_t b_dst = a_dst + C::A_BYTES;
-                        tma_load_2d_pair(a_dst, &k.tmA[ri], bar, kb * BK, mt * 256 + (int)cr * BM);
+                        int32_t r0, c0;
+                        int m = shard_of(k.a_idx[ri], k.a_b0, k.a_b1, k.a_brows, k.a_bcols,
+                                         (int64_t)mt * 256 + (int)cr * BM, (int64_t)kb * BK, &r0, &c0);
+                        tma_load_2d_pair(a_dst, &k.tmA[m], bar, c0, r0);
 #pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            tma_load_2d_pair(b_dst + c * 8192, &k.tmB[ri], bar,
-                                             nt * BN + (int)cr * 128 + c * 64, kb * BK);
+                        for (int c = 0; c < 2; ++c) {
+                            m = shard_of(k.b_idx[ri], k.b_b0, k.b_b1, k.b_brows, k.b_bcols, (int64_t)kb * BK,
+                                         (int64_t)nt * BN + (int)cr * 128 + c * 64, &r0, &c0);
+                            tma_load_2d_pair(b_dst + c * 8192, &k.tmB[m], bar, c0, r0);
+                        }
                         last_parity[s] = (int)ph;
                     }
                 }
@@ -918,14 +947,60 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         const int nu = (a.units - u0) < per_launch ? (a.units - u0) : per_launch;
         TcK k;
         memset(&k, 0, sizeof k);
+        // One tensor map per distinct operand buffer (a shard may serve
+        // every member of its all-gather group); per slot, a block table.
+        const void *ptrs_a[kMaxMaps], *ptrs_b[kMaxMaps];
+        int na = 0, nb = 0;
+        auto map_of = [&](const void *ptr, const void **ptrs, int *n, CUtensorMap *maps, int64_t rows,
+                          int64_t cols, uint32_t bx, uint32_t by) -> int {
+            for (int j = 0; j < *n; ++j)
+                if (ptrs[j] == ptr) return j;
+            if (*n >= kMaxMaps) return -1;
+            if (!make_map(fn, &maps[*n], ptr, rows, cols, bx, by)) return -2;
+            ptrs[*n] = ptr;
+            return (*n)++;
+        };
+        const int a_nb = a.A_src ? a.a_b0 * a.a_b1 : 1;
+        const int b_nb = a.B_src ? a.b_b0 * a.b_b1 : 1;
+        const int64_t a_rows = a.A_src ? a.a_brows : a.M, a_cols = a.A_src ? a.a_bcols : a.Kd;
+        const int64_t b_rows = a.B_src ? a.b_brows : a.Kd, b_cols = a.B_src ? a.b_bcols : a.N;
+        if (a_nb > kMaxMaps || b_nb > kMaxMaps) {
+            if (msg) *msg = "all-gather group larger than one launch's operand maps";
+            return (int)cudaErrorInvalidValue;
+        }
         for (int i = 0; i < nu * G; ++i) {
             const int gi = u0 * G + i;
-            if (!make_map(fn, &k.tmA[i], a.A[gi], a.M, a.Kd, BK, BM) ||
-                !make_map(fn, &k.tmB[i], a.B[gi], a.Kd, a.N, 64, BK)) {
-                if (msg) *msg = "cuTensorMapEncodeTiled rejected an operand";
-                return (int)cudaErrorInvalidValue;
+            for (int p = 0; p < a_nb; ++p) {
+                const void *ptr = a.A_src ? a.A_src[(size_t)gi * a_nb + p] : a.A[gi];
+                const int m = map_of(ptr, ptrs_a, &na, k.tmA, a_rows, a_cols, BK, BM);
+                if (m < 0) {
+                    if (msg) *msg = m == -1 ? "more than 16 distinct A buffers in one launch"
+                                            : "cuTensorMapEncodeTiled rejected an A operand";
+                    return (int)cudaErrorInvalidValue;
+                }
+                k.a_idx[i][p] = (uint8_t)m;
+            }
+            for (int p = 0; p < b_nb; ++p) {
+                const void *ptr = a.B_src ? a.B_src[(size_t)gi * b_nb + p] : a.B[gi];
+                const int m = map_of(ptr, ptrs_b, &nb, k.tmB, b_rows, b_cols, 64, BK);
+                if (m < 0) {
+                    if (msg) *msg = m == -1 ? "more than 16 distinct B buffers in one launch"
+                                            : "cuTensorMapEncodeTiled rejected a B operand";
+                    return (int)cudaErrorInvalidValue;
+                }
+                k.b_idx[i][p] = (uint8_t)m;
             }
         }
+        k.n_maps_a = na;
+        k.n_maps_b = nb;
+        k.a_b0 = a.A_src ? a.a_b0 : 1;
+        k.a_b1 = a.A_src ? a.a_b1 : 1;
+        k.b_b0 = a.B_src ? a.b_b0 : 1;
+        k.b_b1 = a.B_src ? a.b_b1 : 1;
+        k.a_brows = a_rows;
+        k.a_bcols = a_cols;
+        k.b_brows = b_rows;
+        k.b_bcols = b_cols;
         const int nout = a.fused ? nu * G : nu;
         for (int i = 0; i < nout; ++i) k.out[i] = a.out[(a.fused ? u0 * G : u0) + i];
         k.status = status;

@@ -313,6 +313,19 @@ shmm_status_t shmm_plan(const shmm_mesh_t *mesh, const shmm_spec_t *spec_A,
 
     p->fused = p->U.n > 0 && (flags & SHMM_FLAG_FUSED) &&
                (!p->tensor_core || p->red_groups.size <= 16);
+    // The operand all-gathers fuse into the GEMM's loads when every TMA box
+    // (64 columns, 64 or 128 rows) lies inside one shard.
+    {
+        const Box &a = p->boxes[SHMM_TENSOR_A][0], &b = p->boxes[SHMM_TENSOR_B][0];
+        const Groups &ga = p->gA_groups, &gb = p->gB_groups;
+        const bool a_ok = (ga.blocks1 == 1 || a.ext[1] % 64 == 0) && (ga.blocks0 == 1 || a.ext[0] % 128 == 0) &&
+                          a.ext[1] % 8 == 0;
+        const bool b_ok = (gb.blocks0 == 1 || b.ext[0] % 64 == 0) && (gb.blocks1 == 1 || b.ext[1] % 64 == 0) &&
+                          b.ext[1] % 8 == 0;
+        p->fused_gather = (flags & SHMM_FLAG_FUSED) && p->tensor_core && (p->gA.n || p->gB.n) &&
+                          p->nranks <= 16 && (p->gA.n == 0 || a_ok) && (p->gB.n == 0 || b_ok) &&
+                          a.numel() > 0 && b.numel() > 0;
+    }
 
     guard.owned = nullptr;
     *plan_out = p;
@@ -329,8 +342,8 @@ shmm_status_t shmm_workspace_size(const shmm_plan_t *p, size_t *bytes) {
     auto slot = [](int64_t b) { return (size_t)((b + 255) / 256 * 256); };
     size_t ws = 0;
     const int64_t in_b = shmm::elem_bytes(p->in_dt), out_b = shmm::elem_bytes(p->out_dt);
-    if (p->gA.n) ws += p->nranks * slot(p->boxes[SHMM_TENSOR_A_LOCAL][0].numel() * in_b);
-    if (p->gB.n) ws += p->nranks * slot(p->boxes[SHMM_TENSOR_B_LOCAL][0].numel() * in_b);
+    if (p->gA.n && !p->fused_gather) ws += p->nranks * slot(p->boxes[SHMM_TENSOR_A_LOCAL][0].numel() * in_b);
+    if (p->gB.n && !p->fused_gather) ws += p->nranks * slot(p->boxes[SHMM_TENSOR_B_LOCAL][0].numel() * in_b);
     if (p->U.n && !p->fused)
         ws += p->nranks *
               slot(p->boxes[SHMM_TENSOR_P][0].numel() * shmm::elem_bytes(p->part_dt));
@@ -357,6 +370,7 @@ shmm_status_t shmm_plan_query(const shmm_plan_t *p, shmm_plan_info_t *info) {
     info->flags = p->flags;
     info->tensor_core = p->tensor_core ? 1 : 0;
     info->fused = p->fused ? 1 : 0;
+    info->fused_gather = p->fused_gather ? 1 : 0;
     const Box &al = p->boxes[SHMM_TENSOR_A_LOCAL][0];
     const Box &bl = p->boxes[SHMM_TENSOR_B_LOCAL][0];
     info->local_I = al.ext[0];

@@ -68,6 +68,10 @@ struct shmm_plan {
     int collective = SHMM_COLL_NONE;
     int scatter_dim = -1;
     bool tensor_core = false;
+    // Case 2/4 operands are read from their owners' shards by the GEMM's TMA
+    // producer (SHMM_FLAG_FUSED, tensor cores, every TMA box inside one shard,
+    // at most 16 ranks) instead of being all-gathered into the workspace.
+    bool fused_gather = false;
     // Reduction runs in the GEMM epilogue: SHMM_FLAG_FUSED, partial sums to
     // reduce, and (on tensor cores) at most 16 ranks per group, the operand
     // descriptors one launch carries.
@@ -130,6 +134,16 @@ struct GemmArgs {
     const void *const *A = nullptr;
     const void *const *B = nullptr;
     void *const *out = nullptr;
+    // Operands read in place from the shards of their all-gather group
+    // (tensor cores only): the local operand of slot i is a b0 x b1 grid of
+    // brows x bcols shards, shard p at A_src[i * b0 * b1 + p] (row-major
+    // grid).  NULL: the operand is A[i] (B[i]) itself.
+    const void *const *A_src = nullptr;
+    int a_b0 = 1, a_b1 = 1;
+    int64_t a_brows = 0, a_bcols = 0;
+    const void *const *B_src = nullptr;
+    int b_b0 = 1, b_b1 = 1;
+    int64_t b_brows = 0, b_bcols = 0;
 };
 int launch_gemm_simt(const GemmArgs &a, int *status, void *stream);
 bool tcgen05_supported(const GemmArgs &a);

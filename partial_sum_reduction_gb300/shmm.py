@@ -57,7 +57,7 @@ class shmm_plan_info_t(ctypes.Structure):
                 ("local_I", ctypes.c_int64), ("local_J", ctypes.c_int64), ("local_K", ctypes.c_int64),
                 ("flops_per_rank", ctypes.c_int64), ("payload_operand_ag", ctypes.c_int64),
                 ("payload_reduce_scatter", ctypes.c_int64), ("payload_result_ag", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("fused_gather", ctypes.c_int)]
 
 
 class ShmmError(RuntimeError):

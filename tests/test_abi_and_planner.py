@@ -220,3 +220,25 @@ def test_workspace_accounting(shmm):
     assert p.info.fused == 1 and p.workspace_size() == 0
     p = shmm.Plan("{X:32}", "I,J_X", "J_X,K", "I,K", 256, 256, 128, "bf16", "bf16", shmm.FLAG_FUSED)
     assert p.info.fused == 0 and p.workspace_size() == 32 * 256 * 128 * 4
+
+
+def test_in_place_gather_decision(shmm):
+    """SHMM_FLAG_FUSED reads case 2/4 operands from their owners' shards when
+    every TMA box lies inside one shard; otherwise the all-gather stays."""
+    F = shmm.FLAG_FUSED
+    p = shmm.Plan("{X:2,Y:2}", "I,J_X", "J,K", "I,K", 256, 256, 128, "bf16", "bf16", F)
+    assert p.info.fused_gather == 1 and p.workspace_size() == 0
+    p = shmm.Plan("{X:2,Y:2}", "I_X,J", "J,K_X", "I_X,K", 256, 256, 256, "bf16", "bf16", F)
+    assert p.info.case_id == 4 and p.info.fused_gather == 1 and p.workspace_size() == 0
+    # shard width 96 (not a multiple of 64): gather into the workspace
+    p = shmm.Plan("{X:2,Y:2}", "I,J_X", "J,K", "I,K", 256, 192, 128, "bf16", "bf16", F)
+    assert p.info.fused_gather == 0 and p.workspace_size() == 4 * 256 * 192 * 2
+    # without the flag, or off the tensor cores, nothing fuses
+    p = shmm.Plan("{X:2,Y:2}", "I,J_X", "J,K", "I,K", 256, 256, 128, "bf16", "bf16")
+    assert p.info.fused_gather == 0
+    p = shmm.Plan("{X:2,Y:2}", "I,J_X", "J,K", "I,K", 256, 256, 128, "f32", "f32", F)
+    assert p.info.fused_gather == 0
+    # case 3 and case 4 at once: reduction and gather both fused
+    p = shmm.Plan("{X:2,Y:2}", "I_X,J_Y", "J_Y,K_X", "I_X,K", 512, 256, 256, "bf16", "bf16", F)
+    assert p.info.case_id == 3 and p.info.fused == 1 and p.info.fused_gather == 1
+    assert p.workspace_size() == 0

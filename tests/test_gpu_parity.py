@@ -405,3 +405,37 @@ def test_bounded_wait_reports_timeout_and_context_survives(s):
     plan, gpu = run_gpu(Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, "f32", "f32", s.FLAG_FUSED)
     _, ores = oracle_run(Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, "f32")
     compare(plan, gpu, ores, exact=True)
+
+
+# ------------------------------------------ in-place operand gather (f1)
+
+GATHERS = [
+    ("case2", XY22, ((), ("X",)), ((), ()), ((), ()), 384, 512, 264),
+    ("case4", XY22, (("X",), ()), ((), ("X",)), (("X",), ()), 512, 384, 640),
+    ("case3+4", XY22, (("X",), ("Y",)), (("Y",), ("X",)), (("X",), ()), 512, 512, 512),
+    ("case2_both", XY22, ((), ("X",)), (("Y",), ()), ((), ()), 384, 512, 264),
+]
+
+
+@pytest.mark.parametrize("name,mesh,sA,sB,sC,I,J,K", GATHERS)
+@pytest.mark.parametrize("pair", ["1", "0"])
+def test_in_place_gather_equals_explicit_gather(s, name, mesh, sA, sB, sC, I, J, K, pair, monkeypatch):
+    """Operands read from their owners' shards inside the GEMM give the same
+    bits as all-gathering them first, and match the oracle."""
+    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=I + J)
+    p1, g1 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", 0)
+    p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED)
+    assert p1.info.fused_gather == 0 and p2.info.fused_gather == 1 and p2.workspace_size() == 0
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+    _, ores = oracle_run(mesh, sA, sB, sC, A, B, "f32")
+    compare(p2, g2, ores, exact=False)
+
+
+def test_gather_falls_back_when_shards_straddle_boxes(s):
+    A, B = shmm_inputs.scaled_normal_pair(256, 192, 136, "bf16", seed=3)  # shard width 96
+    plan, gpu = run_gpu(XY22, ((), ("X",)), ((), ()), ((), ()), A, B, "bf16", "bf16", s.FLAG_FUSED)
+    assert plan.info.fused_gather == 0
+    _, ores = oracle_run(XY22, ((), ("X",)), ((), ()), ((), ()), A, B, "bf16")
+    compare(plan, gpu, ores, exact=False)
