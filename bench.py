@@ -253,14 +253,40 @@ class Workload:
         return out
 
 
-def time_device(wl, steps, warmup, dist_ctx):
+def capture_graph(wl):
+    """One step of the hot path captured into a CUDA graph (the plan's
+    kernels with their arguments); replaying it removes the host-side
+    marshalling and launch cost that dominates steps of a few microseconds."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            wl.step(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        wl.step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    return g
+
+
+def time_device(wl, steps, warmup, dist_ctx, graph=False):
     """Device-timed loop: CUDA events on the launching stream, one pair per
     step; inputs (>> L2 for the full-size workloads) stay resident."""
     import torch
     s = wl.s
     stream = torch.cuda.current_stream()
+    step = (lambda st: g.replay()) if graph else wl.step
+    if graph:
+        g = capture_graph(wl)
+        launches_per_step = s.shmm_kernel_launches()
+        wl.step(stream)  # count one step's kernels (a replay does not call the library)
+        torch.cuda.synchronize()
+        launches_per_step = s.shmm_kernel_launches() - launches_per_step
     for _ in range(warmup):
-        wl.step(stream)
+        step(stream)
     torch.cuda.synchronize()
     s.shmm_sync_status(stream)
     dist_ctx.barrier()
@@ -280,12 +306,14 @@ def time_device(wl, steps, warmup, dist_ctx):
     t0.record(stream)
     for i in range(steps):
         ev[i][0].record(stream)
-        wl.step(stream)
+        step(stream)
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     sampler.mark_end()
     launches = s.shmm_kernel_launches() - launches0
+    if graph:
+        launches = launches_per_step * steps
     clocks = sampler.stop()
     s.shmm_sync_status(stream)
     total_ms = t0.elapsed_time(t1)
@@ -535,7 +563,7 @@ def run_shmm(args, dist_ctx):
     from partial_sum_reduction_gb300 import helpers as H
     peaks, peak_kind = load_peaks()
     wl = Workload(args.workload, "cuda")
-    total_ms, per_step, launches, clocks = time_device(wl, args.steps, args.warmup, dist_ctx)
+    total_ms, per_step, launches, clocks = time_device(wl, args.steps, args.warmup, dist_ctx, graph=args.graph)
     ms = total_ms / args.steps
     N = dist_ctx.world
     value = wl.flops * N / (total_ms / args.steps * 1e-3) / 1e12
@@ -553,6 +581,7 @@ def run_shmm(args, dist_ctx):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload]["text"], "name": args.workload,
+                   "launch": "CUDA graph replay" if args.graph else "direct shmm_run calls",
                    "l2": "inputs larger than L2 (%.2f GB of per-rank operands per step)" % (wl.input_bytes() / 1e9),
                    "flop_per_step": wl.flops, "replicas": N},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -611,6 +640,8 @@ def main():
     ap.add_argument("--sweep", default=None, choices=[None, "collectives"])
     ap.add_argument("--sizes", default="1,16,256,1024")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay one captured CUDA graph per step (small workloads are host-bound)")
     ap.add_argument("--reference-budget-s", type=float, default=150.0,
                     help="--impl reference: seconds of oracle work for the whole run")
     args = ap.parse_args()

@@ -840,11 +840,51 @@ bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Encoded tensor maps, reused across calls: a map holds nothing but the
+// address, shape, strides and box it was encoded with, so an entry matching
+// all of them is valid whatever allocation now lives at that address.
+struct MapCacheEntry {
+    const void *ptr;
+    int64_t rows, cols;
+    uint32_t bx, by;
+    bool valid;
+    CUtensorMap map;
+};
+
+bool cached_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+                uint32_t bx, uint32_t by) {
+    constexpr int kEntries = 64;
+    thread_local MapCacheEntry cache[kEntries] = {};
+    thread_local int next = 0;
+    for (int i = 0; i < kEntries; ++i) {
+        const MapCacheEntry &e = cache[i];
+        if (e.valid && e.ptr == base && e.rows == rows && e.cols == cols && e.bx == bx && e.by == by) {
+            *m = e.map;
+            return true;
+        }
+    }
+    MapCacheEntry &e = cache[next];
+    next = (next + 1) % kEntries;
+    e.valid = false;
+    if (!make_map(fn, &e.map, base, rows, cols, bx, by)) return false;
+    e.ptr = base;
+    e.rows = rows;
+    e.cols = cols;
+    e.bx = bx;
+    e.by = by;
+    e.valid = true;
+    *m = e.map;
+    return true;
+}
+
 int num_sms() {
+    static int cached[64] = {};
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         n = 148;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
     return n;
 }
 
@@ -956,7 +996,7 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
             for (int j = 0; j < *n; ++j)
                 if (ptrs[j] == ptr) return j;
             if (*n >= kMaxMaps) return -1;
-            if (!make_map(fn, &maps[*n], ptr, rows, cols, bx, by)) return -2;
+            if (!cached_map(fn, &maps[*n], ptr, rows, cols, bx, by)) return -2;
             ptrs[*n] = ptr;
             return (*n)++;
         };
