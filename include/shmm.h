@@ -280,6 +280,39 @@ shmm_status_t shmm_all_gather(const shmm_plan_t *plan, int tensor, const void *c
 shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const void *const *B_r,
                        void *const *C_r, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- planner: which operand to move ("Sharded matmuls and collectives on
+ * a torus", Which operand to move: the ICI roofline) ---------------------- */
+
+/* Per-device rates of the model: C (dense matmul FLOP/s) and W (bytes/s one
+ * device moves on the mesh axis, e.g. the ICI link rate of an axis, or HBM
+ * bandwidth for virtual ranks sharing one GPU). */
+typedef struct {
+    double flops_per_s;
+    double bytes_per_s;
+} shmm_device_model_t;
+
+typedef struct {
+    int choice;              /* 1: all-gather W; 2: keep W sharded, reshard X
+                                to X[B,D_X], all-reduce the [B,F] partials */
+    int gather_compute_bound;/* strategy 1's matmul outlasts its all-gather
+                                (B > C/W) */
+    double bytes_gather;     /* bytes strategy 1 moves per device: e*D*F */
+    double bytes_reduce;     /* bytes strategy 2 moves per device: 2*e*B*F */
+    double t_gather;         /* modelled seconds, max(communication, compute) */
+    double t_reduce;
+} shmm_operand_choice_t;
+
+/* For X[B,D] . W[D_X,F] on a mesh axis of `axis_size` devices with element
+ * size `elem_bytes`: strategy 1 all-gathers W (e*D*F bytes at W, eq. 5.1)
+ * and computes the whole 2*B*D*F product per device; strategy 2 moves the
+ * activations (an all-reduce of e*B*F bytes, 2V/W, eq. 5.2) and computes
+ * 2*B*D*F/axis_size.  Each strategy costs max(communication, compute)
+ * (communication overlaps the matmul); the cheaper one is returned.  At
+ * large B this picks strategy 2 exactly when D > 2C/W, the page's threshold.
+ * Host only.  Errors: NULL, SHAPE (a size <= 0, rates <= 0). */
+shmm_status_t shmm_choose_operand(int64_t B, int64_t D, int64_t F, int axis_size, int elem_bytes,
+                                  const shmm_device_model_t *device, shmm_operand_choice_t *out);
+
 /* Size of the fixed device workspace behind shmm_run_static_workspace. */
 #define SHMM_STATIC_WORKSPACE_BYTES (64u << 20)
 

@@ -420,6 +420,29 @@ shmm_status_t shmm_plan_group(const shmm_plan_t *p, int rank, int *ranks) {
     return shmm::fail(SHMM_ERR_SHAPE, "shmm_plan_group: rank in no group");
 }
 
+shmm_status_t shmm_choose_operand(int64_t B, int64_t D, int64_t F, int axis_size, int elem_bytes,
+                                  const shmm_device_model_t *dev, shmm_operand_choice_t *out) {
+    shmm::clear_error();
+    if (!dev || !out) return shmm::fail(SHMM_ERR_NULL, "shmm_choose_operand: NULL argument");
+    if (B <= 0 || D <= 0 || F <= 0 || axis_size < 1 || elem_bytes <= 0 || !(dev->flops_per_s > 0) ||
+        !(dev->bytes_per_s > 0))
+        return shmm::fail(SHMM_ERR_SHAPE, "shmm_choose_operand: sizes and rates must be positive");
+    const double C = dev->flops_per_s, W = dev->bytes_per_s, e = (double)elem_bytes;
+    const double b = (double)B, d = (double)D, f = (double)F, n = (double)axis_size;
+    const double flops = 2.0 * b * d * f;
+    // strategy 1: all-gather the weight (V = e*D*F, time V/W), whole product
+    out->bytes_gather = e * d * f;
+    const double comm1 = out->bytes_gather / W, comp1 = flops / C;
+    // strategy 2: all-reduce the [B,F] partials (2V/W with V = e*B*F), 1/n of it
+    out->bytes_reduce = 2.0 * e * b * f;
+    const double comm2 = out->bytes_reduce / W, comp2 = flops / (n * C);
+    out->t_gather = comm1 > comp1 ? comm1 : comp1;
+    out->t_reduce = comm2 > comp2 ? comm2 : comp2;
+    out->gather_compute_bound = comp1 > comm1 ? 1 : 0;
+    out->choice = out->t_reduce < out->t_gather ? 2 : 1;
+    return SHMM_OK;
+}
+
 const char *shmm_status_string(shmm_status_t s) {
     switch (s) {
         case SHMM_OK: return "SHMM_OK";

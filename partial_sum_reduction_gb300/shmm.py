@@ -60,6 +60,16 @@ class shmm_plan_info_t(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("fused_gather", ctypes.c_int)]
 
 
+class shmm_device_model_t(ctypes.Structure):
+    _fields_ = [("flops_per_s", ctypes.c_double), ("bytes_per_s", ctypes.c_double)]
+
+
+class shmm_operand_choice_t(ctypes.Structure):
+    _fields_ = [("choice", ctypes.c_int), ("gather_compute_bound", ctypes.c_int),
+                ("bytes_gather", ctypes.c_double), ("bytes_reduce", ctypes.c_double),
+                ("t_gather", ctypes.c_double), ("t_reduce", ctypes.c_double)]
+
+
 class ShmmError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__("%s: %s" % (_status_name(status), message))
@@ -70,7 +80,7 @@ EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_
            "shmm_plan_group", "shmm_workspace_size", "shmm_local_matmul", "shmm_reduce_scatter",
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
            "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace",
-           "shmm_selftest_wait_timeout"]
+           "shmm_selftest_wait_timeout", "shmm_choose_operand"]
 
 _lib = None
 
@@ -104,6 +114,9 @@ def lib():
         L.shmm_run_static_workspace.argtypes = [P, PP, PP, PP, P]
         L.shmm_sync_status.argtypes = [P]
         L.shmm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
+        L.shmm_choose_operand.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                          ctypes.c_int, ctypes.POINTER(shmm_device_model_t),
+                                          ctypes.POINTER(shmm_operand_choice_t)]
         L.shmm_last_error.restype = ctypes.c_char_p
         L.shmm_status_string.argtypes = [ctypes.c_int]
         L.shmm_status_string.restype = ctypes.c_char_p
@@ -366,6 +379,17 @@ STATIC_WORKSPACE_BYTES = 64 << 20
 
 def shmm_sync_status(stream=None) -> None:
     _check(lib().shmm_sync_status(_stream_handle(stream)))
+
+
+def shmm_choose_operand(B: int, D: int, F: int, axis_size: int, flops_per_s: float, bytes_per_s: float,
+                        elem_bytes: int = 2) -> shmm_operand_choice_t:
+    """Which operand of X[B,D].W[D_X,F] to move: 1 = all-gather W, 2 = keep W
+    sharded and all-reduce the [B,F] partials (see include/shmm.h)."""
+    dev = shmm_device_model_t(float(flops_per_s), float(bytes_per_s))
+    out = shmm_operand_choice_t()
+    _check(lib().shmm_choose_operand(int(B), int(D), int(F), int(axis_size), int(elem_bytes),
+                                     ctypes.byref(dev), ctypes.byref(out)))
+    return out
 
 
 def shmm_selftest_wait_timeout(limit_cycles: int, stream=None) -> None:

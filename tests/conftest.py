@@ -25,7 +25,7 @@ def load_golden(name):
             if not line:
                 continue
             k, v = [s.strip() for s in line.split("=", 1)]
-            if re.fullmatch(r"[\[\]\d,.\-\s]+", v):
+            if re.fullmatch(r"[\[\]\d,.\-+eE\s]+", v) and re.search(r"\d", v):
                 v = eval(v, {"__builtins__": {}})  # numbers and nested lists only
             out[k] = v
     return out

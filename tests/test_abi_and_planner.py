@@ -242,3 +242,25 @@ def test_in_place_gather_decision(shmm):
     p = shmm.Plan("{X:2,Y:2}", "I_X,J_Y", "J_Y,K_X", "I_X,K", 512, 256, 256, "bf16", "bf16", F)
     assert p.info.case_id == 3 and p.info.fused == 1 and p.info.fused_gather == 1
     assert p.workspace_size() == 0
+
+
+def test_operand_choice_reproduces_the_pages_thresholds(shmm, golden):
+    """Strategy 1 (gather W) is compute-bound when B > C/W; at large B
+    strategy 2 (reduce the [B,F] partials) wins exactly when D > 2C/W."""
+    g = golden("p4_operand_choice.txt")
+    for chip in ("v5p_book", "v5p_docs", "ironwood"):
+        W = g[chip + "_W"]
+        C = g[chip + "_intensity"] * W
+        thr = g[chip + "_threshold"]
+        assert thr == 2 * g[chip + "_intensity"]
+        F, n, Bbig = 8192, 4, 10 ** 8
+        assert shmm.shmm_choose_operand(Bbig, thr - 10, F, n, C, W).choice == 1
+        assert shmm.shmm_choose_operand(Bbig, thr + 10, F, n, C, W).choice == 2
+        ci = g[chip + "_intensity"]
+        assert shmm.shmm_choose_operand(ci - 5, 4096, F, n, C, W).gather_compute_bound == 0
+        assert shmm.shmm_choose_operand(ci + 5, 4096, F, n, C, W).gather_compute_bound == 1
+    r = shmm.shmm_choose_operand(1024, 4096, 16384, 4, 1e15, 1e11)
+    assert r.bytes_gather == g["strategy1_bytes_per_DF"] * 4096 * 16384
+    assert r.bytes_reduce == g["strategy2_bytes_per_BF"] * 1024 * 16384
+    with pytest.raises(shmm.ShmmError):
+        shmm.shmm_choose_operand(0, 1, 1, 2, 1e15, 1e11)
