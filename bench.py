@@ -398,7 +398,15 @@ def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False):
     rows = numel // cols
     mesh = [("X", G)]
     fl = s.FLAG_PARTIAL_OUT_DTYPE | (s.FLAG_TREE if tree else 0)
-    if op == "all_gather":
+    if op == "all_to_all":
+        # A[I, J_X] -> A[I_X, J]: each rank reads and writes its V/G once
+        src = [torch.empty((rows, cols // G), dtype=H.TORCH_DTYPES[dtype], device="cuda").uniform_(-1, 1)
+               for _ in range(G)]
+        dst = [torch.empty((rows // G, cols), dtype=H.TORCH_DTYPES[dtype], device="cuda") for _ in range(G)]
+        run = lambda: s.shmm_reshard(mesh, ((), ("X",)), (("X",), ()), rows, cols, dtype, src, dst)
+        V = rows * cols * eb          # the logical array; each rank holds V/G
+        nbytes = 2 * V
+    elif op == "all_gather":
         p = s.Plan(mesh, (("X",), ()), ((), ()), ((), ()), rows, 8, cols, dtype, dtype)
         src = [torch.empty((rows // G, cols), dtype=H.TORCH_DTYPES[dtype], device="cuda").uniform_(-1, 1)
                for _ in range(G)]
@@ -431,7 +439,7 @@ def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False):
         b.synchronize()
         times.append(a.elapsed_time(b))
     t = statistics.median(times)
-    busbw_factor = (G - 1) / G if op != "all_reduce" else 2 * (G - 1) / G
+    busbw_factor = {"all_reduce": 2 * (G - 1) / G, "all_to_all": (G - 1) / G / 4}.get(op, (G - 1) / G)
     return {"op": op, "ranks": G, "MiB_per_rank": mib, "dtype": dtype, "order": "tree" if tree else "sequential",
             "ms_median": t, "ms_best": min(times), "GB_s": nbytes / (t * 1e-3) / 1e9,
             "bytes": nbytes, "busbw_GB_s": (V / (t * 1e-3) / 1e9) * busbw_factor}
@@ -617,13 +625,13 @@ def run_sweep(args):
     from partial_sum_reduction_gb300 import helpers as H
     peaks, kind = load_peaks()
     sizes = [int(x) for x in args.sizes.split(",")]
-    for op in ("reduce_scatter", "all_reduce", "all_gather"):
+    for op in ("reduce_scatter", "all_reduce", "all_gather", "all_to_all"):
         for dtype in ("f32", "bf16"):
             for G in (2, 4, 8, 16):
                 for mib in sizes:
                     if G * mib * (2 if op == "all_reduce" else 1) > 40 * 1024:
                         continue
-                    for tree in ((False, True) if op != "all_gather" else (False,)):
+                    for tree in ((False, True) if op in ("reduce_scatter", "all_reduce") else (False,)):
                         r = time_collective(s, H, torch, op, G, mib, dtype, tree=tree)
                         r["frac_hbm"] = r["GB_s"] / peaks["hbm_gbs"]
                         r["peak_kind"] = kind

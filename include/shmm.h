@@ -280,6 +280,22 @@ shmm_status_t shmm_all_gather(const shmm_plan_t *plan, int tensor, const void *c
 shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const void *const *B_r,
                        void *const *C_r, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Reshard a 2-D array [rows, cols] between two shardings on one mesh:
+ * every rank's block under `spec_to` is assembled from the blocks holding it
+ * under `spec_from` (one read and one write of each element).  This is the
+ * AllToAll of "Sharding Matrix Multiply" (Communication primitives) and of
+ * the torus page (The four collectives): A[I, J_X] -> A[I_X, J] moves which
+ * dim is sharded; it also covers all-gathers (axes dropped) and slicing
+ * (axes added).  Where the source replicates a block, rank r reads the copy
+ * held by the rank that shares its coordinates on the replicated axes.
+ *   src_r[N]  in: box of each rank under spec_from (row-major, dense)
+ *   dst_r[N]  out: box of each rank under spec_to
+ * No plan: host work is O(ranks x source blocks) per call.
+ * Errors: NULL, SHAPE, INVALID_SPEC, DTYPE, ALIGN, CUDA. */
+shmm_status_t shmm_reshard(const shmm_mesh_t *mesh, const shmm_spec_t *spec_from,
+                           const shmm_spec_t *spec_to, int64_t rows, int64_t cols, shmm_dtype_t dtype,
+                           const void *const *src_r, void *const *dst_r, void *stream);
+
 /* ---- planner: which operand to move ("Sharded matmuls and collectives on
  * a torus", Which operand to move: the ICI roofline) ---------------------- */
 

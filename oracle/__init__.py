@@ -495,3 +495,31 @@ def local_flops(mesh: Mesh, sA: Spec, sB: Spec, I: int, J: int, K: int) -> int:
     (_, _), (ain, ajn) = shard_box(mesh, plan.local_A, (I, J), 0)
     (_, _), (_, bkn) = shard_box(mesh, plan.local_B, (J, K), 0)
     return 2 * ain * ajn * bkn
+
+
+def reshard(mesh: Mesh, spec_from: Spec, spec_to: Spec, shards_from: Dict[int, np.ndarray],
+            shape: Tuple[int, int]) -> Dict[int, np.ndarray]:
+    """AllToAll / reshard ("Sharding Matrix Multiply", Communication
+    primitives: move which dim is sharded, A[I,J_X] -> A[I_X,J]): rebuild
+    the array from every rank's block under ``spec_from`` (replicas must
+    agree), then hand each rank its block under ``spec_to``."""
+    check_spec(mesh, spec_from, "from")
+    check_spec(mesh, spec_to, "to")
+    full = np.full(shape, np.nan, dtype=np.float64)
+    for r, blk in shards_from.items():
+        (i0, j0), (n0, n1) = shard_box(mesh, spec_from, shape, r)
+        blk = np.asarray(blk, dtype=np.float64)
+        if blk.shape != (n0, n1):
+            raise ValueError("rank %d: block shape %s, expected %s" % (r, blk.shape, (n0, n1)))
+        sub = full[i0:i0 + n0, j0:j0 + n1]
+        seen = ~np.isnan(sub)
+        if not np.array_equal(sub[seen], blk[seen]):
+            raise ValueError("replicated source blocks disagree")
+        full[i0:i0 + n0, j0:j0 + n1] = blk
+    if np.isnan(full).any():
+        raise ValueError("source blocks do not cover the array")
+    out = {}
+    for r in range(mesh_size(mesh)):
+        (i0, j0), (n0, n1) = shard_box(mesh, spec_to, shape, r)
+        out[r] = full[i0:i0 + n0, j0:j0 + n1].copy()
+    return out

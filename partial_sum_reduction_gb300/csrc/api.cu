@@ -80,13 +80,7 @@ __global__ void selftest_wait_kernel(int *status, long long limit) {
     }
 }
 
-// SHMM_INJECT_FAIL="name1,name2": those entry points fail before enqueuing.
-bool injected(const char *fn) {
-    const char *env = getenv("SHMM_INJECT_FAIL");
-    if (!env || !*env) return false;
-    const std::string list = std::string(",") + env + ",";
-    return list.find(std::string(",") + fn + ",") != std::string::npos;
-}
+using shmm::injected;
 
 shmm_status_t cuda_fail(const char *fn, int e, const std::string &extra = "") {
     std::string m = std::string(fn) + ": " + cudaGetErrorString((cudaError_t)e);

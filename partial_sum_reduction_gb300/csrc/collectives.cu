@@ -394,9 +394,78 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
     }
 }
 
+// ---- reshard: rectangles between rank buffers ------------------------------
+
+constexpr int kMaxRects = 128;
+
+struct CopyK {
+    shmm::CopyRect r[kMaxRects];
+};
+
+// Rectangle blockIdx.y; the CTAs along x stride over its rows x units, a unit
+// being a 16-byte vector (VEC) or one element of `elem` bytes.
+template <bool VEC, typename IT>
+__global__ void __launch_bounds__(256) copy_rects_kernel(const __grid_constant__ CopyK k, int elem) {
+    const shmm::CopyRect &R = k.r[blockIdx.y];
+    const IT per_row = VEC ? (IT)(R.w * elem / 16) : (IT)R.w;
+    const IT total = per_row * (IT)R.h;
+    const IT sld = VEC ? (IT)(R.src_ld * elem / 16) : (IT)R.src_ld;
+    const IT dld = VEC ? (IT)(R.dst_ld * elem / 16) : (IT)R.dst_ld;
+    for (IT v = (IT)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (IT)gridDim.x * blockDim.x) {
+        const IT row = v / per_row, c = v - row * per_row;
+        if (VEC) {
+            const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(R.src) + row * sld + c);
+            __stcs(reinterpret_cast<uint4 *>(R.dst) + row * dld + c, x);
+        } else if (elem == 4) {
+            reinterpret_cast<uint32_t *>(R.dst)[row * dld + c] = reinterpret_cast<const uint32_t *>(R.src)[row * sld + c];
+        } else {
+            reinterpret_cast<uint16_t *>(R.dst)[row * dld + c] = reinterpret_cast<const uint16_t *>(R.src)[row * sld + c];
+        }
+    }
+}
+
 }  // namespace
 
 namespace shmm {
+
+int launch_copy_rects(const CopyRect *rects, int n, int elem, int *status, void *stream) {
+    (void)status;
+    cudaStream_t s = (cudaStream_t)stream;
+    for (int i0 = 0; i0 < n; i0 += kMaxRects) {
+        const int m = (n - i0) < kMaxRects ? (n - i0) : kMaxRects;
+        CopyK k;
+        bool vec = true, small = true;
+        int64_t most = 0;
+        for (int i = 0; i < m; ++i) {
+            const CopyRect &r = rects[i0 + i];
+            k.r[i] = r;
+            vec = vec && (r.w * elem) % 16 == 0 && (r.src_ld * elem) % 16 == 0 && (r.dst_ld * elem) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(r.src) % 16 == 0 && reinterpret_cast<uintptr_t>(r.dst) % 16 == 0;
+            const int64_t items = r.h * r.w;
+            most = items > most ? items : most;
+            small = small && r.h * (r.src_ld > r.dst_ld ? r.src_ld : r.dst_ld) < ((int64_t)1 << 32) - 64;
+        }
+        if (most == 0) continue;
+        const int64_t units = vec ? most * elem / 16 : most;
+        int64_t want = (units + 1023) / 1024;
+        const int64_t cap = (int64_t)sm_count() * 8 / m > 0 ? (int64_t)sm_count() * 8 / m : 1;
+        if (want > cap) want = cap;
+        if (want < 1) want = 1;
+        const dim3 grid((unsigned)want, (unsigned)m, 1);
+        count_launch();
+        if (vec) {
+            if (small) copy_rects_kernel<true, uint32_t><<<grid, 256, 0, s>>>(k, elem);
+            else copy_rects_kernel<true, uint64_t><<<grid, 256, 0, s>>>(k, elem);
+        } else {
+            if (small) copy_rects_kernel<false, uint32_t><<<grid, 256, 0, s>>>(k, elem);
+            else copy_rects_kernel<false, uint64_t><<<grid, 256, 0, s>>>(k, elem);
+        }
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return (int)e;
+    }
+    return 0;
+}
+
 
 int launch_reduce(const ReduceArgs &a, int *status, void *stream) {
     (void)status;

@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -29,6 +30,13 @@ shmm_status_t fail(shmm_status_t st, const std::string &msg) {
     return st;
 }
 void clear_error() { g_last_error.clear(); }
+
+bool injected(const char *fn) {
+    const char *env = getenv("SHMM_INJECT_FAIL");
+    if (!env || !*env) return false;
+    const std::string list = std::string(",") + env + ",";
+    return list.find(std::string(",") + fn + ",") != std::string::npos;
+}
 
 int64_t elem_bytes(shmm_dtype_t t) { return t == SHMM_F32 ? 4 : 2; }
 
@@ -418,6 +426,88 @@ shmm_status_t shmm_plan_group(const shmm_plan_t *p, int rank, int *ranks) {
                 return SHMM_OK;
             }
     return shmm::fail(SHMM_ERR_SHAPE, "shmm_plan_group: rank in no group");
+}
+
+shmm_status_t shmm_reshard(const shmm_mesh_t *mesh, const shmm_spec_t *spec_from,
+                           const shmm_spec_t *spec_to, int64_t rows, int64_t cols, shmm_dtype_t dtype,
+                           const void *const *src_r, void *const *dst_r, void *stream) {
+    using shmm::fail;
+    shmm::clear_error();
+    static const char *fn = "shmm_reshard: ";
+    if (!mesh || !spec_from || !spec_to || !src_r || !dst_r) return fail(SHMM_ERR_NULL, std::string(fn) + "NULL argument");
+    if (dtype != SHMM_F32 && dtype != SHMM_BF16) return fail(SHMM_ERR_DTYPE, std::string(fn) + "dtype must be F32 or BF16");
+    if (rows < 0 || cols < 0 || rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 40))
+        return fail(SHMM_ERR_SHAPE, std::string(fn) + "bad array shape");
+    if (mesh->naxes < 0 || mesh->naxes > SHMM_MAX_AXES) return fail(SHMM_ERR_SHAPE, std::string(fn) + "bad mesh");
+    shmm_plan_t p;
+    p.naxes = mesh->naxes;
+    int64_t n = 1;
+    for (int a = 0; a < mesh->naxes; ++a) {
+        if (mesh->size[a] < 1) return fail(SHMM_ERR_SHAPE, std::string(fn) + "mesh axis size < 1");
+        p.size[a] = mesh->size[a];
+        n *= mesh->size[a];
+        if (n > SHMM_MAX_RANKS) return fail(SHMM_ERR_SHAPE, std::string(fn) + "more than SHMM_MAX_RANKS ranks");
+    }
+    p.nranks = (int)n;
+    Spec2 from, to;
+    std::string why;
+    if (!read_spec(p, spec_from, &from, &why)) return fail(SHMM_ERR_INVALID_SPEC, std::string(fn) + "from: " + why);
+    if (!read_spec(p, spec_to, &to, &why)) return fail(SHMM_ERR_INVALID_SPEC, std::string(fn) + "to: " + why);
+    if (!divides(p, from, rows, cols) || !divides(p, to, rows, cols))
+        return fail(SHMM_ERR_SHAPE, std::string(fn) + "a dim does not split evenly over its axes");
+    const int64_t nb0 = ways(p, from.d[0]), nb1 = ways(p, from.d[1]);
+    const int64_t bh = rows / nb0, bw = cols / nb1;
+    const int64_t eb = shmm::elem_bytes(dtype);
+    for (int r = 0; r < p.nranks; ++r) {
+        const Box sb = box_of(p, from, rows, cols, r), db = box_of(p, to, rows, cols, r);
+        if (sb.numel() && (!src_r[r] || reinterpret_cast<uintptr_t>(src_r[r]) % 16))
+            return fail(src_r[r] ? SHMM_ERR_ALIGN : SHMM_ERR_NULL, std::string(fn) + "src_r[" + std::to_string(r) + "]");
+        if (db.numel() && (!dst_r[r] || reinterpret_cast<uintptr_t>(dst_r[r]) % 16))
+            return fail(dst_r[r] ? SHMM_ERR_ALIGN : SHMM_ERR_NULL, std::string(fn) + "dst_r[" + std::to_string(r) + "]");
+    }
+    if (rows == 0 || cols == 0) return SHMM_OK;
+    // The source sharding cuts the array into nb0 x nb1 blocks; destination
+    // box D of rank r is covered by the blocks it overlaps.  Each overlap is
+    // read from the block's holder that shares r's coordinates on every axis
+    // the source sharding leaves replicated.
+    std::vector<shmm::CopyRect> rects;
+    for (int r = 0; r < p.nranks; ++r) {
+        const Box D = box_of(p, to, rows, cols, r);
+        if (D.numel() == 0) continue;
+        for (int64_t i = D.off[0] / bh; i * bh < D.off[0] + D.ext[0]; ++i)
+            for (int64_t j = D.off[1] / bw; j * bw < D.off[1] + D.ext[1]; ++j) {
+                int c[SHMM_MAX_AXES];
+                for (int a = 0; a < p.naxes; ++a) c[a] = coord(p, r, a);
+                int64_t q = i;
+                for (int t = from.d[0].n - 1; t >= 0; --t) {  // first listed axis major
+                    const int a = from.d[0].ax[t];
+                    c[a] = (int)(q % p.size[a]);
+                    q /= p.size[a];
+                }
+                q = j;
+                for (int t = from.d[1].n - 1; t >= 0; --t) {
+                    const int a = from.d[1].ax[t];
+                    c[a] = (int)(q % p.size[a]);
+                    q /= p.size[a];
+                }
+                int s = 0;
+                for (int a = 0; a < p.naxes; ++a) s = s * p.size[a] + c[a];
+                const int64_t r0 = std::max(D.off[0], i * bh), r1 = std::min(D.off[0] + D.ext[0], (i + 1) * bh);
+                const int64_t c0 = std::max(D.off[1], j * bw), c1 = std::min(D.off[1] + D.ext[1], (j + 1) * bw);
+                shmm::CopyRect cr;
+                cr.src = static_cast<const char *>(src_r[s]) + ((r0 - i * bh) * bw + (c0 - j * bw)) * eb;
+                cr.dst = static_cast<char *>(dst_r[r]) + ((r0 - D.off[0]) * D.ext[1] + (c0 - D.off[1])) * eb;
+                cr.src_ld = bw;
+                cr.dst_ld = D.ext[1];
+                cr.h = r1 - r0;
+                cr.w = c1 - c0;
+                rects.push_back(cr);
+            }
+    }
+    if (shmm::injected("shmm_reshard")) return fail(SHMM_ERR_INJECTED, std::string(fn) + "injected failure");
+    const int e = shmm::launch_copy_rects(rects.data(), (int)rects.size(), (int)eb, nullptr, stream);
+    if (e) return fail(SHMM_ERR_CUDA, std::string(fn) + "kernel launch failed (" + std::to_string(e) + ")");
+    return SHMM_OK;
 }
 
 shmm_status_t shmm_choose_operand(int64_t B, int64_t D, int64_t F, int axis_size, int elem_bytes,

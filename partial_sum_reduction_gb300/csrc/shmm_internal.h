@@ -86,6 +86,8 @@ int64_t elem_bytes(shmm_dtype_t t);
 // Sets the calling thread's last-error message and returns `st`.
 shmm_status_t fail(shmm_status_t st, const std::string &msg);
 void clear_error();
+// SHMM_INJECT_FAIL="name1,name2": those entry points fail before enqueuing.
+bool injected(const char *fn);
 
 // ---- kernel launchers (device code in the .cu files) -------------------
 
@@ -117,6 +119,16 @@ struct GatherArgs {
     void *const *dst = nullptr;
 };
 int launch_gather(const GatherArgs &a, int *status, void *stream);
+
+// Copies rectangles between row-major buffers: rectangle i moves h[i] rows of
+// w[i] elements of `elem` bytes from src[i] (row pitch src_ld[i] elements) to
+// dst[i] (pitch dst_ld[i]).  The reshard (all-to-all) collective.
+struct CopyRect {
+    const void *src;
+    void *dst;
+    int64_t src_ld, dst_ld, h, w;
+};
+int launch_copy_rects(const CopyRect *rects, int n, int elem, int *status, void *stream);
 
 // Local GEMMs.  For unit u (a rank, or a reduction group when fused), the
 // G operand pairs A[u*G+q] (M x Kd, row-major) and B[u*G+q] (Kd x N,

@@ -80,7 +80,7 @@ EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_
            "shmm_plan_group", "shmm_workspace_size", "shmm_local_matmul", "shmm_reduce_scatter",
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
            "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace",
-           "shmm_selftest_wait_timeout", "shmm_choose_operand"]
+           "shmm_selftest_wait_timeout", "shmm_choose_operand", "shmm_reshard"]
 
 _lib = None
 
@@ -114,6 +114,9 @@ def lib():
         L.shmm_run_static_workspace.argtypes = [P, PP, PP, PP, P]
         L.shmm_sync_status.argtypes = [P]
         L.shmm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
+        L.shmm_reshard.argtypes = [ctypes.POINTER(shmm_mesh_t), ctypes.POINTER(shmm_spec_t),
+                                   ctypes.POINTER(shmm_spec_t), ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                   PP, PP, P]
         L.shmm_choose_operand.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                           ctypes.c_int, ctypes.POINTER(shmm_device_model_t),
                                           ctypes.POINTER(shmm_operand_choice_t)]
@@ -379,6 +382,16 @@ STATIC_WORKSPACE_BYTES = 64 << 20
 
 def shmm_sync_status(stream=None) -> None:
     _check(lib().shmm_sync_status(_stream_handle(stream)))
+
+
+def shmm_reshard(mesh, spec_from, spec_to, rows: int, cols: int, dtype: str, src_r, dst_r, stream=None):
+    """All-to-all / reshard of a [rows, cols] array between two shardings
+    (see include/shmm.h); src_r, dst_r are per-rank tensors (or pointers)."""
+    m = _mesh_struct(mesh)
+    a, b = _spec_struct(mesh, spec_from), _spec_struct(mesh, spec_to)
+    _check(lib().shmm_reshard(ctypes.byref(m), ctypes.byref(a), ctypes.byref(b), int(rows), int(cols),
+                              DTYPE_CODES[dtype], _ptr_array(src_r, "src"), _ptr_array(dst_r, "dst"),
+                              _stream_handle(stream)))
 
 
 def shmm_choose_operand(B: int, D: int, F: int, axis_size: int, flops_per_s: float, bytes_per_s: float,

@@ -264,3 +264,24 @@ def test_operand_choice_reproduces_the_pages_thresholds(shmm, golden):
     assert r.bytes_reduce == g["strategy2_bytes_per_BF"] * 1024 * 16384
     with pytest.raises(shmm.ShmmError):
         shmm.shmm_choose_operand(0, 1, 1, 2, 1e15, 1e11)
+
+
+def test_reshard_argument_checks(shmm, monkeypatch):
+    import ctypes
+    good = [0x10000, 0x20000]
+    with pytest.raises(shmm.ShmmError) as e:
+        shmm.shmm_reshard("{X:2}", "I,J_X", "I_X,J_X", 4, 4, "f32", good, good, stream=0)
+    assert e.value.status == shmm.shmm.ERR_INVALID_SPEC
+    with pytest.raises(shmm.ShmmError) as e:
+        shmm.shmm_reshard("{X:2}", "I,J_X", "I_X,J", 3, 4, "f32", good, good, stream=0)
+    assert e.value.status == shmm.shmm.ERR_SHAPE
+    with pytest.raises(shmm.ShmmError) as e:
+        shmm.shmm_reshard("{X:2}", "I,J_X", "I_X,J", 4, 4, "f32", [0x10000, 0], good, stream=0)
+    assert e.value.status == shmm.shmm.ERR_NULL
+    with pytest.raises(shmm.ShmmError) as e:
+        shmm.shmm_reshard("{X:2}", "I,J_X", "I_X,J", 4, 4, "f32", good, [0x10000, 0x20004], stream=0)
+    assert e.value.status == shmm.shmm.ERR_ALIGN
+    monkeypatch.setenv("SHMM_INJECT_FAIL", "shmm_reshard")
+    with pytest.raises(shmm.ShmmError) as e:
+        shmm.shmm_reshard("{X:2}", "I,J_X", "I_X,J", 4, 4, "f32", good, good, stream=0)
+    assert e.value.status == shmm.shmm.ERR_INJECTED

@@ -439,3 +439,40 @@ def test_gather_falls_back_when_shards_straddle_boxes(s):
     assert plan.info.fused_gather == 0
     _, ores = oracle_run(XY22, ((), ("X",)), ((), ()), ((), ()), A, B, "bf16")
     compare(plan, gpu, ores, exact=False)
+
+
+# ------------------------------------------------------ all-to-all (f2)
+
+RESHARDS = [
+    ([("X", 2)], ((), ("X",)), (("X",), ())),              # A[I,J_X] -> A[I_X,J]
+    ([("X", 4)], ((), ("X",)), (("X",), ())),
+    ([("X", 8)], (("X",), ()), ((), ("X",))),
+    ([("X", 2), ("Y", 2)], (("X",), ("Y",)), (("Y",), ("X",))),
+    ([("X", 2), ("Y", 2)], ((), ("Y",)), (("X", "Y"), ())),  # replicated over X
+    ([("X", 2), ("Y", 2)], (("X", "Y"), ()), ((), ())),      # all-gather as a reshard
+    ([("X", 2), ("Y", 2)], ((), ()), (("Y",), ("X",))),      # slicing a replica
+]
+
+
+@pytest.mark.parametrize("mesh,sf,st", RESHARDS)
+@pytest.mark.parametrize("dtype,shape", [("bf16", (256, 512)), ("f32", (96, 64)), ("bf16", (24, 40))])
+def test_reshard_bit_exact(s, mesh, sf, st, dtype, shape):
+    import oracle as orc
+    rows, cols = shape
+    full = shmm_inputs.uniform_matrix(shape, -1.0, 1.0, dtype, seed=rows + cols)
+    N = orc.mesh_size(mesh)
+    src, host_src = [], {}
+    for r in range(N):
+        (i0, j0), (n0, n1) = orc.shard_box(mesh, sf, shape, r)
+        blk = full[i0:i0 + n0, j0:j0 + n1].contiguous()
+        host_src[r] = blk.float().numpy()
+        src.append(blk.cuda())
+    dst = []
+    for r in range(N):
+        _, (n0, n1) = orc.shard_box(mesh, st, shape, r)
+        dst.append(torch.full((n0, n1), float("nan"), dtype=full.dtype, device="cuda"))
+    s.shmm_reshard(mesh, sf, st, rows, cols, dtype, src, dst)
+    torch.cuda.synchronize()
+    ref = orc.reshard(mesh, sf, st, host_src, shape)
+    for r in range(N):
+        np.testing.assert_array_equal(dst[r].float().cpu().numpy(), ref[r].astype(np.float32))

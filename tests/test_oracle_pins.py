@@ -340,3 +340,20 @@ def test_planted_mistakes_fail_a_pin(monkeypatch, mutation):
                             lambda parts, order="sequential": orig(list(parts) + [parts[0]], order))
     with pytest.raises(AssertionError):
         _runs_pins()
+
+
+def test_all_to_all_moves_which_dim_is_sharded():
+    """A[I,J_X] -> A[I_X,J] on two ranks, by hand: rank 0 holds column 0
+    and ends with row 0; rank 1 holds column 1 and ends with row 1."""
+    mesh = [("X", 2)]
+    src = {0: np.array([[0.0], [2.0]]), 1: np.array([[1.0], [3.0]])}
+    out = oracle.reshard(mesh, ((), ("X",)), (("X",), ()), src, (2, 2))
+    assert out[0].tolist() == [[0.0, 1.0]] and out[1].tolist() == [[2.0, 3.0]]
+    # dropping the axis is the all-gather
+    full = oracle.reshard(mesh, ((), ("X",)), ((), ()), src, (2, 2))
+    assert full[0].tolist() == full[1].tolist() == [[0.0, 1.0], [2.0, 3.0]]
+    # replicas of one block (ranks 0 and 1 on {X:2,Y:2}) must agree
+    with pytest.raises(ValueError):
+        oracle.reshard([("X", 2), ("Y", 2)], ((), ("X",)), ((), ()),
+                       {0: np.zeros((2, 1)), 1: np.ones((2, 1)), 2: np.ones((2, 1)), 3: np.ones((2, 1))},
+                       (2, 2))
