@@ -523,3 +523,19 @@ def reshard(mesh: Mesh, spec_from: Spec, spec_to: Spec, shards_from: Dict[int, n
         (i0, j0), (n0, n1) = shard_box(mesh, spec_to, shape, r)
         out[r] = full[i0:i0 + n0, j0:j0 + n1].copy()
     return out
+
+
+def layernorm(x, gamma, beta, eps: float = 1e-5, out_dtype: str = "f32") -> np.ndarray:
+    """Layer normalisation of every row (a token) over its features, as the
+    sequence-parallel block applies it locally per token ("The simple maths
+    behind parallel training", Sequence parallelism); the form of Ba, Kiros &
+    Hinton (2016): y = (x - mean) / sqrt(var + eps) * gamma + beta with the
+    mean and the biased variance of the row, evaluated in double and rounded
+    once to ``out_dtype``."""
+    x = np.asarray(x, dtype=np.float64)
+    g = np.asarray(gamma, dtype=np.float64)
+    b = np.asarray(beta, dtype=np.float64)
+    mean = x.mean(axis=1, keepdims=True)
+    var = ((x - mean) ** 2).mean(axis=1, keepdims=True)
+    y = (x - mean) / np.sqrt(var + eps) * g + b
+    return to_dtype(y.astype(np.float32), out_dtype)

@@ -357,3 +357,22 @@ def test_all_to_all_moves_which_dim_is_sharded():
         oracle.reshard([("X", 2), ("Y", 2)], ((), ("X",)), ((), ()),
                        {0: np.zeros((2, 1)), 1: np.ones((2, 1)), 2: np.ones((2, 1)), 3: np.ones((2, 1))},
                        (2, 2))
+
+
+def test_layernorm_closed_form_invariants_and_library():
+    x = np.array([[1.0, 2.0, 3.0, 4.0]], np.float32)
+    y = oracle.layernorm(x, np.ones(4), np.zeros(4), eps=0.0)
+    np.testing.assert_allclose(y[0], np.array([-1.5, -0.5, 0.5, 1.5]) / np.sqrt(1.25), rtol=1e-6)
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((16, 300)) * 3 + 1).astype(np.float32)
+    y = oracle.layernorm(x, np.ones(300), np.zeros(300), eps=1e-5).astype(np.float64)
+    np.testing.assert_allclose(y.mean(axis=1), 0, atol=1e-6)
+    np.testing.assert_allclose(y.var(axis=1), 1, atol=1e-5)
+    g = rng.standard_normal(300).astype(np.float32)
+    b = rng.standard_normal(300).astype(np.float32)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x).double(), (300,), torch.from_numpy(g).double(),
+                                         torch.from_numpy(b).double(), eps=1e-5).numpy()
+    np.testing.assert_allclose(oracle.layernorm(x, g, b, 1e-5), ref.astype(np.float32), rtol=1e-6, atol=1e-6)
+    # shifting or scaling a row leaves its normalised form unchanged
+    np.testing.assert_allclose(oracle.layernorm(5 * x + 7, g, b, 0.0), oracle.layernorm(x, g, b, 0.0),
+                               rtol=0, atol=2e-5)
