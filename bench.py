@@ -52,6 +52,10 @@ WORKLOADS = {
         mesh=[("X", 8)], T=8192, D=4096, F=16384, fused=True,
         text="MLP column->row pair X[8192,4096].W1[4096,16384] (GeLU) .W2[16384,4096] bf16 on {X:8}, "
              "all-reduce of Y fused"),
+    "mlp_pair_sp": dict(
+        mesh=[("X", 8)], T=8192, D=4096, F=16384, fused=True,
+        text="sequence-parallel MLP block on {X:8}: X[8192,4096].W1 (GeLU) .W2 reduce-scattered over "
+             "tokens (fused), then LayerNorm per token fused with the all-gather"),
     "split_k_integer": dict(
         mesh=[("Y", 2)], I=64, J=64, K=64, fused=True,
         text="split-K integer fp32 A[64,64].B[64,64] on {Y:2}, reduce-scatter C[I_Y,K]"),
@@ -204,6 +208,21 @@ class Workload:
             Y_r = H.alloc(p2, s.TENSOR_C, device)
             self.steps_spec.append((p2, H_r, W2_r, Y_r, H.workspace(p2, device)))
             self.flops += p2.info.flops_per_rank * p2.nranks
+        elif name == "mlp_pair_sp":
+            X, W1, W2 = shmm_inputs.mlp_pair(c["T"], c["D"], c["F"], seed=0)
+            self.host_globals = (X, W1, W2)
+            self._add(c["mesh"], ((), ()), ((), ("X",)), ((), ("X",)), X, W1, s.FLAG_GELU, device)
+            H_r = self.steps_spec[0][3]
+            p2 = s.Plan(c["mesh"], ((), ("X",)), (("X",), ()), (("X",), ()), c["T"], c["F"], c["D"], "bf16",
+                        "bf16", s.FLAG_FUSED)
+            W2_r = H.shard(p2, s.TENSOR_B, W2, device)
+            Y_r = H.alloc(p2, s.TENSOR_C, device)
+            self.steps_spec.append((p2, H_r, W2_r, Y_r, H.workspace(p2, device)))
+            self.flops += p2.info.flops_per_rank * p2.nranks
+            self.sp_gather = s.Plan(c["mesh"], (("X",), ()), ((), ()), ((), ()), c["T"], 8, c["D"], "bf16", "bf16")
+            self.sp_out = H.alloc(self.sp_gather, s.TENSOR_C, device)
+            self.sp_gamma = torch.ones(c["D"], dtype=torch.float32, device=device)
+            self.sp_beta = torch.zeros(c["D"], dtype=torch.float32, device=device)
         elif name == "split_k_integer":
             A, B = shmm_inputs.split_k_integer(c["I"], c["J"], c["K"], seed=0)
             self.host_globals = (A, B)
@@ -225,11 +244,14 @@ class Workload:
     def step(self, stream):
         for p, A_r, B_r, C_r, ws in self.steps_spec:
             p.run(A_r, B_r, C_r, ws, stream=stream)
+        if self.name == "mlp_pair_sp":
+            self.sp_gather.layernorm_all_gather(self.steps_spec[-1][3], self.sp_gamma, self.sp_beta, self.sp_out,
+                                                stream=stream)
 
     def input_bytes(self):
         n = 0
         for i, (p, A_r, B_r, C_r, ws) in enumerate(self.steps_spec):
-            if self.name == "mlp_pair" and i == 1:
+            if self.name in ("mlp_pair", "mlp_pair_sp") and i == 1:
                 n += sum(t.numel() * t.element_size() for t in B_r)
                 continue
             n += sum(t.numel() * t.element_size() for t in A_r + B_r)
@@ -238,6 +260,8 @@ class Workload:
     def output_tensors(self):
         if self.name == "mlp_pair":
             return self.steps_spec[-1][3]
+        if self.name == "mlp_pair_sp":
+            return self.sp_out
         out = []
         for p, A_r, B_r, C_r, ws in self.steps_spec:
             out += C_r
@@ -246,7 +270,7 @@ class Workload:
     def input_tensors(self):
         out = []
         for i, (p, A_r, B_r, C_r, ws) in enumerate(self.steps_spec):
-            if self.name == "mlp_pair" and i == 1:
+            if self.name in ("mlp_pair", "mlp_pair_sp") and i == 1:
                 out += B_r
             else:
                 out += A_r + B_r

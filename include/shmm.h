@@ -296,6 +296,28 @@ shmm_status_t shmm_reshard(const shmm_mesh_t *mesh, const shmm_spec_t *spec_from
                            const shmm_spec_t *spec_to, int64_t rows, int64_t cols, shmm_dtype_t dtype,
                            const void *const *src_r, void *const *dst_r, void *stream);
 
+/* Layer normalisation of every row of x [rows, cols] (a token over its
+ * features): y = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c], mean and
+ * biased variance over the row, computed in fp32 and rounded once to dtype.
+ * The per-token normalisation the sequence-parallel block applies locally
+ * ("The simple maths behind parallel training", Sequence parallelism).
+ *   x, y       device buffers (may be the same), 16-byte aligned
+ *   gamma, beta  device fp32 arrays of `cols`
+ * Errors: NULL, ALIGN, SHAPE, DTYPE, CUDA. */
+shmm_status_t shmm_layernorm(int64_t rows, int64_t cols, shmm_dtype_t dtype, const void *x,
+                             const float *gamma, const float *beta, float eps, void *y, void *stream);
+
+/* Sequence parallelism's normalise-then-gather in one pass: for a plan whose
+ * result is row-owned and requested whole (its all-gather runs along rows:
+ * e.g. a reduce-scatter over tokens, Y[T_X, D], gathered to Y[T, D]), every
+ * owner block (box SHMM_TENSOR_C_REDUCED) is layer-normalised row by row and
+ * written to every member's gathered block (box SHMM_TENSOR_C).  Each row
+ * is read once.  gamma, beta: fp32 arrays of the row length shared by all
+ * ranks.  Errors: NULL, ALIGN, UNSUPPORTED (no row all-gather), CUDA. */
+shmm_status_t shmm_layernorm_all_gather(const shmm_plan_t *plan, const void *const *shard_r,
+                                        const float *gamma, const float *beta, float eps,
+                                        void *const *full_r, void *stream);
+
 /* ---- planner: which operand to move ("Sharded matmuls and collectives on
  * a torus", Which operand to move: the ICI roofline) ---------------------- */
 

@@ -463,6 +463,76 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
     return SHMM_OK;
 }
 
+shmm_status_t shmm_layernorm(int64_t rows, int64_t cols, shmm_dtype_t dtype, const void *x,
+                             const float *gamma, const float *beta, float eps, void *y, void *stream) {
+    static const char *fn = "shmm_layernorm";
+    shmm::clear_error();
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    if (dtype != SHMM_F32 && dtype != SHMM_BF16) return fail(SHMM_ERR_DTYPE, std::string(fn) + ": bad dtype");
+    if (rows < 0 || cols < 0) return fail(SHMM_ERR_SHAPE, std::string(fn) + ": negative size");
+    if (rows == 0 || cols == 0) return SHMM_OK;
+    if (!x || !y || !gamma || !beta) return fail(SHMM_ERR_NULL, std::string(fn) + ": NULL argument");
+    if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16)
+        return fail(SHMM_ERR_ALIGN, std::string(fn) + ": x and y must be 16-byte aligned");
+    if (!(eps >= 0.0f)) return fail(SHMM_ERR_SHAPE, std::string(fn) + ": eps must be >= 0");
+    shmm::LayerNormArgs a;
+    a.G = 1;
+    a.ngroups = 1;
+    a.brows = rows;
+    a.cols = cols;
+    a.dt = dtype;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.eps = eps;
+    a.src = &x;
+    a.dst = &y;
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    const int e = shmm::launch_layernorm_gather(a, status, stream);
+    if (e) return cuda_fail(fn, e);
+    return SHMM_OK;
+}
+
+shmm_status_t shmm_layernorm_all_gather(const shmm_plan_t *p, const void *const *shard_r, const float *gamma,
+                                        const float *beta, float eps, void *const *full_r, void *stream) {
+    static const char *fn = "shmm_layernorm_all_gather";
+    shmm::clear_error();
+    if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    const shmm::Groups &g = p->gC_groups;
+    if (g.size == 1 || g.blocks1 != 1)
+        return fail(SHMM_ERR_UNSUPPORTED, std::string(fn) + ": the plan must all-gather its result along rows");
+    if (!gamma || !beta) return fail(SHMM_ERR_NULL, std::string(fn) + ": gamma/beta NULL");
+    if (!(eps >= 0.0f)) return fail(SHMM_ERR_SHAPE, std::string(fn) + ": eps must be >= 0");
+    shmm_status_t st;
+    if ((st = check_ptrs(p, shard_r, SHMM_TENSOR_C_REDUCED, fn, "shard_r")) != SHMM_OK) return st;
+    if ((st = check_ptrs(p, (const void *const *)full_r, SHMM_TENSOR_C, fn, "full_r")) != SHMM_OK) return st;
+    std::vector<const void *> src(g.members.size());
+    std::vector<void *> dst(g.members.size());
+    for (size_t i = 0; i < g.members.size(); ++i) {
+        src[i] = shard_r[g.by_block[i]];
+        dst[i] = full_r[g.members[i]];
+    }
+    shmm::LayerNormArgs a;
+    a.G = g.size;
+    a.ngroups = g.count;
+    a.brows = p->boxes[SHMM_TENSOR_C_REDUCED][0].ext[0];
+    a.cols = p->boxes[SHMM_TENSOR_C_REDUCED][0].ext[1];
+    a.dt = p->out_dt;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.eps = eps;
+    a.src = src.data();
+    a.dst = dst.data();
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    const int e = shmm::launch_layernorm_gather(a, status, stream);
+    if (e) return cuda_fail(fn, e);
+    return SHMM_OK;
+}
+
 shmm_status_t shmm_run_static_workspace(const shmm_plan_t *p, const void *const *A_r,
                                         const void *const *B_r, void *const *C_r, void *stream) {
     static const char *fn = "shmm_run_static_workspace";

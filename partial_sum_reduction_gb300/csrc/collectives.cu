@@ -394,6 +394,104 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
     }
 }
 
+// ---- layer normalisation fused with the all-gather of row blocks ---------
+
+struct LnK {
+    const void *src[kMaxPtrs];  // [g*G + p]: block p of group g
+    void *dst[kMaxPtrs];        // [g*G + m]: every member's gathered buffer
+    const float *gamma, *beta;
+    float eps;
+    int G;
+    int64_t brows, cols;
+};
+
+// Deterministic block-wide sum (fixed shuffle tree, then warps in order).
+__device__ __forceinline__ float block_sum(float v, float *scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x / 32, nw = blockDim.x / 32;
+    __syncthreads();  // scratch is reused between calls
+    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    __syncthreads();
+    float t = 0.0f;
+    for (int i = 0; i < nw; ++i) t += scratch[i];
+    return t;
+}
+
+// One CTA per row (grid-stride over the group's G*brows rows; group =
+// blockIdx.y).  The row stays in registers (up to 32 values per thread,
+// cols <= 8192 in whole 16-byte vectors): mean, then the biased variance of
+// the deviations, then y = (x - mean) / sqrt(var + eps) * gamma + beta in fp32,
+// written to every member.  REG == false re-reads the row instead (any
+// cols), element by element.
+template <typename T, bool REG>
+__global__ void __launch_bounds__(256) ln_gather_kernel(const __grid_constant__ LnK k) {
+    constexpr int V = 16 / sizeof(T);
+    __shared__ float scratch[32];
+    const int g = blockIdx.y;
+    const int64_t rows = (int64_t)k.G * k.brows;
+    const float inv_n = 1.0f / (float)k.cols;
+    for (int64_t t = blockIdx.x; t < rows; t += gridDim.x) {
+        const int p = (int)(t / k.brows);
+        const int64_t rr = t - (int64_t)p * k.brows;
+        const T *x = (const T *)k.src[g * k.G + p] + rr * k.cols;
+        float sum = 0.0f, mean, rstd;
+        if (REG) {
+            float v[4][V];
+            const int nvec = (int)(k.cols / V);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int vi = threadIdx.x + j * blockDim.x;
+                if (vi < nvec) Vec<T>::load(x + (int64_t)vi * V, v[j]);
+                else
+#pragma unroll
+                    for (int i = 0; i < V; ++i) v[j][i] = 0.0f;
+#pragma unroll
+                for (int i = 0; i < V; ++i) sum += v[j][i];
+            }
+            mean = block_sum(sum, scratch) * inv_n;
+            float sq = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int vi = threadIdx.x + j * blockDim.x;
+                if (vi < nvec)
+#pragma unroll
+                    for (int i = 0; i < V; ++i) sq += (v[j][i] - mean) * (v[j][i] - mean);
+            }
+            rstd = 1.0f / sqrtf(block_sum(sq, scratch) * inv_n + k.eps);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int vi = threadIdx.x + j * blockDim.x;
+                if (vi >= nvec) continue;
+                float y[V];
+#pragma unroll
+                for (int i = 0; i < V; ++i) {
+                    const int64_t c = (int64_t)vi * V + i;
+                    y[i] = (v[j][i] - mean) * rstd * k.gamma[c] + k.beta[c];
+                }
+                for (int m = 0; m < k.G; ++m) {
+                    T *d = (T *)k.dst[g * k.G + m] + ((int64_t)p * k.brows + rr) * k.cols + (int64_t)vi * V;
+                    store_n<T, V>(d, y);
+                }
+            }
+        } else {
+            for (int64_t c = threadIdx.x; c < k.cols; c += blockDim.x) sum += Vec<T>::load1(x + c);
+            mean = block_sum(sum, scratch) * inv_n;
+            float sq = 0.0f;
+            for (int64_t c = threadIdx.x; c < k.cols; c += blockDim.x) {
+                const float d = Vec<T>::load1(x + c) - mean;
+                sq += d * d;
+            }
+            rstd = 1.0f / sqrtf(block_sum(sq, scratch) * inv_n + k.eps);
+            for (int64_t c = threadIdx.x; c < k.cols; c += blockDim.x) {
+                const float y = (Vec<T>::load1(x + c) - mean) * rstd * k.gamma[c] + k.beta[c];
+                for (int m = 0; m < k.G; ++m)
+                    Vec<T>::store1((T *)k.dst[g * k.G + m] + ((int64_t)p * k.brows + rr) * k.cols + c, y);
+            }
+        }
+    }
+}
+
 // ---- reshard: rectangles between rank buffers ------------------------------
 
 constexpr int kMaxRects = 128;
@@ -427,6 +525,39 @@ __global__ void __launch_bounds__(256) copy_rects_kernel(const __grid_constant__
 }  // namespace
 
 namespace shmm {
+
+int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream) {
+    (void)status;
+    if (a.ngroups * a.G > kMaxPtrs) return (int)cudaErrorInvalidValue;
+    if (a.brows == 0 || a.cols == 0 || a.ngroups == 0) return 0;
+    LnK k;
+    for (int i = 0; i < a.ngroups * a.G; ++i) {
+        k.src[i] = a.src[i];
+        k.dst[i] = a.dst[i];
+    }
+    k.gamma = a.gamma;
+    k.beta = a.beta;
+    k.eps = a.eps;
+    k.G = a.G;
+    k.brows = a.brows;
+    k.cols = a.cols;
+    const int V = a.dt == SHMM_F32 ? 4 : 8;
+    const bool reg = a.cols % V == 0 && a.cols <= (int64_t)V * 4 * 256;
+    const int64_t rows = (int64_t)a.G * a.brows;
+    int64_t want = rows, cap = (int64_t)sm_count() * 8 / a.ngroups;
+    if (cap < 1) cap = 1;
+    const dim3 grid((unsigned)(want < cap ? want : cap), (unsigned)a.ngroups, 1);
+    cudaStream_t s = (cudaStream_t)stream;
+    count_launch();
+    if (a.dt == SHMM_F32) {
+        if (reg) ln_gather_kernel<float, true><<<grid, 256, 0, s>>>(k);
+        else ln_gather_kernel<float, false><<<grid, 256, 0, s>>>(k);
+    } else {
+        if (reg) ln_gather_kernel<__nv_bfloat16, true><<<grid, 256, 0, s>>>(k);
+        else ln_gather_kernel<__nv_bfloat16, false><<<grid, 256, 0, s>>>(k);
+    }
+    return (int)cudaGetLastError();
+}
 
 int launch_copy_rects(const CopyRect *rects, int n, int elem, int *status, void *stream) {
     (void)status;

@@ -63,22 +63,23 @@ struct TcK {
     int a_b0, a_b1, b_b0, b_b1;
     int64_t a_brows, a_bcols, b_brows, b_bcols;
     int n_maps_a, n_maps_b;
+    int gathered;  // 0: map i is operand slot i's own buffer
 };
 
-// Which shard map holds element (row, col) of an operand read in place from
-// an all-gather group's shards, and its coordinates there.  Boxes never
-// straddle a shard (the planner only fuses when shard edges fall on box
-// edges); coordinates past the operand's end stay past the last shard's end,
-// where TMA fills zeros.
-__device__ __forceinline__ int shard_of(const uint8_t *idx, int b0, int b1, int64_t brows, int64_t bcols,
-                                        int64_t row, int64_t col, int32_t *srow, int32_t *scol) {
-    int p0 = b0 > 1 ? (int)(row / brows) : 0;
-    int p1 = b1 > 1 ? (int)(col / bcols) : 0;
-    if (p0 > b0 - 1) p0 = b0 - 1;
-    if (p1 > b1 - 1) p1 = b1 - 1;
-    *srow = (int32_t)(row - (int64_t)p0 * brows);
-    *scol = (int32_t)(col - (int64_t)p1 * bcols);
-    return idx[p0 * b1 + p1];
+// Operands read in place from an all-gather group's shards: which shard of
+// the b0 x b1 grid holds coordinate `x` along one dim, and the coordinate
+// inside it.  Boxes never straddle a shard (the planner only fuses when shard
+// edges fall on box edges); coordinates past the operand's end stay past the
+// last shard's end, where TMA fills zeros.  Grids of one block cost nothing.
+__device__ __forceinline__ int shard_split(int blocks, int64_t extent, int64_t x, int32_t *local) {
+    if (blocks == 1) {
+        *local = (int32_t)x;
+        return 0;
+    }
+    int p = (int)((uint32_t)x / (uint32_t)extent);
+    if (p > blocks - 1) p = blocks - 1;
+    *local = (int32_t)(x - (int64_t)p * extent);
+    return p;
 }
 
 // ---- PTX wrappers ------------------------------------------------------
@@ -317,7 +318,7 @@ struct Cfg {
     static constexpr int B_BYTES = BK * BN * 2;           // BN * 128
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
-    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 1024 /*barriers, tables*/;
 };
 
 template <int BN>
@@ -332,6 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    // In-place gathers only: block -> shard-map tables, copied once from the
+    // parameters into the shared-memory tail (a byte load from the parameter
+    // block on every TMA issue stalls the producer).
+    uint8_t *s_aidx = reinterpret_cast<uint8_t *>(tmem_holder + 16);
+    uint8_t *s_bidx = s_aidx + kMaxMaps * kMaxMaps;
+    if (k.gathered)
+        for (int i = threadIdx.x; i < kMaxMaps * kMaxMaps; i += blockDim.x) {
+            s_aidx[i] = k.a_idx[i / kMaxMaps][i % kMaxMaps];
+            s_bidx[i] = k.b_idx[i / kMaxMaps][i % kMaxMaps];
+        }
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int Gq = k.fused ? k.G : 1;
@@ -390,6 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 decode(t, &unit, &mt, &nt);
                 for (int q = 0; q < Gq && ok; ++q) {
                     const int ri = unit * Gq + q;
+                    int32_t a_r;
+                    const int a_p0 = shard_split(k.a_b0, k.a_brows, (int64_t)mt * BM, &a_r);
                     for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
@@ -400,15 +413,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         mbar_expect_tx(full_bar(s), C::STAGE);
                         const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
                         const uint32_t b_dst = a_dst + C::A_BYTES;
-                        int32_t r0, c0;
-                        int m = shard_of(k.a_idx[ri], k.a_b0, k.a_b1, k.a_brows, k.a_bcols,
-                                         (int64_t)mt * BM, (int64_t)kb * BK, &r0, &c0);
-                        tma_load_2d(a_dst, &k.tmA[m], full_bar(s), c0, r0);
+                        if (!k.gathered) {
+                            tma_load_2d(a_dst, &k.tmA[ri], full_bar(s), kb * BK, mt * BM);
 #pragma unroll
-                        for (int c = 0; c < BN / 64; ++c) {
-                            m = shard_of(k.b_idx[ri], k.b_b0, k.b_b1, k.b_brows, k.b_bcols, (int64_t)kb * BK,
-                                         (int64_t)nt * BN + c * 64, &r0, &c0);
-                            tma_load_2d(b_dst + c * 8192, &k.tmB[m], full_bar(s), c0, r0);
+                            for (int c = 0; c < BN / 64; ++c)
+                                tma_load_2d(b_dst + c * 8192, &k.tmB[ri], full_bar(s), nt * BN + c * 64, kb * BK);
+                        } else {
+                            int32_t a_c, b_r, x;
+                            const int a_p1 = shard_split(k.a_b1, k.a_bcols, (int64_t)kb * BK, &a_c);
+                            tma_load_2d(a_dst, &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + a_p1]], full_bar(s),
+                                        a_c, a_r);
+                            const int b_p0 = shard_split(k.b_b0, k.b_brows, (int64_t)kb * BK, &b_r);
+#pragma unroll
+                            for (int c = 0; c < BN / 64; ++c) {
+                                const int b_p1 = shard_split(k.b_b1, k.b_bcols, (int64_t)nt * BN + c * 64, &x);
+                                tma_load_2d(b_dst + c * 8192,
+                                            &k.tmB[s_bidx[ri * kMaxMaps + b_p0 * k.b_b1 + b_p1]], full_bar(s), x, b_r);
+                            }
                         }
                         last_parity[s] = (int)ph;
                     }
@@ -567,7 +588,7 @@ struct Cfg2 {
     static constexpr int B_BYTES = BK * 128 * 2;  // 16 KB: this CTA's 128 columns
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int STAGES = 6;
-    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 1024 /*barriers, tables*/;
 };
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcK k) {
@@ -582,6 +603,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
     // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    // In-place gathers only: block -> shard-map tables, copied once from the
+    // parameters into the shared-memory tail (a byte load from the parameter
+    // block on every TMA issue stalls the producer).
+    uint8_t *s_aidx = reinterpret_cast<uint8_t *>(tmem_holder + 16);
+    uint8_t *s_bidx = s_aidx + kMaxMaps * kMaxMaps;
+    if (k.gathered)
+        for (int i = threadIdx.x; i < kMaxMaps * kMaxMaps; i += blockDim.x) {
+            s_aidx[i] = k.a_idx[i / kMaxMaps][i % kMaxMaps];
+            s_bidx[i] = k.b_idx[i / kMaxMaps][i % kMaxMaps];
+        }
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t cr = cluster_ctarank();  // 0: leader, 1: peer
@@ -644,6 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
                 decode(t, &unit, &mt, &nt);
                 for (int q = 0; q < Gq && ok; ++q) {
                     const int ri = unit * Gq + q;
+                    int32_t a_r;
+                    const int a_p0 = shard_split(k.a_b0, k.a_brows, (int64_t)mt * 256 + (int)cr * BM, &a_r);
                     for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
@@ -655,15 +688,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
                         const uint32_t bar = mapa_shared(full_bar(s), 0);
                         const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
                         const uint32_t b_dst = a_dst + C::A_BYTES;
-                        int32_t r0, c0;
-                        int m = shard_of(k.a_idx[ri], k.a_b0, k.a_b1, k.a_brows, k.a_bcols,
-                                         (int64_t)mt * 256 + (int)cr * BM, (int64_t)kb * BK, &r0, &c0);
-                        tma_load_2d_pair(a_dst, &k.tmA[m], bar, c0, r0);
+                        if (!k.gathered) {
+                            tma_load_2d_pair(a_dst, &k.tmA[ri], bar, kb * BK, mt * 256 + (int)cr * BM);
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            m = shard_of(k.b_idx[ri], k.b_b0, k.b_b1, k.b_brows, k.b_bcols, (int64_t)kb * BK,
-                                         (int64_t)nt * BN + (int)cr * 128 + c * 64, &r0, &c0);
-                            tma_load_2d_pair(b_dst + c * 8192, &k.tmB[m], bar, c0, r0);
+                            for (int c = 0; c < 2; ++c)
+                                tma_load_2d_pair(b_dst + c * 8192, &k.tmB[ri], bar, nt * BN + (int)cr * 128 + c * 64,
+                                                 kb * BK);
+                        } else {
+                            int32_t a_c, b_r, x;
+                            const int a_p1 = shard_split(k.a_b1, k.a_bcols, (int64_t)kb * BK, &a_c);
+                            tma_load_2d_pair(a_dst, &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + a_p1]], bar, a_c,
+                                             a_r);
+                            const int b_p0 = shard_split(k.b_b0, k.b_brows, (int64_t)kb * BK, &b_r);
+#pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                const int b_p1 =
+                                    shard_split(k.b_b1, k.b_bcols, (int64_t)nt * BN + (int)cr * 128 + c * 64, &x);
+                                tma_load_2d_pair(b_dst + c * 8192,
+                                                 &k.tmB[s_bidx[ri * kMaxMaps + b_p0 * k.b_b1 + b_p1]], bar, x, b_r);
+                            }
                         }
                         last_parity[s] = (int)ph;
                     }
@@ -991,10 +1034,12 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         // every member of its all-gather group); per slot, a block table.
         const void *ptrs_a[kMaxMaps], *ptrs_b[kMaxMaps];
         int na = 0, nb = 0;
+        const bool gathered = a.A_src || a.B_src;
         auto map_of = [&](const void *ptr, const void **ptrs, int *n, CUtensorMap *maps, int64_t rows,
                           int64_t cols, uint32_t bx, uint32_t by) -> int {
-            for (int j = 0; j < *n; ++j)
-                if (ptrs[j] == ptr) return j;
+            if (gathered)  // a shard may serve several slots: one map each
+                for (int j = 0; j < *n; ++j)
+                    if (ptrs[j] == ptr) return j;
             if (*n >= kMaxMaps) return -1;
             if (!cached_map(fn, &maps[*n], ptr, rows, cols, bx, by)) return -2;
             ptrs[*n] = ptr;
@@ -1033,6 +1078,7 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         }
         k.n_maps_a = na;
         k.n_maps_b = nb;
+        k.gathered = gathered ? 1 : 0;
         k.a_b0 = a.A_src ? a.a_b0 : 1;
         k.a_b1 = a.A_src ? a.a_b1 : 1;
         k.b_b0 = a.B_src ? a.b_b0 : 1;

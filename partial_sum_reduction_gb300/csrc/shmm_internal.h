@@ -120,6 +120,21 @@ struct GatherArgs {
 };
 int launch_gather(const GatherArgs &a, int *status, void *stream);
 
+// Layer normalisation of rows, fused with an all-gather of row blocks: group
+// g's block p (src[g*G+p], brows x cols) is normalised row by row and
+// written as rows [p*brows, (p+1)*brows) of every member's gathered buffer
+// dst[g*G+m] (G*brows x cols).  G = 1 is plain layer normalisation.
+struct LayerNormArgs {
+    int G = 1, ngroups = 1;
+    int64_t brows = 0, cols = 0;
+    shmm_dtype_t dt = SHMM_BF16;
+    const float *gamma = nullptr, *beta = nullptr;
+    float eps = 1e-5f;
+    const void *const *src = nullptr;
+    void *const *dst = nullptr;
+};
+int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream);
+
 // Copies rectangles between row-major buffers: rectangle i moves h[i] rows of
 // w[i] elements of `elem` bytes from src[i] (row pitch src_ld[i] elements) to
 // dst[i] (pitch dst_ld[i]).  The reshard (all-to-all) collective.

@@ -80,7 +80,8 @@ EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_
            "shmm_plan_group", "shmm_workspace_size", "shmm_local_matmul", "shmm_reduce_scatter",
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
            "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace",
-           "shmm_selftest_wait_timeout", "shmm_choose_operand", "shmm_reshard"]
+           "shmm_selftest_wait_timeout", "shmm_choose_operand", "shmm_reshard", "shmm_layernorm",
+           "shmm_layernorm_all_gather"]
 
 _lib = None
 
@@ -114,6 +115,8 @@ def lib():
         L.shmm_run_static_workspace.argtypes = [P, PP, PP, PP, P]
         L.shmm_sync_status.argtypes = [P]
         L.shmm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
+        L.shmm_layernorm.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P, P, ctypes.c_float, P, P]
+        L.shmm_layernorm_all_gather.argtypes = [P, PP, P, P, ctypes.c_float, PP, P]
         L.shmm_reshard.argtypes = [ctypes.POINTER(shmm_mesh_t), ctypes.POINTER(shmm_spec_t),
                                    ctypes.POINTER(shmm_spec_t), ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                    PP, PP, P]
@@ -325,6 +328,13 @@ class Plan:
         _check(lib().shmm_run(self._h, _ptr_array(A_r, "A"), _ptr_array(B_r, "B"), _ptr_array(C_r, "C"),
                               ws_ptr, ws_bytes, _stream_handle(stream)))
 
+    def layernorm_all_gather(self, shard_r, gamma, beta, full_r, eps: float = 1e-5, stream=None):
+        """Layer-normalise the row-owned result blocks and all-gather them
+        (sequence parallelism's LayerNorm then AllGather, in one pass)."""
+        _check(lib().shmm_layernorm_all_gather(self._h, _ptr_array(shard_r, "shard"), gamma.data_ptr(),
+                                               beta.data_ptr(), float(eps), _ptr_array(full_r, "full"),
+                                               _stream_handle(stream)))
+
     def run_static_workspace(self, A_r, B_r, C_r, stream=None):
         """shmm_run on the library's fixed 64 MiB device workspace, for
         callers that cannot allocate device memory (see include/shmm.h)."""
@@ -382,6 +392,14 @@ STATIC_WORKSPACE_BYTES = 64 << 20
 
 def shmm_sync_status(stream=None) -> None:
     _check(lib().shmm_sync_status(_stream_handle(stream)))
+
+
+def shmm_layernorm(x, gamma, beta, y, eps: float = 1e-5, stream=None):
+    """Row-wise layer normalisation of a 2-D CUDA tensor x into y."""
+    rows, cols = x.shape
+    dt = {"torch.float32": "f32", "torch.bfloat16": "bf16"}[str(x.dtype)]
+    _check(lib().shmm_layernorm(int(rows), int(cols), DTYPE_CODES[dt], x.data_ptr(), gamma.data_ptr(),
+                                beta.data_ptr(), float(eps), y.data_ptr(), _stream_handle(stream)))
 
 
 def shmm_reshard(mesh, spec_from, spec_to, rows: int, cols: int, dtype: str, src_r, dst_r, stream=None):

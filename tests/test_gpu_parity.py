@@ -476,3 +476,69 @@ def test_reshard_bit_exact(s, mesh, sf, st, dtype, shape):
     ref = orc.reshard(mesh, sf, st, host_src, shape)
     for r in range(N):
         np.testing.assert_array_equal(dst[r].float().cpu().numpy(), ref[r].astype(np.float32))
+
+
+# --------------------------------------- sequence parallelism (f4)
+
+@pytest.mark.parametrize("rows,cols,dtype", [(64, 4096, "bf16"), (33, 1000, "f32"), (7, 12000, "bf16"),
+                                             (5, 1001, "bf16"), (128, 8192, "bf16"), (3, 4096, "f32")])
+def test_layernorm_rows(s, rows, cols, dtype):
+    x = shmm_inputs.normal_matrix((rows, cols), 2.0, dtype, seed=rows)
+    g = shmm_inputs.normal_matrix((1, cols), 1.0, "f32", seed=1)[0]
+    b = shmm_inputs.normal_matrix((1, cols), 1.0, "f32", seed=2)[0]
+    y = torch.full_like(x, float("nan")).cuda()
+    s.shmm_layernorm(x.cuda(), g.cuda(), b.cuda(), y, eps=1e-5)
+    torch.cuda.synchronize()
+    ref = oracle.layernorm(x.float().numpy(), g.numpy(), b.numpy(), 1e-5, dtype)
+    got = y.float().cpu().numpy()
+    tol = BF16_TOL if dtype == "bf16" else 1e-4
+    assert np.abs(got - ref).max() <= tol * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_sequence_parallel_mlp_block(s, fused):
+    """X -> GeLU(X.W1) (column-parallel) -> .W2 reduce-scattered over tokens
+    -> LayerNorm per token -> all-gather, on {X:8}; equals the oracle chain,
+    and (AllReduce = ReduceScatter + AllGather) equals LayerNorm applied to
+    the all-reduced result bit for bit."""
+    from partial_sum_reduction_gb300 import helpers as H
+    T, D, F = 512, 1024, 2048
+    X, W1, W2 = shmm_inputs.mlp_pair(T, D, F, seed=3)
+    gam = (1.0 + 0.1 * shmm_inputs.normal_matrix((1, D), 1.0, "f32", seed=4)[0]).cuda()
+    bet = (0.1 * shmm_inputs.normal_matrix((1, D), 1.0, "f32", seed=5)[0]).cuda()
+    fl = s.FLAG_FUSED if fused else 0
+    p1 = s.Plan(X8, ((), ()), ((), ("X",)), ((), ("X",)), T, D, F, "bf16", "bf16", s.FLAG_GELU)
+    H_r = H.alloc(p1, s.TENSOR_C)
+    p1.run(H.shard(p1, s.TENSOR_A, X), H.shard(p1, s.TENSOR_B, W1), H_r, H.workspace(p1))
+    p2 = s.Plan(X8, ((), ("X",)), (("X",), ()), (("X",), ()), T, F, D, "bf16", "bf16", fl)
+    W2_r = H.shard(p2, s.TENSOR_B, W2)
+    Y_rs = H.alloc(p2, s.TENSOR_C)
+    p2.run(H_r, W2_r, Y_rs, H.workspace(p2))
+    pg = s.Plan(X8, (("X",), ()), ((), ()), ((), ()), T, 8, D, "bf16", "bf16")  # rows gathered over X
+    Y_n = H.alloc(pg, s.TENSOR_C, fill=float("nan"))
+    pg.layernorm_all_gather(Y_rs, gam, bet, Y_n, eps=1e-5)
+    # the all-reduce route: full Y on every rank, normalised in place
+    pa = s.Plan(X8, ((), ("X",)), (("X",), ()), ((), ()), T, F, D, "bf16", "bf16", fl)
+    Y_ar = H.alloc(pa, s.TENSOR_C)
+    pa.run(H_r, W2_r, Y_ar, H.workspace(pa))
+    for y in Y_ar:
+        s.shmm_layernorm(y, gam, bet, y, eps=1e-5)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    for a, b in zip(Y_n, Y_ar):
+        assert torch.equal(a, b)
+    # oracle chain
+    Xn, W1n, W2n = X.float().numpy(), W1.float().numpy(), W2.float().numpy()
+    _, hres = oracle.sharded_matmul(X8, ((), ()), ((), ("X",)), ((), ("X",)), Xn, W1n, "bf16", gelu=True,
+                                    nthreads=8)
+    Hn = np.zeros((T, F), np.float32)
+    for r, ((i0, k0), blk) in hres.items():
+        Hn[i0:i0 + blk.shape[0], k0:k0 + blk.shape[1]] = blk
+    _, yres = oracle.sharded_matmul(X8, ((), ("X",)), (("X",), ()), (("X",), ()), Hn, W2n, "bf16", nthreads=8)
+    Yn = np.zeros((T, D), np.float32)
+    for r, ((i0, k0), blk) in yres.items():
+        Yn[i0:i0 + blk.shape[0]] = blk
+    ref = oracle.layernorm(Yn, gam.cpu().numpy(), bet.cpu().numpy(), 1e-5, "bf16")
+    for y in Y_n:
+        got = y.float().cpu().numpy()
+        assert np.abs(got - ref).max() <= BF16_TOL * np.abs(ref).max()
