@@ -49,10 +49,15 @@
  * sums are stored in fp32 (unless SHMM_FLAG_PARTIAL_OUT_DTYPE); the sum over a
  * reduction group is formed in fp32 in ascending rank order, one rounding per
  * addition, then rounded once to the output type (bf16: round to nearest
- * even).  The fused path (SHMM_FLAG_FUSED) keeps each rank's partial in its
- * own fp32 accumulator and sums them in the same order, so it matches the
- * standalone reduction bit for bit.  SHMM_FLAG_TREE sums with a balanced
- * pairwise tree over the ranks in ascending order instead.
+ * even).  SHMM_FLAG_TREE sums with a balanced pairwise tree over the ranks in
+ * ascending order instead.  The fused path (SHMM_FLAG_FUSED) on tensor cores
+ * accumulates the group's products in one fp32 accumulator, as one
+ * contraction over the group's concatenated K in ascending rank order: the
+ * same sum, rounded in a different order (no per-rank partial is formed).
+ * With SHMM_FLAG_RANK_ORDER it keeps each rank's partial in its own fp32
+ * accumulator and adds them in ascending rank order, so it matches the
+ * standalone sequential reduction bit for bit; the CUDA-core path always
+ * does this.  Every path is deterministic: one input gives one result.
  */
 #ifndef SHMM_H
 #define SHMM_H
@@ -112,9 +117,10 @@ typedef struct {
 
 /* Plan flags */
 #define SHMM_FLAG_FUSED 0x1u   /* shmm_run: fuse the collectives into the GEMM.
-                                  Partial sums are reduced in the epilogue:
+                                  Partial sums are reduced inside the GEMM:
                                   each output tile is summed over its
-                                  reduction group in ascending rank order and
+                                  reduction group (in its accumulator, or in
+                                  the epilogue with SHMM_FLAG_RANK_ORDER) and
                                   written once to its owner(s).  Operand
                                   all-gathers (cases 2, 4) become in-place
                                   reads of the owners' shards by the GEMM's
@@ -128,6 +134,14 @@ typedef struct {
                                   rank-order sum */
 #define SHMM_FLAG_PARTIAL_OUT_DTYPE 0x8u /* partial buffers are stored in the
                                   output dtype instead of fp32 */
+#define SHMM_FLAG_RANK_ORDER 0x20u /* with SHMM_FLAG_FUSED: form every rank's
+                                  partial on its own and add the partials in
+                                  ascending rank order in the epilogue (bit
+                                  for bit the standalone reduction), instead
+                                  of accumulating the group's products in one
+                                  accumulator; slower when the group is large
+                                  (each rank's product drains the MMA
+                                  pipeline before the epilogue can add it) */
 #define SHMM_FLAG_SIMT 0x10u   /* local GEMM on CUDA cores even for bf16 (the
                                   tensor-core path is used otherwise whenever
                                   the shapes allow TMA: J_r, K_r multiples of

@@ -431,6 +431,7 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         ga.units = g.count;
         ga.G = g.size;
         ga.fused = true;
+        ga.rank_order = (p->flags & SHMM_FLAG_RANK_ORDER) != 0;
         ga.mode = p->collective == SHMM_COLL_REDUCE_SCATTER ? p->scatter_dim : 2;
         ga.gelu = gelu;
         ga.out_dt = p->out_dt;

@@ -54,6 +54,7 @@ struct TcK {
     int *status;
     int units, G, mode;
     int fused, gelu, out_f32;
+    int accum;  // fused: the group's products accumulate in one TMEM buffer
     int64_t M, N, Kd;
     int m_tiles, n_tiles, k_blocks;
     // operand slot i's block p (row-major over a b0 x b1 grid of brows x bcols
@@ -443,9 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         // Two TMEM buffers of BN columns.  Tile i (this CTA's i-th) keeps its
-        // running sum S in buffer i%2; ranks 1..G-1 of the tile are computed
-        // in the other buffer W.  A buffer is refilled only after the
-        // epilogue released its previous contents.
+        // running sum S in buffer i%2.  Rank order: ranks 1..G-1 of the tile
+        // are computed in the other buffer W and folded into S by the
+        // epilogue.  Accumulating (k.accum): every rank's k-blocks continue
+        // the same accumulation in S, one contraction over the group's
+        // concatenated K.  A buffer is refilled only after the epilogue
+        // released its previous contents.
         if (lane == 0) {
             constexpr uint32_t idesc = instr_desc(BN);
             uint32_t it = 0;
@@ -455,9 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_iter) {
                 const int bS = tile_iter & 1;
                 for (int q = 0; q < Gq && ok; ++q) {
-                    const int b = (q == 0) ? bS : (bS ^ 1);
+                    // accum: every rank's product continues the sum in S
+                    const bool into_s = q == 0 || k.accum;
+                    const int b = into_s ? bS : (bS ^ 1);
                     const uint32_t nf = b ? fills1 : fills0;
-                    if (!mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
+                    if ((q == 0 || !k.accum) && !mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
                         ok = false;
                         break;
                     }
@@ -479,11 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                             // swizzle row.  B: MN-major, 16 k rows = 2 atoms.
                             const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
                             const uint64_t bd = smem_desc(b_addr + kk * 2048, 8192, 1024);
-                            umma_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            umma_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0 || (q > 0 && k.accum)) ? 1u : 0u);
                         }
                         umma_commit(empty_bar(s));
                     }
                     if (!ok) break;
+                    if (k.accum && q < Gq - 1) continue;  // S is not finished
                     umma_commit(accf_bar(b));
                     if (b) ++fills1;
                     else ++fills0;
@@ -522,7 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
             if (!warp_wait_full(bS)) break;  // S = product of the group's first rank
             bool ok = true;
-            for (int q = 1; q < Gq; ++q) {
+            const int folds = k.accum ? 1 : Gq;  // accum: S already holds the sum
+            for (int q = 1; q < folds; ++q) {
                 // S = S + P_q in fp32: the ascending-rank sequential sum
                 if (!warp_wait_full(bW)) {
                     ok = false;
@@ -733,9 +741,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
             for (int t = pair; t < total && ok; t += npairs, ++tile_iter) {
                 const int bS = tile_iter & 1;
                 for (int q = 0; q < Gq && ok; ++q) {
-                    const int b = (q == 0) ? bS : (bS ^ 1);
+                    // accum: every rank's product continues the sum in S
+                    const bool into_s = q == 0 || k.accum;
+                    const int b = into_s ? bS : (bS ^ 1);
                     const uint32_t nf = b ? fills1 : fills0;
-                    if (!mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
+                    if ((q == 0 || !k.accum) && !mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
                         ok = false;
                         break;
                     }
@@ -755,11 +765,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
                         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                             const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
                             const uint64_t bd = smem_desc(b_addr + kk * 2048, 8192, 1024);
-                            umma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            umma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0 || (q > 0 && k.accum)) ? 1u : 0u);
                         }
                         umma2_commit_both(empty_bar(s));
                     }
                     if (!ok) break;
+                    if (k.accum && q < Gq - 1) continue;  // S is not finished
                     umma2_commit_both(accf_bar(b));
                     if (b) ++fills1;
                     else ++fills0;
@@ -799,7 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
             const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
             if (!warp_wait_full(bS)) break;
             bool ok = true;
-            for (int q = 1; q < Gq; ++q) {
+            const int folds = k.accum ? 1 : Gq;  // accum: S already holds the sum
+            for (int q = 1; q < folds; ++q) {
                 if (!warp_wait_full(bW)) {
                     ok = false;
                     break;
@@ -1094,6 +1106,7 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         k.G = G;
         k.mode = a.mode;
         k.fused = a.fused ? 1 : 0;
+        k.accum = a.fused && !a.rank_order ? 1 : 0;
         k.gelu = a.gelu ? 1 : 0;
         k.out_f32 = a.out_dt == SHMM_F32 ? 1 : 0;
         k.M = a.M;

@@ -148,12 +148,15 @@ int launch_copy_rects(const CopyRect *rects, int n, int elem, int *status, void 
 // Local GEMMs.  For unit u (a rank, or a reduction group when fused), the
 // G operand pairs A[u*G+q] (M x Kd, row-major) and B[u*G+q] (Kd x N,
 // row-major) are multiplied.  Unfused (G == 1 per unit): out[u] = A.B.
-// Fused: the G products are summed in q order; mode 0/1 scatter along dim
-// 0/1 to out[u*G+b], mode 2 writes every out[u*G+b].
+// Fused: the G products are summed, by default in one fp32 accumulator over
+// the group's concatenated K (tensor cores), with rank_order (and always on
+// CUDA cores) each formed on its own and added in ascending q order; mode
+// 0/1 scatter along dim 0/1 to out[u*G+b], mode 2 writes every out[u*G+b].
 struct GemmArgs {
     int units = 0;          // ranks (unfused) or groups (fused)
     int G = 1;              // ranks per unit
     bool fused = false;
+    bool rank_order = false;  // fused: per-rank partials added in q order
     int mode = 2;           // fused write mode (0/1 RS dim, 2 AR)
     bool gelu = false;
     int64_t M = 0, N = 0, Kd = 0;

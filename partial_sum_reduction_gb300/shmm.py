@@ -30,6 +30,7 @@ OK, ERR_INVALID_SPEC, ERR_ILLEGAL_OUTPUT, ERR_SHAPE, ERR_DTYPE, ERR_NULL, ERR_AL
     ERR_TIMEOUT, ERR_NOMEM, ERR_UNSUPPORTED, ERR_INJECTED = range(12)
 F32, BF16 = 0, 1
 FLAG_FUSED, FLAG_GELU, FLAG_TREE, FLAG_PARTIAL_OUT_DTYPE, FLAG_SIMT = 0x1, 0x2, 0x4, 0x8, 0x10
+FLAG_RANK_ORDER = 0x20
 TENSOR_A, TENSOR_B, TENSOR_C, TENSOR_P, TENSOR_A_LOCAL, TENSOR_B_LOCAL, TENSOR_C_REDUCED = range(7)
 COLL_NONE, COLL_REDUCE_SCATTER, COLL_ALL_REDUCE = range(3)
 COLLECTIVE_NAMES = {COLL_NONE: "none", COLL_REDUCE_SCATTER: "reduce_scatter",

@@ -40,6 +40,23 @@ def test_library_exports_every_declared_symbol(shmm):
     assert shmm.lib().shmm_status_string(0) == b"SHMM_OK"
 
 
+def test_binding_constants_match_header(shmm):
+    """Every SHMM_FLAG_*, SHMM_TENSOR_* and dtype value the header defines has
+    the same value in the binding."""
+    src = open(os.path.join(ROOT, "include", "shmm.h")).read()
+    flags = dict(re.findall(r"#define SHMM_FLAG_([A-Z_]+) (0x[0-9a-fA-F]+)u", src))
+    assert len(flags) >= 6
+    for name, val in flags.items():
+        assert getattr(shmm, "FLAG_" + name) == int(val, 16), name
+    tensors = dict(re.findall(r"SHMM_TENSOR_([A-Z_]+) = (\d+)", src))
+    assert len(tensors) == 7
+    for name, val in tensors.items():
+        assert getattr(shmm, "TENSOR_" + name) == int(val), name
+    ws = re.search(r"#define SHMM_STATIC_WORKSPACE_BYTES \((\d+)u << (\d+)\)", src)
+    assert shmm.shmm.STATIC_WORKSPACE_BYTES == int(ws.group(1)) << int(ws.group(2))
+    assert (shmm.F32, shmm.BF16) == (0, 1)
+
+
 def test_binding_fails_loudly_without_library(monkeypatch):
     import partial_sum_reduction_gb300.shmm as m
     monkeypatch.setattr(m, "_lib", None)

@@ -322,16 +322,58 @@ def test_operand_all_gather_bit_exact(s):
 
 @pytest.mark.parametrize("pair", ["1", "0"])
 def test_fused_equals_unfused_bitwise(s, pair, monkeypatch):
+    """SHMM_FLAG_RANK_ORDER: the fused epilogue adds per-rank partials in
+    ascending rank order, exactly the standalone sequential reduction."""
     monkeypatch.setenv("SHMM_TC_PAIR", pair)
     A, B = shmm_inputs.scaled_normal_pair(640, 1024, 512, "bf16", seed=12)
     for mesh, sA, sB, sC in ((Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ())),
                              (XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ())),
                              ([("X", 4)], ((), ("X",)), (("X",), ()), ((), ("X",)))):
         _, g1 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32")
-        p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED)
+        p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED | s.FLAG_RANK_ORDER)
         assert p2.info.fused == 1
         for a, b in zip(g1, g2):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("pair", ["1", "0"])
+def test_accumulating_fusion_is_one_contraction(s, pair, monkeypatch):
+    """Default fused path: a reduction group's products accumulate in one
+    fp32 accumulator, k-block after k-block in ascending rank order -- the
+    same tensor-core operations as one unsharded GEMM over the whole J, so
+    every output element has the same bits (J_r a multiple of the 64-wide
+    k-block, so block edges coincide)."""
+    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    A, B = shmm_inputs.scaled_normal_pair(640, 1024, 512, "bf16", seed=13)
+    _, full = run_gpu([("Y", 1)], ((), ()), ((), ()), ((), ()), A, B, "bf16", "f32")
+    full = full[0]
+    for mesh, sA, sB, sC in ((Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ())),
+                             (XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ())),
+                             (X8, ((), ("X",)), (("X",), ()), ((), ())),
+                             ([("X", 4)], ((), ("X",)), (("X",), ()), ((), ("X",)))):
+        p, g = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED)
+        assert p.info.fused == 1
+        for r, c in enumerate(g):
+            (o0, o1), ext = p.rank_box(s.TENSOR_C, r)
+            assert torch.equal(c, full[o0:o0 + ext[0], o1:o1 + ext[1]]), (mesh, r)
+
+
+@pytest.mark.parametrize("flags", ["FUSED", "FUSED|RANK_ORDER", "0"])
+@pytest.mark.parametrize("sC", [((), ()), (("X",), ()), ((), ("X",))])
+def test_integer_bf16_tensor_core_bit_exact(s, flags, sC):
+    """Integer-valued bf16 operands on the tensor cores, {X:8}: every
+    partial and every sum is an integer below 2^24, so all reduction orders
+    give the oracle's exact result."""
+    fl = 0
+    for f in flags.split("|"):
+        fl |= getattr(s, "FLAG_" + f) if f != "0" else 0
+    A, B = shmm_inputs.split_k_integer(384, 1024, 320, seed=4)
+    A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    sA, sB = ((), ("X",)), (("X",), ())
+    plan, gpu = run_gpu(X8, sA, sB, sC, A, B, "bf16", "f32", fl)
+    assert plan.info.tensor_core == 1
+    _, ores = oracle_run(X8, sA, sB, sC, A, B, "f32")
+    compare(plan, gpu, ores, exact=True)
 
 
 def test_all_reduce_replicas_identical(s):
@@ -425,12 +467,15 @@ def test_in_place_gather_equals_explicit_gather(s, name, mesh, sA, sB, sC, I, J,
     monkeypatch.setenv("SHMM_TC_PAIR", pair)
     A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=I + J)
     p1, g1 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", 0)
-    p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED)
+    p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED | s.FLAG_RANK_ORDER)
     assert p1.info.fused_gather == 0 and p2.info.fused_gather == 1 and p2.workspace_size() == 0
     for a, b in zip(g1, g2):
         assert torch.equal(a, b)
     _, ores = oracle_run(mesh, sA, sB, sC, A, B, "f32")
-    compare(p2, g2, ores, exact=False)
+    compare(p2, g2, ores, exact=False, tol=F32P_TOL)
+    p3, g3 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED)  # accumulating
+    assert p3.info.fused_gather == 1
+    compare(p3, g3, ores, exact=False, tol=F32P_TOL)
 
 
 def test_gather_falls_back_when_shards_straddle_boxes(s):
