@@ -34,6 +34,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("sharded-matmul TFLOP/s (% bf16 peak) and reduce-scatter GB/s (% HBM) on 1 GB300")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# datasheet figures of one GB300, reported beside the measured denominators
+NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 WORKLOADS = {
     "down_projection": dict(
@@ -267,15 +269,6 @@ class Workload:
             out += C_r
         return out
 
-    def input_tensors(self):
-        out = []
-        for i, (p, A_r, B_r, C_r, ws) in enumerate(self.steps_spec):
-            if self.name in ("mlp_pair", "mlp_pair_sp") and i == 1:
-                out += B_r
-            else:
-                out += A_r + B_r
-        return out
-
 
 def capture_graph(wl):
     """One step of the hot path captured into a CUDA graph (the plan's
@@ -356,48 +349,69 @@ def _smi_bus_id(bus):
     return bus
 
 
-def _pool_views(tensors, device, pin=False):
-    """Lays ``tensors`` out back to back (256-byte aligned) in one byte pool;
-    returns the pool and a view of it per tensor."""
-    import torch
-    offs, off = [], 0
-    for t in tensors:
-        offs.append(off)
-        off += (t.numel() * t.element_size() + 255) // 256 * 256
-    pool = torch.empty(max(off, 1), dtype=torch.uint8, device=device, pin_memory=pin)
-    views = [pool[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
-    return pool, views
+def _distinct_bytes(plan, tensor, elem):
+    """Bytes of the distinct boxes of ``tensor`` over the ranks (replicas
+    counted once): what crosses the host link for it."""
+    seen = {}
+    for r in range(plan.nranks):
+        off, ext = plan.rank_box(tensor, r)
+        seen[tuple(off)] = ext[0] * ext[1] * elem
+    return sum(seen.values())
 
 
 def time_e2e(wl, steps, dist_ctx):
-    """End to end through the public API: every step copies all ranks'
-    inputs from one pinned host buffer to the device (one copy), runs the
-    sharded matmul, and copies all ranks' results back to pinned host memory
-    (one copy), all inside the timed region.  The per-rank buffers are
-    256-byte-aligned slices of one device allocation per direction."""
+    """End to end through the public API from host memory: every step
+    uploads the global operands from pinned host memory (shmm_run_host:
+    each distinct shard once, replicas copied on the device, uploads of one
+    reduction group overlapping the previous group's GEMM), runs the sharded
+    matmul, and writes the global result back to pinned host memory, all
+    inside the timed region.  Chained steps keep their intermediate on the
+    device (a NULL host operand)."""
     import torch
-    ins, outs = wl.input_tensors(), wl.output_tensors()
-    d_in, v_in = _pool_views(ins, "cuda")
-    d_out, v_out = _pool_views(outs, "cuda")
-    for v, t in zip(v_in, ins):
-        v.copy_(t)
-    h_in = torch.empty(d_in.numel(), dtype=torch.uint8, pin_memory=True)
-    h_in.copy_(d_in)
-    h_out = torch.empty(d_out.numel(), dtype=torch.uint8, pin_memory=True)
-    remap = {id(t): v for t, v in zip(ins + outs, v_in + v_out)}
-    specs = [(p, [remap.get(id(t), t) for t in A_r], [remap.get(id(t), t) for t in B_r],
-              [remap.get(id(t), t) for t in C_r], ws) for p, A_r, B_r, C_r, ws in wl.steps_spec]
+    s = wl.s
     stream = torch.cuda.current_stream()
+    pin = lambda t: t.pin_memory()
+    calls = []          # (plan, A_host|None, B_host|None, C_host|None, A_r, B_r, C_r, ws)
+    h2d = d2h = 0
+    final_copy = None
+    specs = wl.steps_spec
+    if wl.name in ("mlp_pair", "mlp_pair_sp"):
+        X, W1, W2 = (pin(t) for t in wl.host_globals)
+        (p1, X_r, W1_r, H_r, ws1), (p2, _, W2_r, Y_r, ws2) = specs
+        last_out = None
+        if wl.name == "mlp_pair":
+            last_out = torch.empty(p2.shape[0], p2.shape[2], dtype=torch.bfloat16).pin_memory()
+        calls.append((p1, X, W1, None, X_r, W1_r, H_r, ws1))
+        calls.append((p2, None, W2, last_out, H_r, W2_r, Y_r, ws2))
+        h2d = sum(t.numel() * t.element_size() for t in (X, W1, W2))
+        if wl.name == "mlp_pair_sp":
+            Y_h = torch.empty(tuple(wl.sp_out[0].shape), dtype=wl.sp_out[0].dtype).pin_memory()
+            final_copy = (Y_h, wl.sp_out[0])
+            d2h = Y_h.numel() * Y_h.element_size()
+        else:
+            d2h = last_out.numel() * last_out.element_size()
+    else:
+        A, B = (pin(t) for t in wl.host_globals)
+        for p, A_r, B_r, C_r, ws in specs:
+            dt = C_r[0].dtype
+            C_h = torch.empty(p.shape[0], p.shape[2], dtype=dt).pin_memory()
+            calls.append((p, A, B, C_h, A_r, B_r, C_r, ws))
+            eb = A.element_size()
+            h2d += _distinct_bytes(p, s.TENSOR_A, eb) + _distinct_bytes(p, s.TENSOR_B, eb)
+            d2h += _distinct_bytes(p, s.TENSOR_C, C_h.element_size())
 
     def one_step():
-        d_in.copy_(h_in, non_blocking=True)
-        for p, A_r, B_r, C_r, ws in specs:
-            p.run(A_r, B_r, C_r, ws, stream=stream)
-        h_out.copy_(d_out, non_blocking=True)
+        for p, A_h, B_h, C_h, A_r, B_r, C_r, ws in calls:
+            p.run_host(A_h, B_h, C_h, A_r, B_r, C_r, ws, stream=stream)
+        if wl.name == "mlp_pair_sp":
+            wl.sp_gather.layernorm_all_gather(specs[-1][3], wl.sp_gamma, wl.sp_beta, wl.sp_out, stream=stream)
+        if final_copy is not None:
+            final_copy[0].copy_(final_copy[1], non_blocking=True)
 
     for _ in range(2):
         one_step()
     torch.cuda.synchronize()
+    s.shmm_sync_status(stream)
     dist_ctx.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -406,9 +420,8 @@ def time_e2e(wl, steps, dist_ctx):
         one_step()
     t1.record(stream)
     torch.cuda.synchronize()
+    s.shmm_sync_status(stream)
     ms = dist_ctx.max(t0.elapsed_time(t1)) / steps
-    h2d = sum(t.numel() * t.element_size() for t in ins)
-    d2h = sum(t.numel() * t.element_size() for t in outs)
     return ms, h2d, d2h
 
 
@@ -464,9 +477,14 @@ def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False):
         times.append(a.elapsed_time(b))
     t = statistics.median(times)
     busbw_factor = {"all_reduce": 2 * (G - 1) / G, "all_to_all": (G - 1) / G / 4}.get(op, (G - 1) / G)
+    # off-rank bytes each rank sends, counted once at the sender ("Sharded
+    # matmuls and collectives on a torus", payload accounting): RS and AG
+    # (G-1)/G of V, AR both, all-to-all (G-1)/G of the rank's V/G
+    payload = {"all_reduce": 2 * (G - 1) * V // G, "all_to_all": (G - 1) * V // (G * G)}.get(op, (G - 1) * V // G)
     return {"op": op, "ranks": G, "MiB_per_rank": mib, "dtype": dtype, "order": "tree" if tree else "sequential",
             "ms_median": t, "ms_best": min(times), "GB_s": nbytes / (t * 1e-3) / 1e9,
-            "bytes": nbytes, "busbw_GB_s": (V / (t * 1e-3) / 1e9) * busbw_factor}
+            "bytes": nbytes, "busbw_GB_s": (V / (t * 1e-3) / 1e9) * busbw_factor,
+            "payload_bytes_per_rank": payload}
 
 
 # --------------------------------------------------------------- oracle
@@ -610,7 +628,8 @@ def run_shmm(args, dist_ctx):
     rs = time_collective(s, H, torch, "reduce_scatter", 8, 256, "f32")
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": N, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "ms_median_step": statistics.median(per_step),
+        "ms_best_step": min(per_step), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload]["text"], "name": args.workload,
                    "launch": "CUDA graph replay" if args.graph else "direct shmm_run calls",
@@ -623,18 +642,25 @@ def run_shmm(args, dist_ctx):
                                                                  for t in wl.output_tensors()),
                      "peak_kind": "%s bf16 burst (cuBLAS 8192^3)" % peak_kind,
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "peak_nominal": NOMINAL_PEAKS["bf16_tflops"],
+                     "frac_of_nominal": achieved / NOMINAL_PEAKS["bf16_tflops"],
                      "kernel": ("gemm_tc2_kernel (CTA pair) with fused reduction epilogue"
                                 if os.environ.get("SHMM_TC_PAIR", "1") != "0"
                                 else "gemm_tc_kernel<256> with fused reduction epilogue")},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "host_link_GB_s": (h2d + d2h) / (e2e_ms * 1e-3) / 1e9,
-                "note": "one pinned H2D copy of all ranks' operands, shmm_run, one D2H copy of all results"},
+                "note": ("shmm_run_host from pinned global host arrays: each distinct shard uploaded once, "
+                         "replicas copied on the device, uploads/GEMMs/downloads pipelined by reduction "
+                         "group; the global result written back to pinned host memory")},
         "gpu_launches": launches,
         "clocks": clocks,
         "reduce_scatter": {"value": rs["GB_s"], "unit": "GB/s", "frac": rs["GB_s"] / peaks["hbm_gbs"],
                            "peak": peaks["hbm_gbs"], "peak_kind": "%s HBM copy" % peak_kind,
                            "config": "fp32 partials, 8 ranks x 256 MiB, sequential rank order, L2 flushed",
-                           "ms": rs["ms_median"], "busbw_GB_s": rs["busbw_GB_s"]},
+                           "ms": rs["ms_median"], "ms_best": rs["ms_best"], "busbw_GB_s": rs["busbw_GB_s"],
+                           "payload_bytes_per_rank": rs["payload_bytes_per_rank"],
+                           "peak_nominal": NOMINAL_PEAKS["hbm_gbs"],
+                           "frac_of_nominal": rs["GB_s"] / NOMINAL_PEAKS["hbm_gbs"]},
     }
     if dist_ctx.rank == 0 and N == 1 and not args.no_cpu_baseline and args.workload == "down_projection":
         out["cpu_baseline"] = cpu_baseline(args.workload, host_globals_f32(wl))

@@ -294,6 +294,41 @@ shmm_status_t shmm_all_gather(const shmm_plan_t *plan, int tensor, const void *c
 shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const void *const *B_r,
                        void *const *C_r, void *workspace, size_t workspace_bytes, void *stream);
 
+/* The sharded matmul end to end from host memory: the pages' input is the
+ * global operands plus their sharding, the output the completed values with
+ * explicit per-rank coordinates ("Sharded matmuls and collectives on a
+ * torus", interface of the sharded matmul).  This call scatters global A and
+ * B onto the ranks' device buffers, runs shmm_run's arithmetic, and writes
+ * the global C back to host memory.
+ *   A_host  in: global A [I, J], row-major, in_dtype, host memory; NULL when
+ *           A_r already holds every rank's shard (nothing is uploaded)
+ *   B_host  in: global B [J, K], likewise
+ *   C_host  out: global C [I, K], row-major, out_dtype, host memory; every
+ *           element written once, from the lowest rank holding it; NULL to
+ *           leave the result on the device only
+ *   A_r[N], B_r[N]  out (or in, for a NULL host operand): device buffers of
+ *           boxes SHMM_TENSOR_A / SHMM_TENSOR_B; each distinct shard crosses
+ *           the host link once, and ranks holding the same box (replicas)
+ *           receive device-to-device copies of it
+ *   C_r[N]  out: box SHMM_TENSOR_C, as for shmm_run
+ *   workspace, workspace_bytes: as for shmm_run
+ * Results are bit for bit those of uploading the shards and calling
+ * shmm_run.  When every unit of work reads only its own ranks' shards (no
+ * operand or result all-gather; a reduction only if fused), the work runs
+ * in up to 4 stages of reduction groups (or of ranks): a stage's uploads
+ * overlap the previous stage's GEMM and its downloads overlap the next.
+ * Copies run on three library-owned streams of the current device (uploads,
+ * replica copies, downloads; created on first use, kept until exit),
+ * ordered against `stream` by events: they start
+ * after the work already enqueued on `stream`, and work enqueued on `stream`
+ * after this call sees every copy complete.  Host buffers must stay valid
+ * until then; page-locked host memory is needed for copies that overlap
+ * compute (pageable memory works, serialised).
+ * Errors: NULL, ALIGN, NOMEM (workspace), CUDA; the shmm_run errors. */
+shmm_status_t shmm_run_host(const shmm_plan_t *plan, const void *A_host, const void *B_host, void *C_host,
+                            void *const *A_r, void *const *B_r, void *const *C_r, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
 /* Reshard a 2-D array [rows, cols] between two shardings on one mesh:
  * every rank's block under `spec_to` is assembled from the blocks holding it
  * under `spec_from` (one read and one write of each element).  This is the

@@ -4,9 +4,13 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "device_wait.cuh"
@@ -104,6 +108,19 @@ shmm_status_t check_ptrs(const shmm_plan_t *p, const void *const *arr, int tenso
     return SHMM_OK;
 }
 
+shmm_status_t check_workspace(const shmm_plan_t *p, const void *workspace, size_t workspace_bytes,
+                              const char *fn) {
+    size_t need = 0;
+    shmm_workspace_size(p, &need);
+    if (workspace_bytes < need)
+        return fail(SHMM_ERR_NOMEM, std::string(fn) + ": workspace of " + std::to_string(workspace_bytes) +
+                                        " bytes, " + std::to_string(need) + " needed");
+    if (need && !workspace) return fail(SHMM_ERR_NULL, std::string(fn) + ": workspace is NULL");
+    if (need && reinterpret_cast<uintptr_t>(workspace) % 256)
+        return fail(SHMM_ERR_ALIGN, std::string(fn) + ": workspace is not 256-byte aligned");
+    return SHMM_OK;
+}
+
 shmm::GemmArgs gemm_args(const shmm_plan_t *p) {
     shmm::GemmArgs g;
     const shmm::Box &al = p->boxes[SHMM_TENSOR_A_LOCAL][0];
@@ -161,6 +178,109 @@ int reduce(const shmm_plan_t *p, const void *const *P, void *const *dst, int mod
     a.src = src.data();
     a.dst = out.data();
     return shmm::launch_reduce(a, status, stream);
+}
+
+// GEMM arguments for units [u0, u1) of the local GEMM: ranks when nothing
+// is reduced, reduction groups when the reduction is fused.  Operands come
+// from A[r], B[r]; results go to dst[r] (a group's owner blocks for a
+// reduce-scatter, every member for an all-reduce).  The pointer arrays live
+// in `ptrs`; slot_rank[i] is the rank of operand slot i.
+struct UnitPtrs {
+    std::vector<const void *> a, b;
+    std::vector<void *> out;
+    std::vector<int> slot_rank;
+};
+shmm::GemmArgs unit_args(const shmm_plan_t *p, const void *const *A, const void *const *B, void *const *dst,
+                         int u0, int u1, UnitPtrs *ptrs) {
+    shmm::GemmArgs ga = gemm_args(p);
+    ga.out_dt = p->out_dt;
+    ga.gelu = (p->flags & SHMM_FLAG_GELU) != 0;
+    ptrs->a.clear();
+    ptrs->b.clear();
+    ptrs->out.clear();
+    ptrs->slot_rank.clear();
+    if (!p->U.n) {
+        ga.units = u1 - u0;
+        ga.G = 1;
+        for (int r = u0; r < u1; ++r) {
+            ptrs->a.push_back(A[r]);
+            ptrs->b.push_back(B[r]);
+            ptrs->out.push_back(dst[r]);
+            ptrs->slot_rank.push_back(r);
+        }
+    } else {
+        const shmm::Groups &g = p->red_groups;
+        const bool rs = p->collective == SHMM_COLL_REDUCE_SCATTER;
+        for (int i = u0 * g.size; i < u1 * g.size; ++i) {
+            const int r = g.members[i];
+            ptrs->a.push_back(A[r]);
+            ptrs->b.push_back(B[r]);
+            ptrs->out.push_back(rs ? dst[g.by_block[i]] : dst[r]);
+            ptrs->slot_rank.push_back(r);
+        }
+        ga.units = u1 - u0;
+        ga.G = g.size;
+        ga.fused = true;
+        ga.rank_order = (p->flags & SHMM_FLAG_RANK_ORDER) != 0;
+        ga.mode = rs ? p->scatter_dim : 2;
+    }
+    ga.A = ptrs->a.data();
+    ga.B = ptrs->b.data();
+    ga.out = ptrs->out.data();
+    return ga;
+}
+
+// Streams shmm_run_host copies on, created once per device and kept for the
+// life of the process: host-to-device uploads, device-to-device replica
+// copies (kept off the upload stream, which the host link limits) and
+// device-to-host downloads, each ordered against the others by events.
+struct SideStreams {
+    cudaStream_t up = nullptr, rep = nullptr, down = nullptr;
+};
+cudaError_t side_streams(SideStreams *out) {
+    static std::mutex mu;
+    static SideStreams cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev].up) {
+        SideStreams s;
+        e = cudaStreamCreateWithFlags(&s.up, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamCreateWithFlags(&s.rep, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            cudaStreamDestroy(s.up);
+            return e;
+        }
+        e = cudaStreamCreateWithFlags(&s.down, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            cudaStreamDestroy(s.up);
+            cudaStreamDestroy(s.rep);
+            return e;
+        }
+        cache[dev] = s;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+// Box b of a row-major global host array with `cols` columns <-> a dense
+// device buffer holding exactly that box.  Whole rows are one linear copy.
+cudaError_t upload_box(void *dev, const void *host, const shmm::Box &b, int64_t cols, int64_t es,
+                       cudaStream_t s) {
+    const char *src = static_cast<const char *>(host) + (b.off[0] * cols + b.off[1]) * es;
+    const size_t w = (size_t)(b.ext[1] * es);
+    if (b.ext[1] == cols) return cudaMemcpyAsync(dev, src, w * (size_t)b.ext[0], cudaMemcpyHostToDevice, s);
+    return cudaMemcpy2DAsync(dev, w, src, (size_t)(cols * es), w, (size_t)b.ext[0], cudaMemcpyHostToDevice, s);
+}
+cudaError_t download_box(void *host, const void *dev, const shmm::Box &b, int64_t cols, int64_t es,
+                         cudaStream_t s) {
+    char *dst = static_cast<char *>(host) + (b.off[0] * cols + b.off[1]) * es;
+    const size_t w = (size_t)(b.ext[1] * es);
+    if (b.ext[1] == cols) return cudaMemcpyAsync(dst, dev, w * (size_t)b.ext[0], cudaMemcpyDeviceToHost, s);
+    return cudaMemcpy2DAsync(dst, (size_t)(cols * es), dev, w, w, (size_t)b.ext[0], cudaMemcpyDeviceToHost, s);
 }
 
 int gather(const shmm_plan_t *p, const shmm::Groups &g, int src_tensor, int64_t elem,
@@ -326,14 +446,7 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
     if ((st = check_ptrs(p, A_r, SHMM_TENSOR_A, fn, "A_r")) != SHMM_OK) return st;
     if ((st = check_ptrs(p, B_r, SHMM_TENSOR_B, fn, "B_r")) != SHMM_OK) return st;
     if ((st = check_ptrs(p, (const void *const *)C_r, SHMM_TENSOR_C, fn, "C_r")) != SHMM_OK) return st;
-    size_t need = 0;
-    shmm_workspace_size(p, &need);
-    if (workspace_bytes < need)
-        return fail(SHMM_ERR_NOMEM, std::string(fn) + ": workspace of " + std::to_string(workspace_bytes) +
-                                        " bytes, " + std::to_string(need) + " needed");
-    if (need && !workspace) return fail(SHMM_ERR_NULL, std::string(fn) + ": workspace is NULL");
-    if (need && reinterpret_cast<uintptr_t>(workspace) % 256)
-        return fail(SHMM_ERR_ALIGN, std::string(fn) + ": workspace is not 256-byte aligned");
+    if ((st = check_workspace(p, workspace, workspace_bytes, fn)) != SHMM_OK) return st;
     std::string err;
     int *status = status_ptr(&err);
     if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
@@ -403,42 +516,15 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         carve(SHMM_TENSOR_C_REDUCED, out_b, &wc);
         dst = wc;
     }
-    const bool gelu = (p->flags & SHMM_FLAG_GELU) != 0;
-    std::vector<int> by_rank(p->nranks);
-    for (int r = 0; r < p->nranks; ++r) by_rank[r] = r;
+    UnitPtrs up;
     if (!p->U.n) {
-        shmm::GemmArgs ga = gemm_args(p);
-        ga.units = p->nranks;
-        ga.G = 1;
-        ga.out_dt = p->out_dt;
-        ga.gelu = gelu;
-        ga.A = A_loc.data();
-        ga.B = B_loc.data();
-        ga.out = dst.data();
-        attach_gather(&ga, by_rank);
+        shmm::GemmArgs ga = unit_args(p, A_loc.data(), B_loc.data(), dst.data(), 0, p->nranks, &up);
+        attach_gather(&ga, up.slot_rank);
         e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
     } else if (fused) {
-        const shmm::Groups &g = p->red_groups;
-        std::vector<const void *> fa(g.members.size()), fb(g.members.size());
-        std::vector<void *> fo(g.members.size());
-        for (size_t i = 0; i < g.members.size(); ++i) {
-            fa[i] = A_loc[g.members[i]];
-            fb[i] = B_loc[g.members[i]];
-            fo[i] = p->collective == SHMM_COLL_REDUCE_SCATTER ? dst[g.by_block[i]] : dst[g.members[i]];
-        }
-        shmm::GemmArgs ga = gemm_args(p);
-        ga.units = g.count;
-        ga.G = g.size;
-        ga.fused = true;
-        ga.rank_order = (p->flags & SHMM_FLAG_RANK_ORDER) != 0;
-        ga.mode = p->collective == SHMM_COLL_REDUCE_SCATTER ? p->scatter_dim : 2;
-        ga.gelu = gelu;
-        ga.out_dt = p->out_dt;
-        ga.A = fa.data();
-        ga.B = fb.data();
-        ga.out = fo.data();
-        attach_gather(&ga, g.members);
+        shmm::GemmArgs ga = unit_args(p, A_loc.data(), B_loc.data(), dst.data(), 0, p->red_groups.count, &up);
+        attach_gather(&ga, up.slot_rank);
         e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
     } else {
@@ -449,6 +535,8 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         ga.A = A_loc.data();
         ga.B = B_loc.data();
         ga.out = wp.data();
+        std::vector<int> by_rank(p->nranks);
+        for (int r = 0; r < p->nranks; ++r) by_rank[r] = r;
         attach_gather(&ga, by_rank);
         e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
@@ -554,6 +642,145 @@ shmm_status_t shmm_run_static_workspace(const shmm_plan_t *p, const void *const 
         if (!ws) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
     }
     return shmm_run(p, A_r, B_r, C_r, ws, need, stream);
+}
+
+shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void *B_host, void *C_host,
+                            void *const *A_r, void *const *B_r, void *const *C_r, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    static const char *fn = "shmm_run_host";
+    constexpr int kStages = 4;
+    shmm::clear_error();
+    if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    shmm_status_t st;
+    if ((st = check_ptrs(p, (const void *const *)A_r, SHMM_TENSOR_A, fn, "A_r")) != SHMM_OK) return st;
+    if ((st = check_ptrs(p, (const void *const *)B_r, SHMM_TENSOR_B, fn, "B_r")) != SHMM_OK) return st;
+    if ((st = check_ptrs(p, (const void *const *)C_r, SHMM_TENSOR_C, fn, "C_r")) != SHMM_OK) return st;
+    if ((st = check_workspace(p, workspace, workspace_bytes, fn)) != SHMM_OK) return st;
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    SideStreams ss;
+    cudaError_t e = side_streams(&ss);
+    if (e != cudaSuccess) return cuda_fail(fn, e, "side streams");
+
+    // Units whose GEMMs read only their own ranks' shards and write only
+    // their own ranks' results (no operand or result gather; a reduction
+    // only if fused): uploads of later stages overlap earlier stages' GEMMs,
+    // and downloads overlap later GEMMs.  Otherwise one stage runs shmm_run.
+    const bool staged = !p->gA.n && !p->gB.n && !p->gC.n && (!p->U.n || p->fused);
+    const int units = p->U.n ? p->red_groups.count : p->nranks;
+    const int stages = staged ? std::min(units, kStages) : 1;
+    const int64_t in_b = shmm::elem_bytes(p->in_dt), out_b = shmm::elem_bytes(p->out_dt);
+    cudaStream_t cs = (cudaStream_t)stream;
+
+    std::vector<cudaEvent_t> events;
+    auto record = [&](cudaStream_t on, cudaStream_t waiter) -> cudaError_t {
+        cudaEvent_t ev;
+        cudaError_t r = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (r != cudaSuccess) return r;
+        events.push_back(ev);
+        r = cudaEventRecord(ev, on);
+        return r == cudaSuccess ? cudaStreamWaitEvent(waiter, ev, 0) : r;
+    };
+    // Every exit joins both side streams back into the caller's stream, so
+    // nothing this call enqueued outlives what the caller orders after it.
+    auto finish = [&](shmm_status_t result) -> shmm_status_t {
+        record(ss.up, cs);
+        record(ss.rep, cs);
+        record(ss.down, cs);
+        for (cudaEvent_t ev : events) cudaEventDestroy(ev);  // released once complete
+        return result;
+    };
+    if ((e = record(cs, ss.up)) != cudaSuccess || (e = record(cs, ss.rep)) != cudaSuccess ||
+        (e = record(cs, ss.down)) != cudaSuccess)
+        return finish(cuda_fail(fn, e, "events"));
+
+    // Each distinct shard crosses the host link once; a replica is a device
+    // copy of the first rank's upload, on the replica stream after an event
+    // that follows the stage's uploads.
+    std::map<std::pair<int64_t, int64_t>, int> first_a, first_b, done_c;
+    struct Replica {
+        void *dst;
+        const void *src;
+        size_t bytes;
+    };
+    std::vector<Replica> replicas;
+    auto upload = [&](int r) -> cudaError_t {
+        struct Op {
+            const void *host;
+            int tensor;
+            int64_t cols;
+            void *const *dev;
+            std::map<std::pair<int64_t, int64_t>, int> *first;
+        } ops[2] = {{A_host, SHMM_TENSOR_A, p->J, A_r, &first_a}, {B_host, SHMM_TENSOR_B, p->K, B_r, &first_b}};
+        for (const Op &o : ops) {
+            const shmm::Box &b = p->boxes[o.tensor][r];
+            if (!o.host || b.numel() == 0) continue;
+            const auto key = std::make_pair(b.off[0], b.off[1]);
+            const auto it = o.first->find(key);
+            cudaError_t r2;
+            if (it == o.first->end()) {
+                (*o.first)[key] = r;
+                r2 = upload_box(o.dev[r], o.host, b, o.cols, in_b, ss.up);
+            } else {
+                replicas.push_back({o.dev[r], o.dev[it->second], (size_t)(b.numel() * in_b)});
+                r2 = cudaSuccess;
+            }
+            if (r2 != cudaSuccess) return r2;
+        }
+        return cudaSuccess;
+    };
+    auto download = [&](int r) -> cudaError_t {
+        const shmm::Box &b = p->boxes[SHMM_TENSOR_C][r];
+        if (!C_host || b.numel() == 0) return cudaSuccess;
+        const auto key = std::make_pair(b.off[0], b.off[1]);
+        if (done_c.count(key)) return cudaSuccess;  // a replica: written once
+        done_c[key] = r;
+        return download_box(C_host, C_r[r], b, p->K, out_b, ss.down);
+    };
+
+    for (int s = 0; s < stages; ++s) {
+        const int u0 = s * units / stages, u1 = (s + 1) * units / stages;
+        std::vector<int> ranks;
+        if (!staged) {
+            for (int r = 0; r < p->nranks; ++r) ranks.push_back(r);
+        } else if (!p->U.n) {
+            for (int r = u0; r < u1; ++r) ranks.push_back(r);
+        } else {
+            const shmm::Groups &g = p->red_groups;
+            for (int i = u0 * g.size; i < u1 * g.size; ++i) ranks.push_back(g.members[i]);
+        }
+        replicas.clear();
+        for (int r : ranks)
+            if ((e = upload(r)) != cudaSuccess) return finish(cuda_fail(fn, e, "upload"));
+        if ((e = record(ss.up, cs)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
+        if (!replicas.empty()) {
+            if ((e = record(ss.up, ss.rep)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
+            for (const Replica &c : replicas)
+                if ((e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToDevice, ss.rep)) != cudaSuccess)
+                    return finish(cuda_fail(fn, e, "replica copy"));
+            if ((e = record(ss.rep, cs)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
+        }
+        if (staged) {
+            UnitPtrs up;
+            const shmm::GemmArgs ga = unit_args(p, (const void *const *)A_r, (const void *const *)B_r, C_r, u0,
+                                                u1, &up);
+            const int ge = run_gemm(p, ga, status, stream, &err);
+            if (ge) return finish(cuda_fail(fn, ge, err));
+        } else {
+            st = shmm_run(p, (const void *const *)A_r, (const void *const *)B_r, C_r, workspace,
+                          workspace_bytes, stream);
+            if (st != SHMM_OK) {
+                const std::string m = shmm_last_error();
+                return finish(fail(st, std::string(fn) + ": " + m));
+            }
+        }
+        if ((e = record(cs, ss.down)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
+        for (int r : ranks)
+            if ((e = download(r)) != cudaSuccess) return finish(cuda_fail(fn, e, "download"));
+    }
+    return finish(SHMM_OK);
 }
 
 shmm_status_t shmm_selftest_wait_timeout(uint64_t limit_cycles, void *stream) {

@@ -82,7 +82,7 @@ EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
            "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace",
            "shmm_selftest_wait_timeout", "shmm_choose_operand", "shmm_reshard", "shmm_layernorm",
-           "shmm_layernorm_all_gather"]
+           "shmm_layernorm_all_gather", "shmm_run_host"]
 
 _lib = None
 
@@ -114,6 +114,7 @@ def lib():
         L.shmm_all_gather.argtypes = [P, ctypes.c_int, PP, PP, P]
         L.shmm_run.argtypes = [P, PP, PP, PP, P, ctypes.c_size_t, P]
         L.shmm_run_static_workspace.argtypes = [P, PP, PP, PP, P]
+        L.shmm_run_host.argtypes = [P, P, P, P, PP, PP, PP, P, ctypes.c_size_t, P]
         L.shmm_sync_status.argtypes = [P]
         L.shmm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
         L.shmm_layernorm.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P, P, ctypes.c_float, P, P]
@@ -336,6 +337,26 @@ class Plan:
                                                beta.data_ptr(), float(eps), _ptr_array(full_r, "full"),
                                                _stream_handle(stream)))
 
+    def run_host(self, A_host, B_host, C_host, A_r, B_r, C_r, workspace=None, stream=None):
+        """shmm_run_host: global A [I,J], B [J,K] (CPU tensors, pinned for
+        overlap, or None when A_r / B_r already hold the shards) in, global C
+        [I,K] (a CPU tensor, or None) out, through the ranks' device buffers."""
+        def host_ptr(t, shape, what):
+            if t is None:
+                return None
+            if (not hasattr(t, "data_ptr") or t.device.type != "cpu" or not t.is_contiguous()
+                    or tuple(t.shape) != shape):
+                raise ValueError("%s_host must be a contiguous CPU tensor of shape %s" % (what, shape))
+            return t.data_ptr()
+        ws_ptr = None if workspace is None else (workspace if isinstance(workspace, int) else workspace.data_ptr())
+        ws_bytes = 0 if workspace is None else (
+            self.workspace_size() if isinstance(workspace, int) else workspace.numel() * workspace.element_size())
+        I, J, K = self.shape
+        _check(lib().shmm_run_host(self._h, host_ptr(A_host, (I, J), "A"), host_ptr(B_host, (J, K), "B"),
+                                   host_ptr(C_host, (I, K), "C"),
+                                   _ptr_array(A_r, "A"), _ptr_array(B_r, "B"), _ptr_array(C_r, "C"),
+                                   ws_ptr, ws_bytes, _stream_handle(stream)))
+
     def run_static_workspace(self, A_r, B_r, C_r, stream=None):
         """shmm_run on the library's fixed 64 MiB device workspace, for
         callers that cannot allocate device memory (see include/shmm.h)."""
@@ -382,6 +403,10 @@ def shmm_all_gather(plan: Plan, tensor: int, shard_r, full_r, stream=None):
 
 def shmm_run(plan: Plan, A_r, B_r, C_r, workspace=None, stream=None):
     plan.run(A_r, B_r, C_r, workspace, stream)
+
+
+def shmm_run_host(plan: Plan, A_host, B_host, C_host, A_r, B_r, C_r, workspace=None, stream=None):
+    plan.run_host(A_host, B_host, C_host, A_r, B_r, C_r, workspace, stream)
 
 
 def shmm_run_static_workspace(plan: Plan, A_r, B_r, C_r, stream=None):

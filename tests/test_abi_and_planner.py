@@ -215,7 +215,18 @@ def test_argument_checks_before_any_device_call(shmm, monkeypatch):
     assert L.shmm_run(pr.handle, good, good, good, ctypes.c_void_p(0x100080), 1 << 20, None) == \
         shmm.shmm.ERR_ALIGN
     assert L.shmm_run(None, good, good, good, None, 0, None) == shmm.shmm.ERR_NULL
-    monkeypatch.setenv("SHMM_INJECT_FAIL", "shmm_run,shmm_all_reduce")
+    # shmm_run_host checks the same arguments before any copy is enqueued
+    h = ctypes.c_void_p(0x30000)
+    assert L.shmm_run_host(None, h, h, h, good, good, good, None, 0, None) == shmm.shmm.ERR_NULL
+    assert L.shmm_run_host(pr.handle, h, h, h, nulls, good, good, None, 0, None) == shmm.shmm.ERR_NULL
+    assert L.shmm_run_host(pr.handle, h, h, h, good, bad_align, good, None, 0, None) == shmm.shmm.ERR_ALIGN
+    assert L.shmm_run_host(pr.handle, h, h, h, good, good, good, None, 0, None) == shmm.shmm.ERR_NOMEM
+    import torch
+    for bad in (np.zeros((64, 64)), torch.zeros(64, 32), torch.zeros(64, 128)[:, :64]):
+        with pytest.raises(ValueError):
+            pr.run_host(bad, None, None, [0x10000] * 2, [0x10000] * 2, [0x10000] * 2)
+    monkeypatch.setenv("SHMM_INJECT_FAIL", "shmm_run,shmm_all_reduce,shmm_run_host")
+    assert L.shmm_run_host(pr.handle, h, h, h, good, good, good, None, 0, None) == shmm.shmm.ERR_INJECTED
     assert L.shmm_run(pr.handle, good, good, good, None, 0, None) == shmm.shmm.ERR_INJECTED
     assert L.shmm_all_reduce(pr.handle, good, good, None) == shmm.shmm.ERR_INJECTED
     assert b"injected" in L.shmm_last_error()
