@@ -313,6 +313,26 @@ __device__ __forceinline__ void store_tile_row(const TcK &k, int unit, int Gq, i
     }
 }
 
+// Work item t -> (unit, m-tile, n-tile).  Within a unit the tiles run in
+// bands of kBandM m-tiles: m fastest inside a band, then n, then the next
+// band.  The CTAs working at one time then cover a roughly square block of
+// the output (about 8 x 9.5 tiles for 76 CTA pairs) instead of a few whole
+// columns, so each wave streams fewer A row panels and B column panels from
+// DRAM.
+constexpr int kBandM = 8;
+__device__ __forceinline__ void tile_coords(const TcK &k, int t, int *unit, int *mt, int *nt) {
+    const int per_unit = k.m_tiles * k.n_tiles;
+    *unit = t / per_unit;
+    const int r = t - *unit * per_unit;
+    const int band_tiles = kBandM * k.n_tiles;
+    const int band = r / band_tiles;
+    const int m0 = band * kBandM;
+    const int bm = k.m_tiles - m0 < kBandM ? k.m_tiles - m0 : kBandM;  // the last band may be short
+    const int q = r - band * band_tiles;
+    *mt = m0 + q % bm;
+    *nt = q / bm;
+}
+
 template <int BN>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;           // 16 KB
@@ -381,12 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    auto decode = [&](int t, int *unit, int *mt, int *nt) {
-        *unit = t / tiles_per_unit;
-        const int r = t - *unit * tiles_per_unit;
-        *mt = r % k.m_tiles;  // m fastest: neighbouring CTAs share a B column block
-        *nt = r / k.m_tiles;
-    };
+    auto decode = [&](int t, int *unit, int *mt, int *nt) { tile_coords(k, t, unit, mt, nt); };
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -662,12 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    auto decode = [&](int t, int *unit, int *mt, int *nt) {
-        *unit = t / tiles_per_unit;
-        const int r = t - *unit * tiles_per_unit;
-        *mt = r % k.m_tiles;
-        *nt = r / k.m_tiles;
-    };
+    auto decode = [&](int t, int *unit, int *mt, int *nt) { tile_coords(k, t, unit, mt, nt); };
 
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
