@@ -51,6 +51,7 @@ struct TcK {
     CUtensorMap tmA[kMaxMaps];   // one map per distinct A shard of the launch
     CUtensorMap tmB[kMaxMaps];
     void *out[kMaxMaps];
+    CUtensorMap tmC[kMaxMaps];  // output i as the epilogue's TMA stores see it
     int *status;
     int units, G, mode;
     int fused, gelu, out_f32;
@@ -65,6 +66,7 @@ struct TcK {
     int64_t a_brows, a_bcols, b_brows, b_bcols;
     int n_maps_a, n_maps_b;
     int gathered;  // 0: map i is operand slot i's own buffer
+    int tma_store;  // 1: the epilogue stores through tmC, else per-thread stores
 };
 
 // Operands read in place from an all-gather group's shards: which shard of
@@ -94,6 +96,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
+}
+
+// Bulk tensor store of a staged shared-memory box to global memory; bulk
+// groups are per-thread state, so one lane issues, commits and waits.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most one committed store group may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy shared-memory writes become visible to the async proxy.
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
@@ -333,13 +355,96 @@ __device__ __forceinline__ void tile_coords(const TcK &k, int t, int *unit, int 
     *nt = q / bm;
 }
 
+// Epilogue output staging: per epilogue warp two buffers of one 32 x 32 box
+// (4 KB at fp32), so a warp fills one while the previous box's store reads
+// the other.
+constexpr int kStageBoxBytes = 32 * 32 * 4;
+constexpr int kStagingBytes = 4 * 2 * kStageBoxBytes;
+
+// Row r of a 32 x 32 output box into its staging buffer, in the swizzled
+// layout the output tensor maps declare: bf16 rows are 64 bytes and 16-byte
+// unit j lands at unit j ^ ((r >> 1) & 3) (64-byte swizzle); fp32 rows are
+// 128 bytes and unit j lands at j ^ (r & 7) (128-byte swizzle).  A warp's 32
+// rows then spread over all banks: four shared-memory wavefronts per 16-byte
+// store, the minimum for 512 bytes.
+__device__ __forceinline__ void stage_row(uint32_t buf, int r, const float *v, bool f32) {
+    if (f32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t a = buf + (uint32_t)(r * 128 + ((j ^ (r & 7)) * 16));
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[4 * j]), "f"(v[4 * j + 1]),
+                         "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                         : "memory");
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+            const uint32_t a = buf + (uint32_t)(r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+        }
+    }
+}
+
+// Final pass over one finished tile for one epilogue warp: output rows
+// row0..row0+31 (row0 < M), TMEM lanes from lane_s.  Each 32-column chunk is
+// loaded from TMEM, passed through GeLU if asked, rounded into the warp's
+// staging buffer and written by one bulk tensor store per destination: the
+// unit's block, the owner's block of a reduce-scatter, or every member's
+// copy of an all-reduce.  Stores clip at the output's edges.  `staged`
+// counts the warp's boxes (it picks the buffer).
+__device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, int row0, int nt, uint32_t lane_s,
+                                               uint32_t cbuf, uint32_t *staged, int lane) {
+    constexpr int BN = 256;
+    const bool f32 = k.out_f32 != 0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = nt * BN + c * 32;
+        if (col0 >= k.N) break;
+        float v[32];
+        tmem_ld32(lane_s + (uint32_t)(c * 32), v);
+        if (k.gelu) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+        }
+        const uint32_t buf = cbuf + (*staged & 1u) * (uint32_t)kStageBoxBytes;
+        if (lane == 0) bulk_wait_read_1();  // the store two boxes back has read this buffer
+        __syncwarp();
+        stage_row(buf, lane, v, f32);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (!k.fused) {
+                tma_store_2d(&k.tmC[unit], buf, col0, row0);
+            } else if (k.mode == 0) {
+                const int per = (int)(k.M / Gq), b = row0 / per;
+                tma_store_2d(&k.tmC[unit * Gq + b], buf, col0, row0 - b * per);
+            } else if (k.mode == 1) {
+                const int per = (int)(k.N / Gq), b = col0 / per;
+                tma_store_2d(&k.tmC[unit * Gq + b], buf, col0 - b * per, row0);
+            } else {
+                for (int b = 0; b < Gq; ++b) tma_store_2d(&k.tmC[unit * Gq + b], buf, col0, row0);
+            }
+            bulk_commit();
+        }
+        ++*staged;
+    }
+}
+
 template <int BN>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;           // 16 KB
     static constexpr int B_BYTES = BK * BN * 2;           // BN * 128
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
-    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 1024 /*barriers, tables*/;
+    static constexpr int SMEM = STAGES * STAGE + kStagingBytes + 1024 /*align*/ + 1024 /*barriers, tables*/;
 };
 
 template <int BN>
@@ -350,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *tiles = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::STAGE);
+    uint8_t *staging = smem + S * C::STAGE;  // 1024-byte aligned: the swizzle needs it
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + kStagingBytes);
     // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -522,6 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const bool f32 = k.out_f32 != 0;
         const int64_t es = f32 ? 4 : 2;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+        const uint32_t cbuf = smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes);
+        uint32_t staged = 0;
         uint32_t used0 = 0, used1 = 0;  // finished products consumed per buffer
         // One lane waits; the warp reconverges before the .sync.aligned TMEM
         // instructions.
@@ -565,24 +673,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 mbar_arrive(acce_bar(bW));  // W may take the next product
             }
             if (!ok) break;
-            const int64_t row = (int64_t)mt * BM + row_in_tile;
-            const bool row_ok = row < k.M;
+            if (k.tma_store) {
+                const int row0 = mt * BM + quad * 32;
+                if (row0 < k.M) store_tile_tma(k, unit, Gq, row0, nt, s_base, cbuf, &staged, lane);
+            } else {
+                const int64_t row = (int64_t)mt * BM + row_in_tile;
+                const bool row_ok = row < k.M;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                float v[32];
-                tmem_ld32(s_base + (uint32_t)(c * 32), v);
-                if (k.gelu) {
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(s_base + (uint32_t)(c * 32), v);
+                    if (k.gelu) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                    }
+                    const int64_t col0 = (int64_t)nt * BN + c * 32;
+                    if (!row_ok || col0 >= k.N) continue;
+                    const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
+                    store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
                 }
-                const int64_t col0 = (int64_t)nt * BN + c * 32;
-                if (!row_ok || col0 >= k.N) continue;
-                const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
-                store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
             }
             fence_before();
             mbar_arrive(acce_bar(bS));  // S may take the next tile's products
         }
+        if (lane == 0) bulk_wait_all();  // no store still reads staging at exit
+        __syncwarp();
     }
 
     fence_before();
@@ -611,7 +726,7 @@ struct Cfg2 {
     static constexpr int B_BYTES = BK * 128 * 2;  // 16 KB: this CTA's 128 columns
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int STAGES = 6;
-    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 1024 /*barriers, tables*/;
+    static constexpr int SMEM = STAGES * STAGE + kStagingBytes + 1024 /*align*/ + 1024 /*barriers, tables*/;
 };
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcK k) {
@@ -622,7 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *tiles = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::STAGE);
+    uint8_t *staging = smem + S * C::STAGE;  // 1024-byte aligned: the swizzle needs it
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + kStagingBytes);
     // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -796,6 +912,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
         const bool f32 = k.out_f32 != 0;
         const int64_t es = f32 ? 4 : 2;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+        const uint32_t cbuf = smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes);
+        uint32_t staged = 0;
         uint32_t used0 = 0, used1 = 0;
         auto warp_wait_full = [&](int b) -> bool {
             const uint32_t n = b ? used1 : used0;
@@ -839,23 +957,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
                 release(bW);
             }
             if (!ok) break;
-            const int64_t row = (int64_t)mt * 256 + row_in_tile;
-            const bool row_ok = row < k.M;
+            if (k.tma_store) {
+                const int row0 = mt * 256 + (int)cr * BM + quad * 32;
+                if (row0 < k.M) store_tile_tma(k, unit, Gq, row0, nt, s_base, cbuf, &staged, lane);
+            } else {
+                const int64_t row = (int64_t)mt * 256 + row_in_tile;
+                const bool row_ok = row < k.M;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                float v[32];
-                tmem_ld32(s_base + (uint32_t)(c * 32), v);
-                if (k.gelu) {
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(s_base + (uint32_t)(c * 32), v);
+                    if (k.gelu) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                    }
+                    const int64_t col0 = (int64_t)nt * BN + c * 32;
+                    if (!row_ok || col0 >= k.N) continue;
+                    const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
+                    store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
                 }
-                const int64_t col0 = (int64_t)nt * BN + c * 32;
-                if (!row_ok || col0 >= k.N) continue;
-                const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
-                store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
             }
             release(bS);
         }
+        if (lane == 0) bulk_wait_all();  // no store still reads staging at exit
+        __syncwarp();
     }
 
     fence_before();
@@ -893,15 +1018,17 @@ EncodeTiledFn encode_fn(std::string *msg) {
     return fn;
 }
 
-// 2-D bf16 tensor map over a row-major rows x cols matrix, box (bx inner, by).
-bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
-              uint32_t bx, uint32_t by) {
+// 2-D tensor map over a row-major rows x cols matrix, box (bx inner, by):
+// bf16 operands with 128-byte swizzle by default; the epilogue's output maps
+// pass their own element type and swizzle.
+bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t bx,
+              uint32_t by, bool f32 = false, CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+    const cuuint64_t strides[1] = {(cuuint64_t)(cols * (f32 ? 4 : 2))};
     const cuuint32_t box[2] = {bx, by};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -912,18 +1039,21 @@ struct MapCacheEntry {
     const void *ptr;
     int64_t rows, cols;
     uint32_t bx, by;
+    bool f32;
+    CUtensorMapSwizzle sw;
     bool valid;
     CUtensorMap map;
 };
 
-bool cached_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
-                uint32_t bx, uint32_t by) {
+bool cached_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t bx,
+                uint32_t by, bool f32 = false, CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
     constexpr int kEntries = 64;
     thread_local MapCacheEntry cache[kEntries] = {};
     thread_local int next = 0;
     for (int i = 0; i < kEntries; ++i) {
         const MapCacheEntry &e = cache[i];
-        if (e.valid && e.ptr == base && e.rows == rows && e.cols == cols && e.bx == bx && e.by == by) {
+        if (e.valid && e.ptr == base && e.rows == rows && e.cols == cols && e.bx == bx && e.by == by &&
+            e.f32 == f32 && e.sw == sw) {
             *m = e.map;
             return true;
         }
@@ -931,8 +1061,10 @@ bool cached_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows
     MapCacheEntry &e = cache[next];
     next = (next + 1) % kEntries;
     e.valid = false;
-    if (!make_map(fn, &e.map, base, rows, cols, bx, by)) return false;
+    if (!make_map(fn, &e.map, base, rows, cols, bx, by, f32, sw)) return false;
     e.ptr = base;
+    e.f32 = f32;
+    e.sw = sw;
     e.rows = rows;
     e.cols = cols;
     e.bx = bx;
@@ -1111,6 +1243,24 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         k.b_bcols = b_cols;
         const int nout = a.fused ? nu * G : nu;
         for (int i = 0; i < nout; ++i) k.out[i] = a.out[(a.fused ? u0 * G : u0) + i];
+        // Output maps for the TMA-store epilogue: each destination block as
+        // rows x cols, 32 x 32 boxes.  A reduce-scatter's owner blocks must
+        // hold whole 32-row (32-column) boxes, else per-thread stores.
+        const bool out_f32 = a.out_dt == SHMM_F32;
+        int64_t c_rows = a.M, c_cols = a.N;
+        bool tma_store = true;
+        if (a.fused && a.mode == 0) {
+            c_rows = a.M / G;
+            tma_store = c_rows % 32 == 0;
+        } else if (a.fused && a.mode == 1) {
+            c_cols = a.N / G;
+            tma_store = c_cols % 32 == 0;
+        }
+        if ((c_cols * (out_f32 ? 4 : 2)) % 16) tma_store = false;
+        for (int i = 0; i < nout && tma_store; ++i)
+            tma_store = cached_map(fn, &k.tmC[i], k.out[i], c_rows, c_cols, 32, 32, out_f32,
+                                   out_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        k.tma_store = tma_store ? 1 : 0;
         k.status = status;
         k.units = nu;
         k.G = G;
