@@ -362,31 +362,8 @@ static shmm_status_t reduce_entry(const char *fn, const shmm_plan_t *p, const vo
     std::string err;
     int *status = status_ptr(&err);
     if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
-    // An all-reduce plan reduce-scattered by rows: owners in member order.
-    if (!all_reduce && p->scatter_dim < 0) {
-        const shmm::Groups &g = p->red_groups;
-        std::vector<const void *> src(g.members.size());
-        std::vector<void *> out(g.members.size());
-        for (size_t i = 0; i < g.members.size(); ++i) {
-            src[i] = P_r[g.members[i]];
-            out[i] = C_r[g.members[i]];
-        }
-        shmm::ReduceArgs a;
-        a.G = g.size;
-        a.ngroups = g.count;
-        a.rows = p->boxes[SHMM_TENSOR_P][0].ext[0];
-        a.cols = p->boxes[SHMM_TENSOR_P][0].ext[1];
-        a.mode = 0;
-        a.tree = (p->flags & SHMM_FLAG_TREE) != 0;
-        a.gelu = (p->flags & SHMM_FLAG_GELU) != 0;
-        a.pt = p->part_dt;
-        a.ot = p->out_dt;
-        a.src = src.data();
-        a.dst = out.data();
-        const int e = shmm::launch_reduce(a, status, stream);
-        if (e) return cuda_fail(fn, e);
-        return SHMM_OK;
-    }
+    // An all-reduce plan reduce-scattered by rows (mode 0, no scatter dim):
+    // reduce() gives row block q to the group's q-th member.
     const int e = reduce(p, P_r, C_r, mode, status, stream);
     if (e) return cuda_fail(fn, e);
     return SHMM_OK;
