@@ -315,8 +315,10 @@ shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const vo
  * Results are bit for bit those of uploading the shards and calling
  * shmm_run.  When every unit of work reads only its own ranks' shards (no
  * operand or result all-gather; a reduction only if fused), the work runs
- * in up to 4 stages of reduction groups (or of ranks): a stage's uploads
- * overlap the previous stage's GEMM and its downloads overlap the next.
+ * in up to 16 stages (reduction groups or ranks, each split into blocks of
+ * 256-row multiples when there are few of them and a block of C rows needs
+ * only the same rows of A): a stage's uploads overlap the previous stage's
+ * GEMM and its downloads overlap the next.
  * Copies run on three library-owned streams of the current device (uploads,
  * replica copies, downloads; created on first use, kept until exit),
  * ordered against `stream` by events: they start

@@ -625,7 +625,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
                             void *const *A_r, void *const *B_r, void *const *C_r, void *workspace,
                             size_t workspace_bytes, void *stream) {
     static const char *fn = "shmm_run_host";
-    constexpr int kStages = 4;
+    constexpr int kStages = 16;
     shmm::clear_error();
     if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
@@ -645,10 +645,40 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
     // their own ranks' results (no operand or result gather; a reduction
     // only if fused): uploads of later stages overlap earlier stages' GEMMs,
     // and downloads overlap later GEMMs.  Otherwise one stage runs shmm_run.
+    // With few units, a unit's stage is further split into blocks of output
+    // rows (multiples of the 256-row tile) wherever a block of C rows needs
+    // only the same rows of A: no reduction, an all-reduce, or a
+    // reduce-scatter over columns.
     const bool staged = !p->gA.n && !p->gB.n && !p->gC.n && (!p->U.n || p->fused);
     const int units = p->U.n ? p->red_groups.count : p->nranks;
-    const int stages = staged ? std::min(units, kStages) : 1;
+    const int64_t M = p->boxes[SHMM_TENSOR_A_LOCAL][0].ext[0];
+    const int64_t Kd = p->boxes[SHMM_TENSOR_A_LOCAL][0].ext[1];
+    const int64_t c_cols = p->boxes[SHMM_TENSOR_C][0].ext[1];
+    // At most one stage per 16 MB of host operands: a stage costs a launch
+    // and a few events, ~10-20 us, against ~76 us to upload 16 MB.
     const int64_t in_b = shmm::elem_bytes(p->in_dt), out_b = shmm::elem_bytes(p->out_dt);
+    const int64_t host_bytes = ((A_host ? p->I * p->J : 0) + (B_host ? p->J * p->K : 0)) * in_b;
+    const int want_stages = (int)std::max<int64_t>(1, std::min<int64_t>(kStages, host_bytes >> 24));
+    const bool row_blocks = staged && units < want_stages &&
+                            !(p->U.n && p->collective == SHMM_COLL_REDUCE_SCATTER && p->scatter_dim == 0);
+    struct Stage {
+        int u0, u1;
+        bool block;      // a block of rows: [r0, r1) of the units' A and C boxes
+        int64_t r0, r1;  // (otherwise whole boxes)
+    };
+    std::vector<Stage> plan_stages;
+    if (!staged) {
+        plan_stages.push_back({0, units, false, 0, M});
+    } else if (row_blocks) {
+        const int64_t want = std::min<int64_t>((want_stages + units - 1) / units, (M + 255) / 256);
+        const int64_t rows = ((M + want - 1) / want + 255) / 256 * 256;
+        for (int u = 0; u < units; ++u)
+            for (int64_t r0 = 0; r0 < M; r0 += rows)
+                plan_stages.push_back({u, u + 1, true, r0, std::min(M, r0 + rows)});
+    } else {
+        const int n = std::min(units, want_stages);
+        for (int i = 0; i < n; ++i) plan_stages.push_back({i * units / n, (i + 1) * units / n, false, 0, M});
+    }
     cudaStream_t cs = (cudaStream_t)stream;
 
     std::vector<cudaEvent_t> events;
@@ -673,52 +703,74 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
         (e = record(cs, ss.down)) != cudaSuccess)
         return finish(cuda_fail(fn, e, "events"));
 
-    // Each distinct shard crosses the host link once; a replica is a device
-    // copy of the first rank's upload, on the replica stream after an event
-    // that follows the stage's uploads.
-    std::map<std::pair<int64_t, int64_t>, int> first_a, first_b, done_c;
+    // Each distinct shard (A: each row block of it) crosses the host link
+    // once; a replica is a device copy of the first rank's upload, on the
+    // replica stream after an event that follows the stage's uploads.
+    typedef std::pair<std::pair<int64_t, int64_t>, int64_t> Key;  // box offset, first row
+    std::map<Key, int> first_a, first_b, done_c;
     struct Replica {
         void *dst;
         const void *src;
         size_t bytes;
     };
     std::vector<Replica> replicas;
-    auto upload = [&](int r) -> cudaError_t {
+    // Rows [r0, r1) of box b, and where they start in its dense buffer.
+    auto rows_of = [](const shmm::Box &b, int64_t r0, int64_t r1) {
+        shmm::Box s = b;
+        s.off[0] += r0;
+        s.ext[0] = r1 - r0;
+        return s;
+    };
+    std::vector<char> b_done(p->nranks, 0);
+    auto upload = [&](int r, const Stage &stg) -> cudaError_t {
         struct Op {
             const void *host;
             int tensor;
             int64_t cols;
             void *const *dev;
-            std::map<std::pair<int64_t, int64_t>, int> *first;
-        } ops[2] = {{A_host, SHMM_TENSOR_A, p->J, A_r, &first_a}, {B_host, SHMM_TENSOR_B, p->K, B_r, &first_b}};
+            std::map<Key, int> *first;
+            bool whole;  // B: the whole box at its first use
+        } ops[2] = {{A_host, SHMM_TENSOR_A, p->J, A_r, &first_a, false},
+                    {B_host, SHMM_TENSOR_B, p->K, B_r, &first_b, true}};
         for (const Op &o : ops) {
-            const shmm::Box &b = p->boxes[o.tensor][r];
-            if (!o.host || b.numel() == 0) continue;
-            const auto key = std::make_pair(b.off[0], b.off[1]);
+            const shmm::Box &whole = p->boxes[o.tensor][r];
+            if (!o.host || whole.numel() == 0) continue;
+            if (o.whole) {
+                if (b_done[r]) continue;  // an earlier row block brought it
+                b_done[r] = 1;
+            }
+            const bool part = stg.block && !o.whole;
+            const int64_t q0 = part ? stg.r0 : 0, q1 = part ? stg.r1 : whole.ext[0];
+            const Key key(std::make_pair(whole.off[0], whole.off[1]), q0);
+            const shmm::Box b = rows_of(whole, q0, q1);
+            const size_t at = (size_t)(q0 * whole.ext[1] * in_b), bytes = (size_t)(b.numel() * in_b);
+            char *dst = static_cast<char *>(o.dev[r]) + at;
             const auto it = o.first->find(key);
             cudaError_t r2;
             if (it == o.first->end()) {
                 (*o.first)[key] = r;
-                r2 = upload_box(o.dev[r], o.host, b, o.cols, in_b, ss.up);
+                r2 = upload_box(dst, o.host, b, o.cols, in_b, ss.up);
             } else {
-                replicas.push_back({o.dev[r], o.dev[it->second], (size_t)(b.numel() * in_b)});
+                replicas.push_back({dst, static_cast<const char *>(o.dev[it->second]) + at, bytes});
                 r2 = cudaSuccess;
             }
             if (r2 != cudaSuccess) return r2;
         }
         return cudaSuccess;
     };
-    auto download = [&](int r) -> cudaError_t {
-        const shmm::Box &b = p->boxes[SHMM_TENSOR_C][r];
-        if (!C_host || b.numel() == 0) return cudaSuccess;
-        const auto key = std::make_pair(b.off[0], b.off[1]);
+    auto download = [&](int r, const Stage &stg) -> cudaError_t {
+        const shmm::Box &whole = p->boxes[SHMM_TENSOR_C][r];
+        if (!C_host || whole.numel() == 0) return cudaSuccess;
+        const int64_t r0 = stg.block ? stg.r0 : 0, r1 = stg.block ? stg.r1 : whole.ext[0];
+        const Key key(std::make_pair(whole.off[0], whole.off[1]), r0);
         if (done_c.count(key)) return cudaSuccess;  // a replica: written once
         done_c[key] = r;
-        return download_box(C_host, C_r[r], b, p->K, out_b, ss.down);
+        const char *src = static_cast<const char *>(C_r[r]) + (size_t)(r0 * whole.ext[1] * out_b);
+        return download_box(C_host, src, rows_of(whole, r0, r1), p->K, out_b, ss.down);
     };
 
-    for (int s = 0; s < stages; ++s) {
-        const int u0 = s * units / stages, u1 = (s + 1) * units / stages;
+    for (const Stage &stg : plan_stages) {
+        const int u0 = stg.u0, u1 = stg.u1;
         std::vector<int> ranks;
         if (!staged) {
             for (int r = 0; r < p->nranks; ++r) ranks.push_back(r);
@@ -730,7 +782,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
         }
         replicas.clear();
         for (int r : ranks)
-            if ((e = upload(r)) != cudaSuccess) return finish(cuda_fail(fn, e, "upload"));
+            if ((e = upload(r, stg)) != cudaSuccess) return finish(cuda_fail(fn, e, "upload"));
         if ((e = record(ss.up, cs)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
         if (!replicas.empty()) {
             if ((e = record(ss.up, ss.rep)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
@@ -741,8 +793,12 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
         }
         if (staged) {
             UnitPtrs up;
-            const shmm::GemmArgs ga = unit_args(p, (const void *const *)A_r, (const void *const *)B_r, C_r, u0,
-                                                u1, &up);
+            shmm::GemmArgs ga = unit_args(p, (const void *const *)A_r, (const void *const *)B_r, C_r, u0, u1, &up);
+            if (stg.block) {  // a block of rows: the same rows of every slot's A and C
+                ga.M = stg.r1 - stg.r0;
+                for (auto &a : up.a) a = static_cast<const char *>(a) + stg.r0 * Kd * in_b;
+                for (auto &o : up.out) o = static_cast<char *>(o) + stg.r0 * c_cols * out_b;
+            }
             const int ge = run_gemm(p, ga, status, stream, &err);
             if (ge) return finish(cuda_fail(fn, ge, err));
         } else {
@@ -755,7 +811,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
         }
         if ((e = record(cs, ss.down)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
         for (int r : ranks)
-            if ((e = download(r)) != cudaSuccess) return finish(cuda_fail(fn, e, "download"));
+            if ((e = download(r, stg)) != cudaSuccess) return finish(cuda_fail(fn, e, "download"));
     }
     return finish(SHMM_OK);
 }

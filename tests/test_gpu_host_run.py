@@ -26,6 +26,16 @@ PLANS = [
     ("case2_gather", XY22, ((), ("X",)), ((), ()), ((), ()), 384, 512, 264, "0", False),
     ("unfused_AR", Y2, ((), ("Y",)), (("Y",), ()), ((), ()), 256, 512, 320, "0", False),
     ("fused_then_replicate", XY22, ((), ("Y",)), (("Y",), ()), ((), ()), 256, 512, 320, "FUSED", True),
+    # Host operands of >= 32 MB run in one stage per 16 MB; with fewer units
+    # than that, each unit's stage splits into blocks of output rows.
+    # One reduction group, 84 MB: five row blocks of 1024, the last 4 rows.
+    ("row_blocks_fused_AR", Y2, ((), ("Y",)), (("Y",), ()), ((), ()), 4100, 8192, 1024, "FUSED", True),
+    # A replicated over both ranks, 53 MB: two blocks per rank, and rank 1's
+    # blocks are device copies of rank 0's
+    ("row_blocks_replicated_A", [("X", 2)], ((), ()), ((), ("X",)), ((), ("X",)), 6000, 4096, 512, "0", True),
+    # rank-order fold, reduce-scatter over columns, 57 MB: three row blocks
+    ("row_blocks_RS_cols_rank_order", Y2, ((), ("Y",)), (("Y",), ()), ((), ("Y",)), 3000, 8192, 512,
+     "FUSED|RANK_ORDER", True),
 ]
 
 
