@@ -368,12 +368,41 @@ cudaError_t reduce_dispatch_idx(const ReduceK &k, bool vec_ok, bool tree, bool g
 }
 
 // All-gather: one read of each source vector, G writes; group g = blockIdx.y.
+// 16-byte vectors: four loads per thread issued before their stores (one
+// load in flight per thread left the gather at 0.88 of the copy rate).
 template <bool VEC16, typename IT>
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherK k, int elem) {
     const int g = blockIdx.y;
     const IT total = (IT)k.nvec;
     const IT bvecs = (IT)k.bvecs, brows = (IT)k.brows, per_block = brows * bvecs;
     const IT full_vecs = (IT)k.full_vecs;
+    if constexpr (VEC16) {
+        // four independent loads per thread in flight before the stores
+        constexpr int U = 4;
+        for (IT base = (IT)blockIdx.x * blockDim.x * U + threadIdx.x; base < total;
+             base += (IT)gridDim.x * blockDim.x * U) {
+            uint4 x[U];
+            IT dst_off[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const IT v = base + (IT)u * blockDim.x;
+                if (v >= total) continue;
+                const int p = (int)(v / per_block);
+                const IT w = v - (IT)p * per_block;
+                const IT r = w / bvecs, c = w - r * bvecs;
+                const int p0 = p / k.blocks1, p1 = p - p0 * k.blocks1;
+                dst_off[u] = ((IT)p0 * brows + r) * full_vecs + (IT)p1 * bvecs + c;
+                x[u] = __ldcs(reinterpret_cast<const uint4 *>(k.src[g * k.G + p]) + w);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const IT v = base + (IT)u * blockDim.x;
+                if (v >= total) continue;
+                for (int m = 0; m < k.G; ++m) __stcs(reinterpret_cast<uint4 *>(k.dst[g * k.G + m]) + dst_off[u], x[u]);
+            }
+        }
+        return;
+    }
     for (IT v = (IT)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (IT)gridDim.x * blockDim.x) {
         const int p = (int)(v / per_block);
         const IT w = v - (IT)p * per_block;
@@ -381,10 +410,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
         const int p0 = p / k.blocks1, p1 = p - p0 * k.blocks1;
         const IT src_off = w;
         const IT dst_off = ((IT)p0 * brows + r) * full_vecs + (IT)p1 * bvecs + c;
-        if (VEC16) {
-            const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(k.src[g * k.G + p]) + src_off);
-            for (int m = 0; m < k.G; ++m) __stcs(reinterpret_cast<uint4 *>(k.dst[g * k.G + m]) + dst_off, x);
-        } else if (elem == 4) {  // element-wise: "vectors" are single elements
+        if (elem == 4) {  // element-wise: "vectors" are single elements
             const uint32_t x = reinterpret_cast<const uint32_t *>(k.src[g * k.G + p])[src_off];
             for (int m = 0; m < k.G; ++m) reinterpret_cast<uint32_t *>(k.dst[g * k.G + m])[dst_off] = x;
         } else {
@@ -651,7 +677,7 @@ int launch_gather(const GatherArgs &a, int *status, void *stream) {
     k.full_vecs = (int64_t)a.blocks1 * k.bvecs;
     k.nvec = (int64_t)a.G * a.brows * k.bvecs;
     cudaStream_t s = (cudaStream_t)stream;
-    const dim3 grid = grid_for(k.nvec, 256 * 2, k.ngroups);
+    const dim3 grid = grid_for(k.nvec, vec ? 256 * 4 : 256, k.ngroups);
     const int elem = (int)a.elem;
     const bool small = k.nvec < ((int64_t)1 << 32) - 64 &&
                        (int64_t)a.blocks0 * a.brows * k.full_vecs < ((int64_t)1 << 32) - 64;
