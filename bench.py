@@ -489,23 +489,124 @@ def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False):
 
 # --------------------------------------------------------------- oracle
 
+def _spread(n, k):
+    """k row indices spread evenly over [0, n) (all rows when k >= n)."""
+    if k >= n:
+        return list(range(n))
+    return sorted({int(i * n / k) for i in range(k)})
+
+
+def _oracle_matmul(mesh, sA, sB, sC, A, B, out_dtype, rows, nthreads, gelu=False):
+    """The oracle on sampled output rows; returns (per-rank result, FLOPs the
+    sample took: each rank's local product over its sampled rows)."""
+    import numpy as np
+    import oracle
+    _, res = oracle.sharded_matmul(mesh, sA, sB, sC, A, B, out_dtype=out_dtype, gelu=gelu, rows=rows,
+                                   nthreads=nthreads)
+    plan = oracle.plan_matmul(mesh, sA, sB, sC)
+    I, J = A.shape
+    K = B.shape[1]
+    row_set = None if rows is None else np.asarray(sorted(set(rows)), np.int64)
+    fl = 0
+    for r in range(oracle.mesh_size(mesh)):
+        (ai0, _), (ain, ajn) = oracle.shard_box(mesh, plan.local_A, (I, J), r)
+        (_, _), (_, bkn) = oracle.shard_box(mesh, plan.local_B, (J, K), r)
+        nr = ain if row_set is None else int(((row_set >= ai0) & (row_set < ai0 + ain)).sum())
+        fl += 2 * nr * ajn * bkn
+    return res, fl
+
+
 def oracle_sample_step(cfg_name, rows_per_rank, nthreads, host_globals):
-    """One bounded sample of the workload computed by the CPU oracle:
+    """One bounded sample of the workload computed by the CPU oracle: about
     ``rows_per_rank`` output rows of every rank's block (local products,
-    rank-order sum, rounding, ownership).  Returns the sample's FLOPs."""
+    rank-order sum, rounding, ownership); the integer split-K case whole.
+    Returns the sample's FLOPs."""
     import numpy as np
     import oracle
     c = WORKLOADS[cfg_name]
     if cfg_name in ("down_projection", "down_projection_quarter"):
         A, B = host_globals
-        mesh, sA, sB, sC = c["mesh"], c["sA"], c["sB"], c["sC"]
-        xs = dict(mesh)["X"]
+        xs = dict(c["mesh"])["X"]
         blk = c["I"] // xs
         rows = sorted({x * blk + int(i * blk / rows_per_rank) for x in range(xs) for i in range(rows_per_rank)})
-        oracle.sharded_matmul(mesh, sA, sB, sC, A, B, out_dtype="bf16", rows=rows, nthreads=nthreads)
-        nr = len(rows) // xs  # rows per X block; each is formed by the 2 Y ranks
-        return 2 * nr * (c["J"] // 2) * c["K"] * oracle.mesh_size(mesh)
+        return _oracle_matmul(c["mesh"], c["sA"], c["sB"], c["sC"], A, B, "bf16", rows, nthreads)[1]
+    if cfg_name == "split_k_integer":
+        A, B = host_globals
+        return _oracle_matmul(c["mesh"], ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, "f32", None, nthreads)[1]
+    if cfg_name == "four_case":
+        A, B = host_globals
+        rows = _spread(c["I"], 4 * rows_per_rank)
+        return sum(_oracle_matmul(c["mesh"], sA, sB, sC, A, B, "bf16", rows, nthreads)[1]
+                   for sA, sB, sC in FOUR_CASES)
+    if cfg_name in ("mlp_pair", "mlp_pair_sp"):
+        # sampled tokens through both matmuls: H rows for those tokens, then
+        # the second matmul (and for the sequence-parallel block its
+        # reduce-scatter and LayerNorm) on them
+        X, W1, W2 = host_globals
+        mesh, T, D, F = c["mesh"], c["T"], c["D"], c["F"]
+        n = oracle.mesh_size(mesh)
+        t = _spread(T, max(n, (rows_per_rank * n) // n * n))
+        t = t[:len(t) // n * n]
+        res1, fl1 = _oracle_matmul(mesh, ((), ()), ((), ("X",)), ((), ("X",)), X, W1, "bf16", t, nthreads,
+                                   gelu=True)
+        H = np.zeros((len(t), F), np.float32)
+        for r, (grows, k0, arr) in res1.items():
+            H[:, k0:k0 + arr.shape[1]] = arr
+        sC = (("X",), ()) if cfg_name == "mlp_pair_sp" else ((), ())
+        res2, fl2 = _oracle_matmul(mesh, ((), ("X",)), (("X",), ()), sC, H, W2, "bf16", None, nthreads)
+        if cfg_name == "mlp_pair_sp":
+            for r, (off, y) in res2.items():
+                oracle.layernorm(y, np.ones(D), np.zeros(D), 1e-5, out_dtype="bf16")
+        return fl1 + fl2
     raise ValueError("no oracle sample for %s" % cfg_name)
+
+
+def sample_text(cfg_name, rows, sample_flops, step_flops):
+    if cfg_name == "split_k_integer":
+        return "the whole step (%.3g MFLOP)" % (step_flops / 1e6)
+    return ("about %d output rows of each rank's block (%.3g GFLOP of the step's %.4g GFLOP)"
+            % (rows, sample_flops / 1e9, step_flops / 1e9))
+
+
+def reference_host_globals(cfg_name):
+    """The workload's global inputs as fp32 numpy arrays (the GPU arm's seeds)."""
+    import shmm_inputs
+    c = WORKLOADS[cfg_name]
+    if cfg_name in ("mlp_pair", "mlp_pair_sp"):
+        g = shmm_inputs.mlp_pair(c["T"], c["D"], c["F"], seed=0)
+    elif cfg_name == "split_k_integer":
+        g = shmm_inputs.split_k_integer(c["I"], c["J"], c["K"], seed=0)
+    else:
+        g = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
+    return tuple(t.float().numpy() for t in g)
+
+
+def full_step_flops(cfg_name):
+    """FLOPs of one whole step of the workload, as the GPU arm counts them."""
+    import oracle
+    c = WORKLOADS[cfg_name]
+    if cfg_name in ("mlp_pair", "mlp_pair_sp"):
+        return 4.0 * c["T"] * c["D"] * c["F"]
+    if cfg_name == "four_case":
+        return float(oracle.mesh_size(c["mesh"]) *
+                     sum(oracle.local_flops(c["mesh"], sA, sB, c["I"], c["J"], c["K"]) for sA, sB, _ in FOUR_CASES))
+    return 2.0 * c["I"] * c["J"] * c["K"]
+
+
+def oracle_reduce_scatter_gbs(nthreads, G=8, mib=16):
+    """The oracle's reduce-scatter (ascending-rank fp32 sum, owner blocks) on
+    G fp32 partial buffers of ``mib`` MiB, in GB/s by the GPU arm's byte
+    count (G reads of V plus V written)."""
+    import numpy as np
+    import oracle
+    n = mib * (1 << 20) // 4
+    rng = np.random.default_rng(0)
+    parts = [rng.uniform(-1, 1, (n // 4096, 4096)).astype(np.float32) for _ in range(G)]
+    t0 = time.time()
+    oracle.collective_reduce(parts, "reduce_scatter", "f32")
+    dt = time.time() - t0
+    return {"value": (G + 1) * n * 4 / dt / 1e9, "unit": "GB/s",
+            "sample": "%d fp32 partials of %d MiB, reduce-scatter over rows" % (G, mib)}
 
 
 def host_globals_f32(wl):
@@ -515,16 +616,15 @@ def host_globals_f32(wl):
 def cpu_baseline(cfg_name, host_globals, target_s=12.0):
     nthreads = len(os.sched_getaffinity(0))
     t0 = time.time()
-    fl = oracle_sample_step(cfg_name, 8, nthreads, host_globals)
+    oracle_sample_step(cfg_name, 8, nthreads, host_globals)
     dt = time.time() - t0
     rows = max(8, min(1024, int(8 * target_s / max(dt, 1e-3))))
     t0 = time.time()
     fl = oracle_sample_step(cfg_name, rows, nthreads, host_globals)
     dt = time.time() - t0
-    c = WORKLOADS[cfg_name]
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-            "sample": "%d output rows of each of the 8 ranks' blocks (%.1f GFLOP of the step's %.0f), "
-                      "%.1f s" % (rows, fl / 1e9, 2.0 * c["I"] * c["J"] * c["K"] / 1e9, dt)}
+            "sample": "%s, %.1f s" % (sample_text(cfg_name, rows, fl, full_step_flops(cfg_name)), dt),
+            "reduce_scatter": oracle_reduce_scatter_gbs(nthreads)}
 
 
 # ---------------------------------------------------------- distributed
@@ -569,11 +669,9 @@ def run_reference(args, dist_ctx):
     """The oracle on the host cores as the reference arm."""
     if dist_ctx.rank != 0:
         return None
-    import shmm_inputs
     name = args.workload
     c = WORKLOADS[name]
-    A, B = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
-    hg = (A.float().numpy(), B.float().numpy())
+    hg = reference_host_globals(name)
     nthreads = len(os.sched_getaffinity(0))
     budget = args.reference_budget_s / max(1, args.steps + args.warmup)
     t0 = time.time()
@@ -588,15 +686,14 @@ def run_reference(args, dist_ctx):
         fl += oracle_sample_step(name, rows, nthreads, hg)
     dt = time.time() - t0
     value = fl / dt / 1e12
-    step_gflop = 2.0 * c["I"] * c["J"] * c["K"] / 1e9
-    sample = ("%d output rows of each rank's block per step (%.2f GFLOP of the step's %.0f GFLOP)"
-              % (rows, fl / args.steps / 1e9, step_gflop))
+    sample = sample_text(name, rows, fl / args.steps, full_step_flops(name)) + " per step"
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate",
             "data": "synthetic", "config": {"workload": c["text"], "sample": sample},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
                              "sample": sample},
+            "reduce_scatter": oracle_reduce_scatter_gbs(nthreads),
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -662,7 +759,7 @@ def run_shmm(args, dist_ctx):
                            "peak_nominal": NOMINAL_PEAKS["hbm_gbs"],
                            "frac_of_nominal": rs["GB_s"] / NOMINAL_PEAKS["hbm_gbs"]},
     }
-    if dist_ctx.rank == 0 and N == 1 and not args.no_cpu_baseline and args.workload == "down_projection":
+    if dist_ctx.rank == 0 and N == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.workload, host_globals_f32(wl))
     return out
 
