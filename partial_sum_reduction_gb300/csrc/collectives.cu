@@ -401,21 +401,21 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
                 for (int m = 0; m < k.G; ++m) __stcs(reinterpret_cast<uint4 *>(k.dst[g * k.G + m]) + dst_off[u], x[u]);
             }
         }
-        return;
-    }
-    for (IT v = (IT)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (IT)gridDim.x * blockDim.x) {
-        const int p = (int)(v / per_block);
-        const IT w = v - (IT)p * per_block;
-        const IT r = w / bvecs, c = w - r * bvecs;
-        const int p0 = p / k.blocks1, p1 = p - p0 * k.blocks1;
-        const IT src_off = w;
-        const IT dst_off = ((IT)p0 * brows + r) * full_vecs + (IT)p1 * bvecs + c;
-        if (elem == 4) {  // element-wise: "vectors" are single elements
-            const uint32_t x = reinterpret_cast<const uint32_t *>(k.src[g * k.G + p])[src_off];
-            for (int m = 0; m < k.G; ++m) reinterpret_cast<uint32_t *>(k.dst[g * k.G + m])[dst_off] = x;
-        } else {
-            const uint16_t x = reinterpret_cast<const uint16_t *>(k.src[g * k.G + p])[src_off];
-            for (int m = 0; m < k.G; ++m) reinterpret_cast<uint16_t *>(k.dst[g * k.G + m])[dst_off] = x;
+    } else {
+        for (IT v = (IT)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (IT)gridDim.x * blockDim.x) {
+            const int p = (int)(v / per_block);
+            const IT w = v - (IT)p * per_block;
+            const IT r = w / bvecs, c = w - r * bvecs;
+            const int p0 = p / k.blocks1, p1 = p - p0 * k.blocks1;
+            const IT src_off = w;
+            const IT dst_off = ((IT)p0 * brows + r) * full_vecs + (IT)p1 * bvecs + c;
+            if (elem == 4) {  // element-wise: "vectors" are single elements
+                const uint32_t x = reinterpret_cast<const uint32_t *>(k.src[g * k.G + p])[src_off];
+                for (int m = 0; m < k.G; ++m) reinterpret_cast<uint32_t *>(k.dst[g * k.G + m])[dst_off] = x;
+            } else {
+                const uint16_t x = reinterpret_cast<const uint16_t *>(k.src[g * k.G + p])[src_off];
+                for (int m = 0; m < k.G; ++m) reinterpret_cast<uint16_t *>(k.dst[g * k.G + m])[dst_off] = x;
+            }
         }
     }
 }
