@@ -1131,12 +1131,12 @@ cudaError_t launch_pair(TcK &k, cudaStream_t s) {
         int n = 0;
         e = cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &q);
         if (e != cudaSuccess) return e;
-        if (n < 1) return cudaErrorNotSupported;
         if (!cache) return cudaErrorInvalidDevice;
-        max_pairs[dev] = n;
+        max_pairs[dev] = n < 0 ? 0 : n;
         attr_set[dev] = true;
     }
     const int cap = max_pairs[dev];
+    if (cap < 1) return cudaErrorNotSupported;  // no pair can be resident: the caller falls back
     k.m_tiles = (int)((k.M + 255) / 256);
     k.n_tiles = (int)((k.N + 255) / 256);
     const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
@@ -1275,7 +1275,13 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         k.m_tiles = (int)((a.M + BM - 1) / BM);
         k.k_blocks = (int)((a.Kd + BK - 1) / BK);
         // 256-row tiles on CTA pairs unless the local M fits one 128-row tile
-        const cudaError_t e = (a.M > BM && pair_kernel_enabled()) ? launch_pair(k, s) : launch_bn<bn>(k, s);
+        cudaError_t e = cudaErrorNotSupported;
+        if (a.M > BM && pair_kernel_enabled()) e = launch_pair(k, s);
+        if (e == cudaErrorNotSupported) {
+            // single-CTA tiles when no CTA pair fits (or is wanted)
+            k.m_tiles = (int)((a.M + BM - 1) / BM);
+            e = launch_bn<bn>(k, s);
+        }
         if (e != cudaSuccess) return (int)e;
     }
     return 0;
