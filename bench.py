@@ -244,6 +244,20 @@ class Workload:
         return p
 
     def step(self, stream):
+        if self.name == "four_case":
+            # four independent sharded matmuls: forked onto their own streams
+            # so one case's last partial wave overlaps the next case's work
+            torch = self.torch
+            if not hasattr(self, "side"):
+                self.side = [torch.cuda.Stream() for _ in self.steps_spec[1:]]
+            for st in self.side:
+                st.wait_stream(stream)
+            for i, (p, A_r, B_r, C_r, ws) in enumerate(self.steps_spec):
+                st = stream if i == 0 else self.side[i - 1]
+                p.run(A_r, B_r, C_r, ws, stream=st)
+            for st in self.side:
+                stream.wait_stream(st)
+            return
         for p, A_r, B_r, C_r, ws in self.steps_spec:
             p.run(A_r, B_r, C_r, ws, stream=stream)
         if self.name == "mlp_pair_sp":
