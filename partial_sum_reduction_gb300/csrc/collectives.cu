@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(256) ln_gather_reg_kernel(const __grid_constan
 
 // ---- reshard: rectangles between rank buffers ------------------------------
 
-constexpr int kMaxRects = 128;
+constexpr int kMaxRects = 256;  // one launch for a 16-rank all-to-all (16 x 16 rectangles)
 
 struct CopyK {
     shmm::CopyRect r[kMaxRects];
