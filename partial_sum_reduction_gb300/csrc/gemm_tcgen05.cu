@@ -438,6 +438,92 @@ __device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, i
     }
 }
 
+// Epilogue of one warp (warps 2..5) over the tiles its CTA (or CTA pair)
+// owns: work items first, first + stride, ... < total; output rows
+// mt * tile_rows + row_base + [0, 32) of each tile, TMEM lanes from
+// lane_base.  Tile i's sum S sits in TMEM buffer i % 2.  In rank order the
+// group's later products arrive in the other buffer W and are folded into S
+// (fp32, ascending rank order), W handed back after each; accumulating, S
+// already holds the sum.  Then GeLU if asked, one rounding and the stores
+// (bulk tensor stores through the staging buffers at cbuf, or per thread),
+// and S is handed back.  full_bar(b): the barrier on which the MMA thread
+// reports a finished product in buffer b; release(b): hands buffer b back.
+template <typename FullBar, typename Release>
+__device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride, int total, int Gq, int tile_rows,
+                                            int row_base, uint32_t lane_base, uint32_t cbuf, int lane,
+                                            volatile int *abort_flag, FullBar full_bar, Release release) {
+    constexpr int BN = 256;
+    const bool f32 = k.out_f32 != 0;
+    const int64_t es = f32 ? 4 : 2;
+    uint32_t staged = 0;
+    uint32_t used0 = 0, used1 = 0;  // finished products consumed per buffer
+    // One lane waits; the warp reconverges before the .sync.aligned TMEM
+    // instructions.
+    auto warp_wait_full = [&](int b) -> bool {
+        const uint32_t n = b ? used1 : used0;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(full_bar(b), n & 1, abort_flag, k.status) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (b) ++used1;
+        else ++used0;
+        if (ok) fence_after();
+        return ok != 0;
+    };
+    int tile_iter = 0;
+    for (int t = first; t < total; t += stride, ++tile_iter) {
+        int unit, mt, nt;
+        tile_coords(k, t, &unit, &mt, &nt);
+        const int bS = tile_iter & 1, bW = bS ^ 1;
+        const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
+        const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
+        if (!warp_wait_full(bS)) break;  // S = product of the group's first rank
+        bool ok = true;
+        const int folds = k.accum ? 1 : Gq;  // accum: S already holds the sum
+        for (int q = 1; q < folds; ++q) {
+            // S = S + P_q in fp32: the ascending-rank sequential sum
+            if (!warp_wait_full(bW)) {
+                ok = false;
+                break;
+            }
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float a[32], w[32];
+                tmem_ld32(s_base + (uint32_t)(c * 32), a);
+                tmem_ld32(w_base + (uint32_t)(c * 32), w);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[i] = a[i] + w[i];
+                tmem_st32(s_base + (uint32_t)(c * 32), a);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            release(bW);  // W may take the next product
+        }
+        if (!ok) break;
+        const int row0 = mt * tile_rows + row_base;
+        if (k.tma_store) {
+            if (row0 < k.M) store_tile_tma(k, unit, Gq, row0, nt, s_base, cbuf, &staged, lane);
+        } else {
+            const int64_t row = (int64_t)row0 + lane;
+            const bool row_ok = row < k.M;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                tmem_ld32(s_base + (uint32_t)(c * 32), v);
+                if (k.gelu) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                }
+                const int64_t col0 = (int64_t)nt * BN + c * 32;
+                if (!row_ok || col0 >= k.N) continue;
+                const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
+                store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
+            }
+        }
+        release(bS);  // S may take the next tile's products
+    }
+    if (lane == 0) bulk_wait_all();  // no store still reads staging at exit
+    __syncwarp();
+}
+
 template <int BN>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;           // 16 KB
@@ -624,80 +710,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int quad = warp % 4;
-        const int row_in_tile = quad * 32 + lane;
-        const bool f32 = k.out_f32 != 0;
-        const int64_t es = f32 ? 4 : 2;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-        const uint32_t cbuf = smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes);
-        uint32_t staged = 0;
-        uint32_t used0 = 0, used1 = 0;  // finished products consumed per buffer
-        // One lane waits; the warp reconverges before the .sync.aligned TMEM
-        // instructions.
-        auto warp_wait_full = [&](int b) -> bool {
-            const uint32_t n = b ? used1 : used0;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(accf_bar(b), n & 1, abort_flag, k.status) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (b) ++used1;
-            else ++used0;
-            if (ok) fence_after();
-            return ok != 0;
-        };
-        int tile_iter = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_iter) {
-            int unit, mt, nt;
-            decode(t, &unit, &mt, &nt);
-            const int bS = tile_iter & 1, bW = bS ^ 1;
-            const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
-            const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
-            if (!warp_wait_full(bS)) break;  // S = product of the group's first rank
-            bool ok = true;
-            const int folds = k.accum ? 1 : Gq;  // accum: S already holds the sum
-            for (int q = 1; q < folds; ++q) {
-                // S = S + P_q in fp32: the ascending-rank sequential sum
-                if (!warp_wait_full(bW)) {
-                    ok = false;
-                    break;
-                }
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float a[32], w[32];
-                    tmem_ld32(s_base + (uint32_t)(c * 32), a);
-                    tmem_ld32(w_base + (uint32_t)(c * 32), w);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) a[i] = a[i] + w[i];
-                    tmem_st32(s_base + (uint32_t)(c * 32), a);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                fence_before();
-                mbar_arrive(acce_bar(bW));  // W may take the next product
-            }
-            if (!ok) break;
-            if (k.tma_store) {
-                const int row0 = mt * BM + quad * 32;
-                if (row0 < k.M) store_tile_tma(k, unit, Gq, row0, nt, s_base, cbuf, &staged, lane);
-            } else {
-                const int64_t row = (int64_t)mt * BM + row_in_tile;
-                const bool row_ok = row < k.M;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(s_base + (uint32_t)(c * 32), v);
-                    if (k.gelu) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
-                    }
-                    const int64_t col0 = (int64_t)nt * BN + c * 32;
-                    if (!row_ok || col0 >= k.N) continue;
-                    const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
-                    store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
-                }
-            }
-            fence_before();
-            mbar_arrive(acce_bar(bS));  // S may take the next tile's products
-        }
-        if (lane == 0) bulk_wait_all();  // no store still reads staging at exit
-        __syncwarp();
+        drain_tiles(k, blockIdx.x, gridDim.x, total, Gq, BM, quad * 32, tmem_base + ((uint32_t)(quad * 32) << 16),
+                    smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes), lane, abort_flag,
+                    [&](int b) { return accf_bar(b); },
+                    [&](int b) {
+                        fence_before();
+                        mbar_arrive(acce_bar(b));
+                    });
     }
 
     fence_before();
@@ -908,79 +927,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
     } else {
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
         const int quad = warp % 4;
-        const int row_in_tile = (int)cr * BM + quad * 32 + lane;
-        const bool f32 = k.out_f32 != 0;
-        const int64_t es = f32 ? 4 : 2;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-        const uint32_t cbuf = smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes);
-        uint32_t staged = 0;
-        uint32_t used0 = 0, used1 = 0;
-        auto warp_wait_full = [&](int b) -> bool {
-            const uint32_t n = b ? used1 : used0;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(accf_bar(b), n & 1, abort_flag, k.status) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (b) ++used1;
-            else ++used0;
-            if (ok) fence_after();
-            return ok != 0;
-        };
-        auto release = [&](int b) {
-            fence_before();
-            mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));  // the leader's barrier
-        };
-        int tile_iter = 0;
-        for (int t = pair; t < total; t += npairs, ++tile_iter) {
-            int unit, mt, nt;
-            decode(t, &unit, &mt, &nt);
-            const int bS = tile_iter & 1, bW = bS ^ 1;
-            const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
-            const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
-            if (!warp_wait_full(bS)) break;
-            bool ok = true;
-            const int folds = k.accum ? 1 : Gq;  // accum: S already holds the sum
-            for (int q = 1; q < folds; ++q) {
-                if (!warp_wait_full(bW)) {
-                    ok = false;
-                    break;
-                }
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float a[32], w[32];
-                    tmem_ld32(s_base + (uint32_t)(c * 32), a);
-                    tmem_ld32(w_base + (uint32_t)(c * 32), w);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) a[i] = a[i] + w[i];
-                    tmem_st32(s_base + (uint32_t)(c * 32), a);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                release(bW);
-            }
-            if (!ok) break;
-            if (k.tma_store) {
-                const int row0 = mt * 256 + (int)cr * BM + quad * 32;
-                if (row0 < k.M) store_tile_tma(k, unit, Gq, row0, nt, s_base, cbuf, &staged, lane);
-            } else {
-                const int64_t row = (int64_t)mt * 256 + row_in_tile;
-                const bool row_ok = row < k.M;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(s_base + (uint32_t)(c * 32), v);
-                    if (k.gelu) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
-                    }
-                    const int64_t col0 = (int64_t)nt * BN + c * 32;
-                    if (!row_ok || col0 >= k.N) continue;
-                    const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
-                    store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
-                }
-            }
-            release(bS);
-        }
-        if (lane == 0) bulk_wait_all();  // no store still reads staging at exit
-        __syncwarp();
+        drain_tiles(k, pair, npairs, total, Gq, 256, (int)cr * BM + quad * 32,
+                    tmem_base + ((uint32_t)(quad * 32) << 16),
+                    smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes), lane, abort_flag,
+                    [&](int b) { return accf_bar(b); },
+                    [&](int b) {
+                        fence_before();
+                        mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));  // the leader's barrier
+                    });
     }
 
     fence_before();
