@@ -225,13 +225,14 @@ def test_mlp_pair_full_size_sampled(s, sY):
 
 # -------------------------------------------- collectives on given partials
 
-@pytest.mark.parametrize("G", [2, 3, 4, 5, 8, 12, 16])
+@pytest.mark.parametrize("G", [2, 3, 4, 5, 8, 12, 16, 24, 32])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("order", ["sequential", "pairwise"])
 @pytest.mark.parametrize("numel", [1 << 16, 4099 * 8])
 def test_collectives_bit_exact(s, G, dtype, order, numel):
     """Reduce-scatter, all-reduce and all-gather of given partial buffers
-    ({X:G}), bit for bit against the oracle in the same order."""
+    ({X:G}), bit for bit against the oracle in the same order.  G = 24 and
+    32 take the runtime-G sequential kernel and the 32-lane shuffle tree."""
     from partial_sum_reduction_gb300 import helpers as H
     cols = 64 if numel % (64 * G) == 0 else 8
     rows = numel // cols
