@@ -71,9 +71,10 @@ FOUR_CASES = [
 
 
 # DRAM bytes per launch of the dominant kernel from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum, one pass, full-size launch;
-# profiles/gemm_tc2_fused_down_projection_quarter.md gives the command), valid
-# only for the kernel source it was taken on.
+# (dram__bytes_read.sum + dram__bytes_write.sum, one pass, full-size launch:
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+#       -k regex:gemm_tc2 -s 3 -c 1 python bench.py --steps 5 --warmup 3 --no-cpu-baseline),
+# valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
     "down_projection": {"kernel_sha256_16": "70e21457086fa367", "bytes": 4.313467648e9 + 0.262102784e9,
                         "kernel": "gemm_tc2_kernel"},

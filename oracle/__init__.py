@@ -28,8 +28,12 @@ axes with the first axis major; a sharding gives, per array dim, the tuple
 of mesh axes that split it (several axes flatten with the first listed
 major, as in I_XY).
 
-Readings of points the pages leave open are listed in the design doc.  Every
-function below is pinned by ``tests/test_oracle_pins.py``.
+Where the pages leave a step open, the oracle reads it plainly: a
+reduce-scatter splits the dim the requested C sharding extends (rows in the
+worked example); a replicated operand is one buffer per rank; every rank
+computes its own product; partials are fp32 and are added in ascending rank
+order; GeLU is the tanh form; uneven shards are rejected.  Every function
+below is pinned by ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
 
