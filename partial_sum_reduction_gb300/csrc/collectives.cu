@@ -350,7 +350,15 @@ cudaError_t reduce_dispatch(const ReduceK &k, bool vec_ok, bool tree, bool gelu,
     if (tree && (k.G == 2 || k.G == 4 || k.G == 8 || k.G == 16)) {
         // power-of-two groups fit in registers: pairwise tree per thread
         switch (k.G) {
-            case 2: reduce_seq_kernel<PT, OT, 2, 4, IT, true><<<grid_for(k.nvec, 256 * 4, k.ngroups), 256, 0, s>>>(k, gelu); break;
+            case 2: {  // as the sequential two-rank case below
+                constexpr int U2 = sizeof(PT) == 2 ? 2 : 4;
+                auto kern = reduce_seq_kernel<PT, OT, 2, U2, IT, true>;
+                const bool resident = sizeof(PT) == 2 || k.mode != 2;
+                const dim3 grid = resident ? grid_resident(kern, k.nvec, 256 * U2, k.ngroups)
+                                           : grid_for(k.nvec, 256 * U2, k.ngroups);
+                kern<<<grid, 256, 0, s>>>(k, gelu);
+                break;
+            }
             case 4: reduce_seq_kernel<PT, OT, 4, 2, IT, true><<<grid_for(k.nvec, 256 * 2, k.ngroups), 256, 0, s>>>(k, gelu); break;
             case 8: reduce_seq_kernel<PT, OT, 8, 1, IT, true><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
             default: reduce_seq_kernel<PT, OT, 16, 1, IT, true><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
