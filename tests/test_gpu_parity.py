@@ -588,3 +588,21 @@ def test_sequence_parallel_mlp_block(s, fused):
     for y in Y_n:
         got = y.float().cpu().numpy()
         assert np.abs(got - ref).max() <= BF16_TOL * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("mesh,sA,sB,sC,I,J,K", [
+    (Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), 300, 2000, 264),          # J_r = 1000 = 15 k-blocks + 40
+    (XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ()), 1040, 1808, 520),  # J_r = 904, M_r = 260
+])
+def test_ragged_contraction(s, pair, fused, mesh, sA, sB, sC, I, J, K, monkeypatch):
+    """Per-rank contraction lengths that are not a multiple of the 64-wide
+    k-block (the last block is zero-filled by TMA), with ragged M and N, on
+    both GEMM kernels, fused and unfused, against the oracle."""
+    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=I + K)
+    plan, gpu = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED if fused else 0)
+    assert plan.info.tensor_core == 1
+    _, ores = oracle_run(mesh, sA, sB, sC, A, B, "f32")
+    compare(plan, gpu, ores, exact=False, tol=F32P_TOL)
