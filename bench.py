@@ -733,7 +733,12 @@ def run_shmm(args, dist_ctx):
     # one fused GEMM launch, so the per-step event time is its duration
     launch_ms = statistics.mean(per_step)
     achieved = wl.flops / (launch_ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]
+    # The measured burst rate is the denominator for a kernel timed alone; a
+    # kernel timed in a long back-to-back loop that ran under the power cap
+    # (sw_power_cap during the timed region) is in the regime of the
+    # measured sustained rate.  Both fractions are reported.
+    power_capped = "sw_power_cap" in (clocks or {}).get("reasons", [])
+    peak = peaks["bf16_tflops_sustained"] if power_capped else peaks["bf16_tflops"]
     e2e_steps = max(3, min(10, args.steps // 10))
     e2e_ms, h2d, d2h = time_e2e(wl, e2e_steps, dist_ctx)
     e2e_value = wl.flops * N / (e2e_ms * 1e-3) / 1e12
@@ -752,7 +757,10 @@ def run_shmm(args, dist_ctx):
                      "traffic_unit": "DRAM bytes per launch (ncu)",
                      "algorithmic_bytes": wl.input_bytes() + sum(t.numel() * t.element_size()
                                                                  for t in wl.output_tensors()),
-                     "peak_kind": "%s bf16 burst (cuBLAS 8192^3)" % peak_kind,
+                     "peak_kind": ("%s bf16 sustained (cuBLAS 8192^3 back to back): the timed loop ran under "
+                                   "the power cap" % peak_kind if power_capped
+                                   else "%s bf16 burst (cuBLAS 8192^3)" % peak_kind),
+                     "frac_of_burst": achieved / peaks["bf16_tflops"],
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "peak_nominal": NOMINAL_PEAKS["bf16_tflops"],
                      "frac_of_nominal": achieved / NOMINAL_PEAKS["bf16_tflops"],
