@@ -180,7 +180,7 @@ typedef struct {
     int in_dtype, out_dtype, partial_dtype;
     uint32_t flags;
     int tensor_core;       /* 1 if the local GEMM runs on tcgen05 */
-    int fused;             /* 1 if shmm_run reduces in the GEMM epilogue
+    int fused;             /* 1 if shmm_run reduces inside the GEMM
                               (SHMM_FLAG_FUSED honoured: on tensor cores, at
                               most 16 ranks per group; otherwise shmm_run
                               reduces with the standalone kernel) */
@@ -283,7 +283,7 @@ shmm_status_t shmm_all_gather(const shmm_plan_t *plan, int tensor, const void *c
                               void *const *full_r, void *stream);
 
 /* The whole sharded matmul: operand all-gathers (cases 2, 4), local GEMMs,
- * the reduction (fused into the GEMM epilogue with SHMM_FLAG_FUSED, else a
+ * the reduction (fused into the GEMM with SHMM_FLAG_FUSED, else a
  * standalone kernel over fp32 partials in the workspace) and the result
  * all-gather the requested ownership needs.
  *   A_r[N], B_r[N]  in: boxes SHMM_TENSOR_A / SHMM_TENSOR_B
@@ -315,10 +315,11 @@ shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const vo
  * Results are bit for bit those of uploading the shards and calling
  * shmm_run.  When every unit of work reads only its own ranks' shards (no
  * operand or result all-gather; a reduction only if fused), the work runs
- * in up to 16 stages (reduction groups or ranks, each split into blocks of
- * 256-row multiples when there are few of them and a block of C rows needs
- * only the same rows of A): a stage's uploads overlap the previous stage's
- * GEMM and its downloads overlap the next.
+ * in stages, at most one per 16 MB of host operands and at most 16:
+ * reduction groups or ranks, each split into blocks of 256-row multiples
+ * when there are fewer units than stages and a block of C rows needs only
+ * the same rows of A.  A stage's uploads overlap the previous stage's GEMM
+ * and its downloads overlap the next.
  * Copies run on three library-owned streams of the current device (uploads,
  * replica copies, downloads; created on first use, kept until exit),
  * ordered against `stream` by events: they start
