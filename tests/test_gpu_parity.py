@@ -606,3 +606,31 @@ def test_ragged_contraction(s, pair, fused, mesh, sA, sB, sC, I, J, K, monkeypat
     assert plan.info.tensor_core == 1
     _, ores = oracle_run(mesh, sA, sB, sC, A, B, "f32")
     compare(plan, gpu, ores, exact=False, tol=F32P_TOL)
+
+
+@pytest.mark.parametrize("flags", ["FUSED", "FUSED|RANK_ORDER", "0"])
+def test_repeated_runs_give_identical_bits(s, flags):
+    """Every path is deterministic: one input gives one result, run after run
+    (fixed reduction orders, no atomics), through shmm_run and shmm_run_host."""
+    from partial_sum_reduction_gb300 import helpers as H
+    fl = 0
+    for f in flags.split("|"):
+        fl |= getattr(s, "FLAG_" + f) if f != "0" else 0
+    I, J, K = 1024, 2048, 768
+    A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=31)
+    p = s.Plan(XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ()), I, J, K, "bf16", "bf16", fl)
+    A_r, B_r, ws = H.shard(p, s.TENSOR_A, A), H.shard(p, s.TENSOR_B, B), H.workspace(p)
+    first = None
+    for _ in range(5):
+        C_r = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+        p.run(A_r, B_r, C_r, ws)
+        torch.cuda.synchronize()
+        bits = torch.cat([c.flatten() for c in C_r]).view(torch.int16).cpu()
+        first = bits if first is None else first
+        assert torch.equal(bits, first)
+    C_h = torch.empty(I, K, dtype=torch.bfloat16).pin_memory()
+    C_r = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+    p.run_host(A.pin_memory(), B.pin_memory(), C_h, H.alloc(p, s.TENSOR_A), H.alloc(p, s.TENSOR_B), C_r, ws)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([c.flatten() for c in C_r]).view(torch.int16).cpu(), first)
