@@ -46,31 +46,54 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 }
 
 // One 64x64 output tile of one rank's product into acc (fp32, ascending k).
+// The k-tiles are software-pipelined: all of a tile's global loads are
+// issued at once into registers, and the next tile's loads are in flight
+// while the current one is multiplied from shared memory.  (Loading element
+// by element into shared memory put one memory latency per element on the
+// critical path: 32 us for a single 64x64x64 tile.)  256 threads.
 template <typename IT>
-__device__ void tile_product(const IT *__restrict__ A, const IT *__restrict__ B, int64_t M,
-                             int64_t N, int64_t Kd, int64_t m0, int64_t n0, float (*As)[BM],
-                             float (*Bs)[BN], float acc[TM][TN]) {
+__device__ __forceinline__ void tile_product(const IT *__restrict__ A, const IT *__restrict__ B, int64_t M,
+                                             int64_t N, int64_t Kd, int64_t m0, int64_t n0, float (*As)[BM],
+                                             float (*Bs)[BN], float acc[TM][TN]) {
+    constexpr int LA = BM * BK / 256, LB = BK * BN / 256;  // elements per thread
     const int tid = threadIdx.x;
     const int tr = tid / (BN / TN), tc = tid % (BN / TN);
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
-    for (int64_t k0 = 0; k0 < Kd; k0 += BK) {
-        // A tile: BM x BK, stored transposed; B tile: BK x BN.  256 threads
-        // load 1024 elements each way, zero-filled outside the matrices.
-        for (int idx = tid; idx < BM * BK; idx += blockDim.x) {
-            const int r = idx / BK, c = idx % BK;
+    float ra[LA], rb[LB];
+    // A tile: BM x BK (stored transposed); B tile: BK x BN; zero-filled
+    // outside the matrices
+    auto load = [&](int64_t k0) {
+#pragma unroll
+        for (int i = 0; i < LA; ++i) {
+            const int idx = tid + i * 256, r = idx / BK, c = idx % BK;
             const int64_t gr = m0 + r, gc = k0 + c;
-            As[c][r] = (gr < M && gc < Kd) ? to_f(A[gr * Kd + gc]) : 0.0f;
+            ra[i] = (gr < M && gc < Kd) ? to_f(A[gr * Kd + gc]) : 0.0f;
         }
-        for (int idx = tid; idx < BK * BN; idx += blockDim.x) {
-            const int r = idx / BN, c = idx % BN;
+#pragma unroll
+        for (int i = 0; i < LB; ++i) {
+            const int idx = tid + i * 256, r = idx / BN, c = idx % BN;
             const int64_t gr = k0 + r, gc = n0 + c;
-            Bs[r][c] = (gr < Kd && gc < N) ? to_f(B[gr * N + gc]) : 0.0f;
+            rb[i] = (gr < Kd && gc < N) ? to_f(B[gr * N + gc]) : 0.0f;
+        }
+    };
+    load(0);
+    for (int64_t k0 = 0; k0 < Kd; k0 += BK) {
+#pragma unroll
+        for (int i = 0; i < LA; ++i) {
+            const int idx = tid + i * 256;
+            As[idx % BK][idx / BK] = ra[i];
+        }
+#pragma unroll
+        for (int i = 0; i < LB; ++i) {
+            const int idx = tid + i * 256;
+            Bs[idx / BN][idx % BN] = rb[i];
         }
         __syncthreads();
-#pragma unroll
+        if (k0 + BK < Kd) load(k0 + BK);  // next tile's loads in flight during the FMAs
+#pragma unroll 4
         for (int kk = 0; kk < BK; ++kk) {
             float a[TM], b[TN];
 #pragma unroll
@@ -104,25 +127,25 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < TN; ++j) sum[i][j] = (q == 0) ? acc[i][j] : sum[i][j] + acc[i][j];
     }
-#pragma unroll
+    // the epilogue runs once per tile: kept rolled, since a launch of a few
+    // tiles waits mostly on fetching its code
+#pragma unroll 1
     for (int i = 0; i < TM; ++i) {
         const int64_t row = m0 + tr * TM + i;
         if (row >= k.M) continue;
-#pragma unroll
+#pragma unroll 1
         for (int j = 0; j < TN; ++j) {
             const int64_t col = n0 + tc * TN + j;
             if (col >= k.N) continue;
             const float v = k.gelu ? gelu_tanh(sum[i][j]) : sum[i][j];
             if (!k.fused) {
                 put<OT>((OT *)k.out[unit] + row * k.N + col, v);
-            } else if (k.mode == 0) {
-                const int64_t per = k.M / G;
-                const int b = (int)(row / per);
-                put<OT>((OT *)k.out[unit * G + b] + (row - b * per) * k.N + col, v);
+            } else if (k.mode == 0) {  // 32-bit owner arithmetic: M, N < 2^31
+                const uint32_t per = (uint32_t)(k.M / G), b = (uint32_t)row / per;
+                put<OT>((OT *)k.out[unit * G + b] + (int64_t)((uint32_t)row - b * per) * k.N + col, v);
             } else if (k.mode == 1) {
-                const int64_t per = k.N / G;
-                const int b = (int)(col / per);
-                put<OT>((OT *)k.out[unit * G + b] + row * per + (col - b * per), v);
+                const uint32_t per = (uint32_t)(k.N / G), b = (uint32_t)col / per;
+                put<OT>((OT *)k.out[unit * G + b] + row * per + ((uint32_t)col - b * per), v);
             } else {
                 for (int b = 0; b < G; ++b) put<OT>((OT *)k.out[unit * G + b] + row * k.N + col, v);
             }
@@ -153,7 +176,8 @@ int launch_gemm_simt(const GemmArgs &a, int *status, void *stream) {
     k.N = a.N;
     k.Kd = a.Kd;
     const int64_t gy = (a.M + BM - 1) / BM, gx = (a.N + BN - 1) / BN;
-    if (gy > 65535) return (int)cudaErrorInvalidConfiguration;
+    if (gy > 65535 || a.M >= ((int64_t)1 << 31) || a.N >= ((int64_t)1 << 31))
+        return (int)cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)a.units);
     cudaStream_t s = (cudaStream_t)stream;
     count_launch();
