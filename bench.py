@@ -13,6 +13,7 @@ Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl shmm|referen
         [--workload down_projection|four_case|mlp_pair|split_k_integer]
         python bench.py --sweep collectives     (reduce-scatter / all-reduce /
                                                  all-gather bandwidth sweep)
+        python bench.py --sweep gemm            (the local GEMM beside cuBLAS)
 Under torchrun (N > 1) every GPU runs its own replica of the workload (the
 virtual-rank mesh lives on one GPU); the reported value is the work of all
 replicas over the slowest replica's time (weak scaling).
@@ -787,6 +788,52 @@ def run_shmm(args, dist_ctx):
     return out
 
 
+GEMM_SHAPES = [(8192, 8192, 2048), (8192, 8192, 8192), (8192, 8192, 16384), (16384, 16384, 2048),
+               (2048, 8192, 14336), (8192, 4096, 16384)]
+
+
+def run_gemm_sweep(args):
+    """The local GEMM alone (one rank, no sharding) beside cuBLAS through
+    torch.matmul on the same bf16 operands: CUDA events around batches of 10
+    back-to-back launches, warm-up, median of 5 batches.  One JSON line per
+    shape."""
+    import torch
+    from partial_sum_reduction_gb300 import build
+    build.build()
+    import partial_sum_reduction_gb300 as s
+    peaks, kind = load_peaks()
+
+    def med(fn, reps=5, batch=10):
+        # batches of back-to-back launches between two events, so the host's
+        # per-call cost overlaps the device work as in a real step loop
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(reps):
+            a.record()
+            for _ in range(batch):
+                fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) / batch)
+        return statistics.median(ts)
+
+    for M, N, K in GEMM_SHAPES:
+        A = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+        B = torch.randn(K, N, device="cuda").to(torch.bfloat16)
+        C = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        p = s.Plan([("X", 1)], ((), ()), ((), ()), ((), ()), M, K, N, "bf16", "bf16")
+        f = 2.0 * M * N * K
+        t_s = med(lambda: p.run([A], [B], [C]))
+        t_c = med(lambda: torch.matmul(A, B, out=C))
+        print(json.dumps({"gemm": [M, N, K], "shmm_tflops": f / t_s / 1e9, "cublas_tflops": f / t_c / 1e9,
+                          "shmm_over_cublas": t_c / t_s, "frac_of_burst": f / t_s / 1e9 / peaks["bf16_tflops"],
+                          "peak_kind": kind}), flush=True)
+        del A, B, C
+
+
 def run_sweep(args):
     import torch
     from partial_sum_reduction_gb300 import build
@@ -815,7 +862,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="shmm", choices=["shmm", "reference"])
     ap.add_argument("--workload", default="down_projection", choices=sorted(WORKLOADS))
-    ap.add_argument("--sweep", default=None, choices=[None, "collectives"])
+    ap.add_argument("--sweep", default=None, choices=[None, "collectives", "gemm"])
     ap.add_argument("--sizes", default="1,16,256,1024")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -825,6 +872,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep == "gemm":
+        run_gemm_sweep(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
