@@ -141,3 +141,30 @@ def test_run_host_null_operands_and_chained_calls(s):
     for x, y in zip(Y_r, Y_d):
         assert torch.equal(x, y)
     assert torch.equal(Y_h, Y_d[0].cpu())
+
+
+@pytest.mark.parametrize("mesh,sA,sB,sC,I,J,K,flags", [
+    (Y2, ((), ("Y",)), (("Y",), ()), ((), ()), 2048, 4096, 512, "FUSED"),       # 40 MB: row blocks
+    (XY22, (("X",), ()), ((), ("Y",)), (("X",), ("Y",)), 512, 256, 768, "0"),  # no reduction
+])
+def test_run_host_fp32_cuda_cores(s, mesh, sA, sB, sC, I, J, K, flags):
+    """fp32 operands run on the CUDA-core GEMM; shmm_run_host stages them the
+    same way (row blocks of a fused all-reduce included), bit for bit the
+    device path."""
+    from partial_sum_reduction_gb300 import helpers as H
+    A, B = shmm_inputs.scaled_normal_pair(I, J, K, "f32", seed=I + J)
+    plan = s.Plan(mesh, sA, sB, sC, I, J, K, "f32", "f32", _flags(s, flags))
+    assert plan.info.tensor_core == 0
+    A_d, B_d = H.shard(plan, s.TENSOR_A, A), H.shard(plan, s.TENSOR_B, B)
+    C_d = H.alloc(plan, s.TENSOR_C, fill=float("nan"))
+    ws = H.workspace(plan)
+    plan.run(A_d, B_d, C_d, ws)
+    C_h = torch.full((I, K), float("nan")).pin_memory()
+    A_r, B_r = H.alloc(plan, s.TENSOR_A), H.alloc(plan, s.TENSOR_B)
+    C_r = H.alloc(plan, s.TENSOR_C, fill=float("nan"))
+    plan.run_host(A.pin_memory(), B.pin_memory(), C_h, A_r, B_r, C_r, ws)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    for x, y in zip(C_r, C_d):
+        assert torch.equal(x, y)
+    assert torch.equal(C_h, _stitch(plan, s, C_d, I, K, torch.float32))
