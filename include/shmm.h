@@ -91,7 +91,11 @@ typedef enum {
                                     this operation cannot serve (e.g. a
                                     reduce-scatter on a plan with no
                                     contracted-axis split) */
-    SHMM_ERR_INJECTED = 11       /* failure forced by SHMM_INJECT_FAIL (tests) */
+    SHMM_ERR_INJECTED = 11,      /* failure forced by SHMM_INJECT_FAIL (tests) */
+    SHMM_ERR_BOUNDS = 12         /* bounds-checked build only: a kernel computed
+                                    a global index outside its buffer and
+                                    skipped the access (device status word;
+                                    see shmm_bounds_checked) */
 } shmm_status_t;
 
 typedef enum { SHMM_F32 = 0, SHMM_BF16 = 1 } shmm_dtype_t;
@@ -430,8 +434,9 @@ shmm_status_t shmm_run_static_workspace(const shmm_plan_t *plan, const void *con
                                         const void *const *B_r, void *const *C_r, void *stream);
 
 /* Synchronises `stream`, then reads and clears the device status word that
- * kernels set when a bounded wait expires.  Returns SHMM_OK, SHMM_ERR_TIMEOUT
- * or SHMM_ERR_CUDA. */
+ * kernels set when a bounded wait expires (or, in the bounds-checked build,
+ * when an index falls outside its buffer).  Returns SHMM_OK,
+ * SHMM_ERR_TIMEOUT, SHMM_ERR_BOUNDS or SHMM_ERR_CUDA. */
 shmm_status_t shmm_sync_status(void *stream);
 
 /* Failure-detection self-test: enqueues one kernel that waits on a barrier
@@ -452,6 +457,18 @@ const char *shmm_status_string(shmm_status_t status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int shmm_version(void);
+
+/* 1 if this library is the bounds-checked build (libshmm_checked.so,
+ * compiled with SHMM_CHECKED), else 0.  That build compares every global
+ * index its kernels compute with the extent of the buffer it addresses,
+ * derived from the buffer sizes this header documents; an index outside it
+ * is not accessed and shmm_sync_status() then reports SHMM_ERR_BOUNDS.  The
+ * tensor-core GEMM's operand loads and bulk result stores go through tensor
+ * maps whose extents are those buffer sizes, so the TMA unit clips them; its
+ * per-thread store path is checked like the other kernels.  A debugging aid
+ * with no counterpart on the pages; the checks cost time, so the ordinary
+ * build leaves them out. */
+int shmm_bounds_checked(void);
 
 /* Number of kernels this library has enqueued since it was loaded, over all
  * threads and devices (a diagnostic for benchmarks and tests). */

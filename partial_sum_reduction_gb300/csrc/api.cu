@@ -86,6 +86,16 @@ __global__ void selftest_wait_kernel(int *status, long long limit) {
 
 using shmm::injected;
 
+}  // namespace
+
+int shmm::device_status_ptr(int **ptr) {
+    std::string err;
+    *ptr = status_ptr(&err);
+    return *ptr ? 0 : (int)cudaErrorNoDevice;
+}
+
+namespace {
+
 shmm_status_t cuda_fail(const char *fn, int e, const std::string &extra = "") {
     std::string m = std::string(fn) + ": " + cudaGetErrorString((cudaError_t)e);
     if (!extra.empty()) m += " (" + extra + ")";
@@ -312,6 +322,7 @@ shmm_status_t shmm_local_matmul(const shmm_plan_t *p, const void *const *A_r, co
                                 void *const *P_r, void *stream) {
     static const char *fn = "shmm_local_matmul";
     shmm::clear_error();
+    shmm::Range range(fn);
     if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
     shmm_status_t st;
@@ -332,6 +343,7 @@ shmm_status_t shmm_local_matmul(const shmm_plan_t *p, const void *const *A_r, co
 static shmm_status_t reduce_entry(const char *fn, const shmm_plan_t *p, const void *const *P_r,
                                   void *const *C_r, void *stream, bool all_reduce) {
     shmm::clear_error();
+    shmm::Range range(fn);
     if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
     if (p->U.n == 0)
@@ -383,6 +395,7 @@ shmm_status_t shmm_all_gather(const shmm_plan_t *p, int tensor, const void *cons
                               void *const *full_r, void *stream) {
     static const char *fn = "shmm_all_gather";
     shmm::clear_error();
+    shmm::Range range(fn);
     if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
     const shmm::Groups *g;
@@ -417,6 +430,7 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
                        void *const *C_r, void *workspace, size_t workspace_bytes, void *stream) {
     static const char *fn = "shmm_run";
     shmm::clear_error();
+    shmm::Range range(fn);
     if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
     shmm_status_t st;
@@ -443,12 +457,14 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
     std::vector<void *> wa, wb, wp, wc;
     int e = 0;
     if (p->gA.n && !p->fused_gather) {
+        shmm::Range phase("gather A");
         carve(SHMM_TENSOR_A_LOCAL, in_b, &wa);
         e = gather(p, p->gA_groups, SHMM_TENSOR_A, in_b, A_r, wa.data(), status, stream);
         if (e) return cuda_fail(fn, e, "gather A");
         for (int r = 0; r < p->nranks; ++r) A_loc[r] = wa[r];
     }
     if (p->gB.n && !p->fused_gather) {
+        shmm::Range phase("gather B");
         carve(SHMM_TENSOR_B_LOCAL, in_b, &wb);
         e = gather(p, p->gB_groups, SHMM_TENSOR_B, in_b, B_r, wb.data(), status, stream);
         if (e) return cuda_fail(fn, e, "gather B");
@@ -495,11 +511,13 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
     }
     UnitPtrs up;
     if (!p->U.n) {
+        shmm::Range phase("local matmul");
         shmm::GemmArgs ga = unit_args(p, A_loc.data(), B_loc.data(), dst.data(), 0, p->nranks, &up);
         attach_gather(&ga, up.slot_rank);
         e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
     } else if (fused) {
+        shmm::Range phase("local matmul + fused reduction");
         shmm::GemmArgs ga = unit_args(p, A_loc.data(), B_loc.data(), dst.data(), 0, p->red_groups.count, &up);
         attach_gather(&ga, up.slot_rank);
         e = run_gemm(p, ga, status, stream, &err);
@@ -515,13 +533,20 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         std::vector<int> by_rank(p->nranks);
         for (int r = 0; r < p->nranks; ++r) by_rank[r] = r;
         attach_gather(&ga, by_rank);
-        e = run_gemm(p, ga, status, stream, &err);
+        {
+            shmm::Range phase("local matmul");
+            e = run_gemm(p, ga, status, stream, &err);
+        }
         if (e) return cuda_fail(fn, e, err);
         const int mode = p->collective == SHMM_COLL_REDUCE_SCATTER ? p->scatter_dim : 2;
-        e = reduce(p, (const void *const *)wp.data(), dst.data(), mode, status, stream);
+        {
+            shmm::Range phase(mode == 2 ? "all-reduce" : "reduce-scatter");
+            e = reduce(p, (const void *const *)wp.data(), dst.data(), mode, status, stream);
+        }
         if (e) return cuda_fail(fn, e, "reduce");
     }
     if (p->gC.n) {
+        shmm::Range phase("gather C");
         e = gather(p, p->gC_groups, SHMM_TENSOR_C_REDUCED, out_b, (const void *const *)wc.data(), C_r,
                    status, stream);
         if (e) return cuda_fail(fn, e, "gather C");
@@ -533,6 +558,7 @@ shmm_status_t shmm_layernorm(int64_t rows, int64_t cols, shmm_dtype_t dtype, con
                              const float *gamma, const float *beta, float eps, void *y, void *stream) {
     static const char *fn = "shmm_layernorm";
     shmm::clear_error();
+    shmm::Range range(fn);
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
     if (dtype != SHMM_F32 && dtype != SHMM_BF16) return fail(SHMM_ERR_DTYPE, std::string(fn) + ": bad dtype");
     if (rows < 0 || cols < 0) return fail(SHMM_ERR_SHAPE, std::string(fn) + ": negative size");
@@ -564,6 +590,7 @@ shmm_status_t shmm_layernorm_all_gather(const shmm_plan_t *p, const void *const 
                                         const float *beta, float eps, void *const *full_r, void *stream) {
     static const char *fn = "shmm_layernorm_all_gather";
     shmm::clear_error();
+    shmm::Range range(fn);
     if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
     const shmm::Groups &g = p->gC_groups;
@@ -627,6 +654,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
     static const char *fn = "shmm_run_host";
     constexpr int kStages = 16;
     shmm::clear_error();
+    shmm::Range range(fn);
     if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
     shmm_status_t st;
@@ -770,6 +798,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
     };
 
     for (const Stage &stg : plan_stages) {
+        shmm::Range phase("stage");
         const int u0 = stg.u0, u1 = stg.u1;
         std::vector<int> ranks;
         if (!staged) {

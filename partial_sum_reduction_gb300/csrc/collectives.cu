@@ -22,9 +22,12 @@
 #include <map>
 #include <mutex>
 
+#include "checked.cuh"
 #include "shmm_internal.h"
 
 namespace {
+
+using shmm_dev::in_bounds;
 
 constexpr int kMaxPtrs = SHMM_MAX_RANKS;
 
@@ -34,6 +37,8 @@ struct ReduceK {
     int G, ngroups, mode;       // mode: 0 RS rows, 1 RS cols, 2 AR
     int64_t rows, cols, n;      // per-rank partial shape, n = rows*cols
     int64_t nvec;               // vectors per group (per rank's partial)
+    int *status;                // device status word (bounds-checked build)
+    int64_t src_n, dst_n;       // elements per source / destination buffer
 };
 
 struct GatherK {
@@ -43,6 +48,8 @@ struct GatherK {
     int64_t brows, bvecs;       // block rows, 16-byte vectors per block row
     int64_t full_vecs;          // vectors per row of the gathered box
     int64_t nvec;               // vectors per group = G * brows * bvecs
+    int *status;                // device status word (bounds-checked build)
+    int64_t src_n, dst_n;       // vectors (or elements) per shard / gathered box
 };
 
 __device__ __forceinline__ float gelu_tanh(float x) {
@@ -142,6 +149,7 @@ __device__ __forceinline__ void write_out(const ReduceK &k, int g, IT e, float *
     int b;
     IT off;
     route<IT>(k, e, &b, &off);
+    if (!in_bounds(k.status, (int64_t)off, NV, k.dst_n)) return;
     const int q0 = b >= 0 ? b : 0, q1 = b >= 0 ? b + 1 : k.G;
     for (int q = q0; q < q1; ++q) {
         OT *d = (OT *)k.dst[g * k.G + q] + off;
@@ -172,6 +180,11 @@ __global__ void __launch_bounds__(256) reduce_seq_kernel(const __grid_constant__
             const IT v = base + (IT)u * blockDim.x;
             if (v >= total) continue;
             const IT e = v * V;
+            if (!in_bounds(k.status, (int64_t)e, V, k.src_n)) {
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[u][i] = 0.0f;
+                continue;
+            }
             if constexpr (GT > 0) {
                 float x[GT][V];
 #pragma unroll
@@ -225,6 +238,7 @@ __global__ void __launch_bounds__(256) reduce_scalar_kernel(const __grid_constan
     const int g = blockIdx.y;
     const IT total = (IT)k.n;
     for (IT e = (IT)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (IT)gridDim.x * blockDim.x) {
+        if (!in_bounds(k.status, (int64_t)e, 1, k.src_n)) continue;
         float s;
         if (!TREE) {
             s = Vec<PT>::load1((const PT *)k.src[g * k.G] + e);
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(256) reduce_tree_kernel(const __grid_constant_
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const IT v = base + (IT)u * PER_WARP + sub;
-            if (v < total && src) {
+            if (v < total && src && in_bounds(k.status, (int64_t)v * V, V, k.src_n)) {
                 Vec<PT>::load(src + v * V, x[u]);
             } else {
 #pragma unroll
@@ -289,6 +303,7 @@ __global__ void __launch_bounds__(256) reduce_tree_kernel(const __grid_constant_
             IT off;
             route<IT>(k, v * V, &b, &off);
             if (b >= 0 && b != q) continue;  // RS: only the owner's lane writes
+            if (!in_bounds(k.status, (int64_t)off, V, k.dst_n)) continue;
             store_n<OT, V>((OT *)k.dst[g * k.G + q] + off, s);
         }
     }
@@ -428,6 +443,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
              base += (IT)gridDim.x * blockDim.x * U) {
             uint4 x[U];
             IT dst_off[U];
+            bool ok[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const IT v = base + (IT)u * blockDim.x;
@@ -437,12 +453,14 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
                 const IT r = w / bvecs, c = w - r * bvecs;
                 const int p0 = p / k.blocks1, p1 = p - p0 * k.blocks1;
                 dst_off[u] = ((IT)p0 * brows + r) * full_vecs + (IT)p1 * bvecs + c;
-                x[u] = __ldcs(reinterpret_cast<const uint4 *>(k.src[g * k.G + p]) + w);
+                ok[u] = in_bounds(k.status, (int64_t)w, 1, k.src_n) &&
+                        in_bounds(k.status, (int64_t)dst_off[u], 1, k.dst_n);
+                if (ok[u]) x[u] = __ldcs(reinterpret_cast<const uint4 *>(k.src[g * k.G + p]) + w);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const IT v = base + (IT)u * blockDim.x;
-                if (v >= total) continue;
+                if (v >= total || !ok[u]) continue;
                 for (int m = 0; m < k.G; ++m) __stcs(reinterpret_cast<uint4 *>(k.dst[g * k.G + m]) + dst_off[u], x[u]);
             }
         }
@@ -454,6 +472,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
             const int p0 = p / k.blocks1, p1 = p - p0 * k.blocks1;
             const IT src_off = w;
             const IT dst_off = ((IT)p0 * brows + r) * full_vecs + (IT)p1 * bvecs + c;
+            if (!in_bounds(k.status, (int64_t)src_off, 1, k.src_n) ||
+                !in_bounds(k.status, (int64_t)dst_off, 1, k.dst_n))
+                continue;
             if (elem == 4) {  // element-wise: "vectors" are single elements
                 const uint32_t x = reinterpret_cast<const uint32_t *>(k.src[g * k.G + p])[src_off];
                 for (int m = 0; m < k.G; ++m) reinterpret_cast<uint32_t *>(k.dst[g * k.G + m])[dst_off] = x;
@@ -474,6 +495,8 @@ struct LnK {
     float eps;
     int G;
     int64_t brows, cols;
+    int *status;                // device status word (bounds-checked build)
+    int64_t src_n, dst_n, gb_n;  // elements per block / gathered buffer / gamma and beta
 };
 
 // Deterministic block-wide sum (fixed shuffle tree, then warps in order).
@@ -503,6 +526,10 @@ __global__ void __launch_bounds__(256) ln_gather_scalar_kernel(const __grid_cons
     for (int64_t t = blockIdx.x; t < rows; t += gridDim.x) {
         const int p = (int)(t / k.brows);
         const int64_t rr = t - (int64_t)p * k.brows;
+        const int64_t drow = ((int64_t)p * k.brows + rr) * k.cols;
+        if (!in_bounds(k.status, rr * k.cols, k.cols, k.src_n) || !in_bounds(k.status, drow, k.cols, k.dst_n) ||
+            !in_bounds(k.status, 0, k.cols, k.gb_n))
+            continue;  // the same for every thread of the CTA: block_sum stays collective
         const T *x = (const T *)k.src[g * k.G + p] + rr * k.cols;
         float sum = 0.0f, mean, rstd;
         for (int64_t c = threadIdx.x; c < k.cols; c += blockDim.x) sum += Vec<T>::load1(x + c);
@@ -515,8 +542,7 @@ __global__ void __launch_bounds__(256) ln_gather_scalar_kernel(const __grid_cons
         rstd = 1.0f / sqrtf(block_sum(sq, scratch) * inv_n + k.eps);
         for (int64_t c = threadIdx.x; c < k.cols; c += blockDim.x) {
             const float y = (Vec<T>::load1(x + c) - mean) * rstd * k.gamma[c] + k.beta[c];
-            for (int m = 0; m < k.G; ++m)
-                Vec<T>::store1((T *)k.dst[g * k.G + m] + ((int64_t)p * k.brows + rr) * k.cols + c, y);
+            for (int m = 0; m < k.G; ++m) Vec<T>::store1((T *)k.dst[g * k.G + m] + drow + c, y);
         }
     }
 }
@@ -540,8 +566,9 @@ __global__ void __launch_bounds__(256) ln_gather_reg_kernel(const __grid_constan
         const int vi = threadIdx.x + j * blockDim.x;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
-            ga[j][i] = vi < nvec ? k.gamma[(int64_t)vi * V + i] : 0.0f;
-            be[j][i] = vi < nvec ? k.beta[(int64_t)vi * V + i] : 0.0f;
+            const bool in = vi < nvec && in_bounds(k.status, (int64_t)vi * V + i, 1, k.gb_n);
+            ga[j][i] = in ? k.gamma[(int64_t)vi * V + i] : 0.0f;
+            be[j][i] = in ? k.beta[(int64_t)vi * V + i] : 0.0f;
         }
     }
     auto load_row = [&](int64_t t, float (*v)[V]) {
@@ -551,7 +578,8 @@ __global__ void __launch_bounds__(256) ln_gather_reg_kernel(const __grid_constan
 #pragma unroll
         for (int j = 0; j < NVT; ++j) {
             const int vi = threadIdx.x + j * blockDim.x;
-            if (vi < nvec) Vec<T>::load(x + (int64_t)vi * V, v[j]);
+            if (vi < nvec && in_bounds(k.status, rr * k.cols + (int64_t)vi * V, V, k.src_n))
+                Vec<T>::load(x + (int64_t)vi * V, v[j]);
             else
 #pragma unroll
                 for (int i = 0; i < V; ++i) v[j][i] = 0.0f;
@@ -584,10 +612,9 @@ __global__ void __launch_bounds__(256) ln_gather_reg_kernel(const __grid_constan
             float y[V];
 #pragma unroll
             for (int i = 0; i < V; ++i) y[i] = (v[j][i] - mean) * rstd * ga[j][i] + be[j][i];
-            for (int m = 0; m < k.G; ++m) {
-                T *d = (T *)k.dst[g * k.G + m] + ((int64_t)p * k.brows + rr) * k.cols + (int64_t)vi * V;
-                store_n<T, V>(d, y);
-            }
+            const int64_t d0 = ((int64_t)p * k.brows + rr) * k.cols + (int64_t)vi * V;
+            if (!in_bounds(k.status, d0, V, k.dst_n)) continue;
+            for (int m = 0; m < k.G; ++m) store_n<T, V>((T *)k.dst[g * k.G + m] + d0, y);
         }
         if (t + gridDim.x < rows) load_row(t + gridDim.x, v);
     }
@@ -599,6 +626,7 @@ constexpr int kMaxRects = 256;  // one launch for a 16-rank all-to-all (16 x 16 
 
 struct CopyK {
     shmm::CopyRect r[kMaxRects];
+    int *status;  // device status word (bounds-checked build)
 };
 
 // Rectangle blockIdx.y; the CTAs along x stride over its rows x units, a unit
@@ -610,8 +638,13 @@ __global__ void __launch_bounds__(256) copy_rects_kernel(const __grid_constant__
     const IT total = per_row * (IT)R.h;
     const IT sld = VEC ? (IT)(R.src_ld * elem / 16) : (IT)R.src_ld;
     const IT dld = VEC ? (IT)(R.dst_ld * elem / 16) : (IT)R.dst_ld;
+    const int64_t sroom = VEC ? R.src_room * elem / 16 : R.src_room;
+    const int64_t droom = VEC ? R.dst_room * elem / 16 : R.dst_room;
     for (IT v = (IT)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (IT)gridDim.x * blockDim.x) {
         const IT row = v / per_row, c = v - row * per_row;
+        if (!in_bounds(k.status, (int64_t)(row * sld + c), 1, sroom) ||
+            !in_bounds(k.status, (int64_t)(row * dld + c), 1, droom))
+            continue;
         if (VEC) {
             const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(R.src) + row * sld + c);
             __stcs(reinterpret_cast<uint4 *>(R.dst) + row * dld + c, x);
@@ -628,7 +661,6 @@ __global__ void __launch_bounds__(256) copy_rects_kernel(const __grid_constant__
 namespace shmm {
 
 int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream) {
-    (void)status;
     if (a.ngroups * a.G > kMaxPtrs) return (int)cudaErrorInvalidValue;
     if (a.brows == 0 || a.cols == 0 || a.ngroups == 0) return 0;
     LnK k;
@@ -642,6 +674,10 @@ int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream) {
     k.G = a.G;
     k.brows = a.brows;
     k.cols = a.cols;
+    k.status = status;
+    k.src_n = a.brows * a.cols;
+    k.dst_n = (int64_t)a.G * a.brows * a.cols;
+    k.gb_n = a.cols;
     const int V = a.dt == SHMM_F32 ? 4 : 8;
     const bool reg = a.cols % V == 0 && a.cols <= (int64_t)V * 4 * 256;
     const int64_t rows = (int64_t)a.G * a.brows;
@@ -668,11 +704,11 @@ int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream) {
 }
 
 int launch_copy_rects(const CopyRect *rects, int n, int elem, int *status, void *stream) {
-    (void)status;
     cudaStream_t s = (cudaStream_t)stream;
     for (int i0 = 0; i0 < n; i0 += kMaxRects) {
         const int m = (n - i0) < kMaxRects ? (n - i0) : kMaxRects;
         CopyK k;
+        k.status = status;
         bool vec = true, small = true;
         int64_t most = 0;
         for (int i = 0; i < m; ++i) {
@@ -707,7 +743,6 @@ int launch_copy_rects(const CopyRect *rects, int n, int elem, int *status, void 
 
 
 int launch_reduce(const ReduceArgs &a, int *status, void *stream) {
-    (void)status;
     if (a.ngroups * a.G > kMaxPtrs) return (int)cudaErrorInvalidValue;
     const int64_t n = a.rows * a.cols;
     if (n == 0 || a.ngroups == 0) return 0;
@@ -722,6 +757,9 @@ int launch_reduce(const ReduceArgs &a, int *status, void *stream) {
     k.rows = a.rows;
     k.cols = a.cols;
     k.n = n;
+    k.status = status;
+    k.src_n = n;
+    k.dst_n = a.mode == 2 ? n : n / a.G;  // a reduce-scatter owner holds 1/G of the partial
     if (a.tree && a.G > 32) return (int)cudaErrorInvalidValue;
     const int V = a.pt == SHMM_F32 ? 4 : 8;
     // A 16-byte vector of partials (V elements) must not straddle an owner
@@ -741,7 +779,6 @@ int launch_reduce(const ReduceArgs &a, int *status, void *stream) {
 }
 
 int launch_gather(const GatherArgs &a, int *status, void *stream) {
-    (void)status;
     if (a.ngroups * a.G > kMaxPtrs) return (int)cudaErrorInvalidValue;
     if (a.brows == 0 || a.bcols == 0 || a.ngroups == 0) return 0;
     GatherK k;
@@ -758,6 +795,10 @@ int launch_gather(const GatherArgs &a, int *status, void *stream) {
     k.bvecs = a.bcols / per;
     k.full_vecs = (int64_t)a.blocks1 * k.bvecs;
     k.nvec = (int64_t)a.G * a.brows * k.bvecs;
+    k.status = status;
+    const int64_t unit = vec ? 16 : a.elem;  // bytes per vector or element
+    k.src_n = a.brows * a.bcols * a.elem / unit;
+    k.dst_n = (int64_t)a.blocks0 * a.brows * a.blocks1 * a.bcols * a.elem / unit;
     cudaStream_t s = (cudaStream_t)stream;
     const dim3 grid = grid_for(k.nvec, vec ? 256 * 4 : 256, k.ngroups);
     const int elem = (int)a.elem;

@@ -14,9 +14,12 @@
 
 #include <cstdint>
 
+#include "checked.cuh"
 #include "shmm_internal.h"
 
 namespace {
+
+using shmm_dev::in_bounds;
 
 constexpr int BM = 64, BN = 64, BK = 16, TM = 4, TN = 4;
 
@@ -27,6 +30,8 @@ struct SimtK {
     int G, mode;
     bool fused, gelu;
     int64_t M, N, Kd;
+    int *status;               // device status word (bounds-checked build)
+    int64_t a_n, b_n, out_n;   // elements per A, B and output buffer
 };
 
 template <typename T> __device__ __forceinline__ float to_f(T x);
@@ -52,9 +57,9 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 // by element into shared memory put one memory latency per element on the
 // critical path: 32 us for a single 64x64x64 tile.)  256 threads.
 template <typename IT>
-__device__ __forceinline__ void tile_product(const IT *__restrict__ A, const IT *__restrict__ B, int64_t M,
-                                             int64_t N, int64_t Kd, int64_t m0, int64_t n0, float (*As)[BM],
-                                             float (*Bs)[BN], float acc[TM][TN]) {
+__device__ __forceinline__ void tile_product(const SimtK &k, const IT *__restrict__ A, const IT *__restrict__ B,
+                                             int64_t M, int64_t N, int64_t Kd, int64_t m0, int64_t n0,
+                                             float (*As)[BM], float (*Bs)[BN], float acc[TM][TN]) {
     constexpr int LA = BM * BK / 256, LB = BK * BN / 256;  // elements per thread
     const int tid = threadIdx.x;
     const int tr = tid / (BN / TN), tc = tid % (BN / TN);
@@ -70,13 +75,13 @@ __device__ __forceinline__ void tile_product(const IT *__restrict__ A, const IT 
         for (int i = 0; i < LA; ++i) {
             const int idx = tid + i * 256, r = idx / BK, c = idx % BK;
             const int64_t gr = m0 + r, gc = k0 + c;
-            ra[i] = (gr < M && gc < Kd) ? to_f(A[gr * Kd + gc]) : 0.0f;
+            ra[i] = (gr < M && gc < Kd && in_bounds(k.status, gr * Kd + gc, 1, k.a_n)) ? to_f(A[gr * Kd + gc]) : 0.0f;
         }
 #pragma unroll
         for (int i = 0; i < LB; ++i) {
             const int idx = tid + i * 256, r = idx / BN, c = idx % BN;
             const int64_t gr = k0 + r, gc = n0 + c;
-            rb[i] = (gr < Kd && gc < N) ? to_f(B[gr * N + gc]) : 0.0f;
+            rb[i] = (gr < Kd && gc < N && in_bounds(k.status, gr * N + gc, 1, k.b_n)) ? to_f(B[gr * N + gc]) : 0.0f;
         }
     };
     load(0);
@@ -120,7 +125,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
     float sum[TM][TN];
     for (int q = 0; q < G; ++q) {
         float acc[TM][TN];
-        tile_product<IT>((const IT *)k.A[unit * G + q], (const IT *)k.B[unit * G + q], k.M, k.N,
+        tile_product<IT>(k, (const IT *)k.A[unit * G + q], (const IT *)k.B[unit * G + q], k.M, k.N,
                          k.Kd, m0, n0, As, Bs, acc);
 #pragma unroll
         for (int i = 0; i < TM; ++i)
@@ -139,14 +144,16 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
             if (col >= k.N) continue;
             const float v = k.gelu ? gelu_tanh(sum[i][j]) : sum[i][j];
             if (!k.fused) {
-                put<OT>((OT *)k.out[unit] + row * k.N + col, v);
+                if (in_bounds(k.status, row * k.N + col, 1, k.out_n)) put<OT>((OT *)k.out[unit] + row * k.N + col, v);
             } else if (k.mode == 0) {  // 32-bit owner arithmetic: M, N < 2^31
                 const uint32_t per = (uint32_t)(k.M / G), b = (uint32_t)row / per;
-                put<OT>((OT *)k.out[unit * G + b] + (int64_t)((uint32_t)row - b * per) * k.N + col, v);
+                const int64_t off = (int64_t)((uint32_t)row - b * per) * k.N + col;
+                if (in_bounds(k.status, off, 1, k.out_n)) put<OT>((OT *)k.out[unit * G + b] + off, v);
             } else if (k.mode == 1) {
                 const uint32_t per = (uint32_t)(k.N / G), b = (uint32_t)col / per;
-                put<OT>((OT *)k.out[unit * G + b] + row * per + ((uint32_t)col - b * per), v);
-            } else {
+                const int64_t off = row * per + ((uint32_t)col - b * per);
+                if (in_bounds(k.status, off, 1, k.out_n)) put<OT>((OT *)k.out[unit * G + b] + off, v);
+            } else if (in_bounds(k.status, row * k.N + col, 1, k.out_n)) {
                 for (int b = 0; b < G; ++b) put<OT>((OT *)k.out[unit * G + b] + row * k.N + col, v);
             }
         }
@@ -158,7 +165,6 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
 namespace shmm {
 
 int launch_gemm_simt(const GemmArgs &a, int *status, void *stream) {
-    (void)status;
     const int G = a.fused ? a.G : 1;
     if (a.units * G > SHMM_MAX_RANKS) return (int)cudaErrorInvalidValue;
     if (a.M == 0 || a.N == 0 || a.units == 0) return 0;
@@ -175,6 +181,10 @@ int launch_gemm_simt(const GemmArgs &a, int *status, void *stream) {
     k.M = a.M;
     k.N = a.N;
     k.Kd = a.Kd;
+    k.status = status;
+    k.a_n = a.M * a.Kd;
+    k.b_n = a.Kd * a.N;
+    k.out_n = a.fused && a.mode != 2 ? a.M * a.N / G : a.M * a.N;  // an owner's block, or a whole copy
     const int64_t gy = (a.M + BM - 1) / BM, gx = (a.N + BN - 1) / BN;
     if (gy > 65535 || a.M >= ((int64_t)1 << 31) || a.N >= ((int64_t)1 << 31))
         return (int)cudaErrorInvalidConfiguration;

@@ -36,6 +36,7 @@
 #include <mutex>
 #include <string>
 
+#include "checked.cuh"
 #include "device_wait.cuh"
 #include "shmm_internal.h"
 
@@ -67,6 +68,7 @@ struct TcK {
     int n_maps_a, n_maps_b;
     int gathered;  // 0: map i is operand slot i's own buffer
     int tma_store;  // 1: the epilogue stores through tmC, else per-thread stores
+    int64_t out_n;  // elements per output buffer (per-thread stores, bounds-checked build)
 };
 
 // Operands read in place from an all-gather group's shards: which shard of
@@ -306,32 +308,35 @@ __device__ __forceinline__ void store_run(void *p, const float *v, int n, bool f
 __device__ __forceinline__ void store_tile_row(const TcK &k, int unit, int Gq, int64_t row, int64_t col0,
                                                const float *v, int n, bool f32, int64_t es) {
     if (!k.fused) {
-        char *p = (char *)k.out[unit] + (row * k.N + col0) * es;
-        store_run(p, v, n, f32, true);
+        const int64_t off = row * k.N + col0;
+        if (!in_bounds(k.status, off, n, k.out_n)) return;
+        store_run((char *)k.out[unit] + off * es, v, n, f32, true);
     } else if (k.mode == 0) {
         const int64_t per = k.M / Gq;
         const int b = (int)(row / per);
-        char *p = (char *)k.out[unit * Gq + b] + ((row - b * per) * k.N + col0) * es;
-        store_run(p, v, n, f32, true);
+        const int64_t off = (row - b * per) * k.N + col0;
+        if (!in_bounds(k.status, off, n, k.out_n)) return;
+        store_run((char *)k.out[unit * Gq + b] + off * es, v, n, f32, true);
     } else if (k.mode == 1) {
         const int64_t per = k.N / Gq;
         if ((per % 32) == 0) {
             const int b = (int)(col0 / per);
-            char *p = (char *)k.out[unit * Gq + b] + (row * per + (col0 - b * per)) * es;
-            store_run(p, v, n, f32, true);
+            const int64_t off = row * per + (col0 - b * per);
+            if (!in_bounds(k.status, off, n, k.out_n)) return;
+            store_run((char *)k.out[unit * Gq + b] + off * es, v, n, f32, true);
         } else {
             for (int i = 0; i < n; ++i) {
                 const int64_t col = col0 + i;
                 const int b = (int)(col / per);
-                char *p = (char *)k.out[unit * Gq + b] + (row * per + (col - b * per)) * es;
-                store_run(p, v + i, 1, f32, false);
+                const int64_t off = row * per + (col - b * per);
+                if (!in_bounds(k.status, off, 1, k.out_n)) continue;
+                store_run((char *)k.out[unit * Gq + b] + off * es, v + i, 1, f32, false);
             }
         }
     } else {
-        for (int b = 0; b < Gq; ++b) {
-            char *p = (char *)k.out[unit * Gq + b] + (row * k.N + col0) * es;
-            store_run(p, v, n, f32, true);
-        }
+        const int64_t off = row * k.N + col0;
+        if (!in_bounds(k.status, off, n, k.out_n)) return;
+        for (int b = 0; b < Gq; ++b) store_run((char *)k.out[unit * Gq + b] + off * es, v, n, f32, true);
     }
 }
 
@@ -1226,6 +1231,7 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         k.M = a.M;
         k.N = a.N;
         k.Kd = a.Kd;
+        k.out_n = c_rows * c_cols;  // an owner's block, or a whole copy
         k.m_tiles = (int)((a.M + BM - 1) / BM);
         k.k_blocks = (int)((a.Kd + BK - 1) / BK);
         // 256-row tiles on CTA pairs unless the local M fits one 128-row tile

@@ -433,6 +433,7 @@ shmm_status_t shmm_reshard(const shmm_mesh_t *mesh, const shmm_spec_t *spec_from
                            const void *const *src_r, void *const *dst_r, void *stream) {
     using shmm::fail;
     shmm::clear_error();
+    shmm::Range range("shmm_reshard");
     static const char *fn = "shmm_reshard: ";
     if (!mesh || !spec_from || !spec_to || !src_r || !dst_r) return fail(SHMM_ERR_NULL, std::string(fn) + "NULL argument");
     if (dtype != SHMM_F32 && dtype != SHMM_BF16) return fail(SHMM_ERR_DTYPE, std::string(fn) + "dtype must be F32 or BF16");
@@ -495,8 +496,12 @@ shmm_status_t shmm_reshard(const shmm_mesh_t *mesh, const shmm_spec_t *spec_from
                 const int64_t r0 = std::max(D.off[0], i * bh), r1 = std::min(D.off[0] + D.ext[0], (i + 1) * bh);
                 const int64_t c0 = std::max(D.off[1], j * bw), c1 = std::min(D.off[1] + D.ext[1], (j + 1) * bw);
                 shmm::CopyRect cr;
-                cr.src = static_cast<const char *>(src_r[s]) + ((r0 - i * bh) * bw + (c0 - j * bw)) * eb;
-                cr.dst = static_cast<char *>(dst_r[r]) + ((r0 - D.off[0]) * D.ext[1] + (c0 - D.off[1])) * eb;
+                const int64_t so = (r0 - i * bh) * bw + (c0 - j * bw);
+                const int64_t dof = (r0 - D.off[0]) * D.ext[1] + (c0 - D.off[1]);
+                cr.src = static_cast<const char *>(src_r[s]) + so * eb;
+                cr.dst = static_cast<char *>(dst_r[r]) + dof * eb;
+                cr.src_room = bh * bw - so;
+                cr.dst_room = D.numel() - dof;
                 cr.src_ld = bw;
                 cr.dst_ld = D.ext[1];
                 cr.h = r1 - r0;
@@ -505,7 +510,10 @@ shmm_status_t shmm_reshard(const shmm_mesh_t *mesh, const shmm_spec_t *spec_from
             }
     }
     if (shmm::injected("shmm_reshard")) return fail(SHMM_ERR_INJECTED, std::string(fn) + "injected failure");
-    const int e = shmm::launch_copy_rects(rects.data(), (int)rects.size(), (int)eb, nullptr, stream);
+    int *status = nullptr;
+    if (const int se = shmm::device_status_ptr(&status))
+        return fail(SHMM_ERR_CUDA, std::string(fn) + "device status word (" + std::to_string(se) + ")");
+    const int e = shmm::launch_copy_rects(rects.data(), (int)rects.size(), (int)eb, status, stream);
     if (e) return fail(SHMM_ERR_CUDA, std::string(fn) + "kernel launch failed (" + std::to_string(e) + ")");
     return SHMM_OK;
 }
@@ -547,6 +555,7 @@ const char *shmm_status_string(shmm_status_t s) {
         case SHMM_ERR_NOMEM: return "SHMM_ERR_NOMEM";
         case SHMM_ERR_UNSUPPORTED: return "SHMM_ERR_UNSUPPORTED";
         case SHMM_ERR_INJECTED: return "SHMM_ERR_INJECTED";
+        case SHMM_ERR_BOUNDS: return "SHMM_ERR_BOUNDS";
     }
     return "SHMM_ERR_UNKNOWN";
 }
@@ -554,6 +563,12 @@ const char *shmm_status_string(shmm_status_t s) {
 const char *shmm_last_error(void) { return shmm::g_last_error.c_str(); }
 
 int shmm_version(void) { return 100; }
+
+#ifdef SHMM_CHECKED
+int shmm_bounds_checked(void) { return 1; }
+#else
+int shmm_bounds_checked(void) { return 0; }
+#endif
 
 uint64_t shmm_kernel_launches(void) { return shmm::g_launches.load(std::memory_order_relaxed); }
 

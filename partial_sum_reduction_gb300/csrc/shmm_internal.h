@@ -2,6 +2,8 @@
 // kernel launchers of libshmm.  Not part of the public interface.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -138,10 +140,13 @@ int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream);
 // Copies rectangles between row-major buffers: rectangle i moves h[i] rows of
 // w[i] elements of `elem` bytes from src[i] (row pitch src_ld[i] elements) to
 // dst[i] (pitch dst_ld[i]).  The reshard (all-to-all) collective.
+// src_room / dst_room: elements from src[i] / dst[i] to the end of their
+// buffers (the extents the bounds-checked build compares indices with).
 struct CopyRect {
     const void *src;
     void *dst;
     int64_t src_ld, dst_ld, h, w;
+    int64_t src_room, dst_room;
 };
 int launch_copy_rects(const CopyRect *rects, int n, int elem, int *status, void *stream);
 
@@ -183,8 +188,20 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
 // Count of kernels enqueued by this library since it was loaded.
 void count_launch(int n = 1);
 
-// Device status word (set by kernels whose bounded waits expire).
-int device_status_ptr(int **ptr);  // cudaError_t value
-int device_status_read_clear(int *value, void *stream);
+// An NVTX range around the enqueueing of one entry point or phase: a
+// profiler (ncu --nvtx, Nsight Systems) files the kernels launched inside it
+// under its name.  With no profiler attached, push and pop cost a call each.
+class Range {
+  public:
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range &) = delete;
+    Range &operator=(const Range &) = delete;
+};
+
+// Device address of the status word that kernels set when a bounded wait
+// expires or (bounds-checked build) an index falls outside its buffer, on
+// the current device.  Returns a cudaError_t value.
+int device_status_ptr(int **ptr);
 
 }  // namespace shmm

@@ -20,14 +20,16 @@ import re
 from typing import List, Optional, Sequence, Tuple
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libshmm.so")
+# SHMM_CHECKED=1 selects the bounds-checked build (build.build(checked=True)):
+# the same kernels with every global index compared with its buffer's extent.
+LIB_PATH = os.path.join(HERE, "libshmm_checked.so" if os.environ.get("SHMM_CHECKED") == "1" else "libshmm.so")
 
 MAX_AXES = 8
 MAX_RANKS = 256
 
 # status codes
 OK, ERR_INVALID_SPEC, ERR_ILLEGAL_OUTPUT, ERR_SHAPE, ERR_DTYPE, ERR_NULL, ERR_ALIGN, ERR_CUDA, \
-    ERR_TIMEOUT, ERR_NOMEM, ERR_UNSUPPORTED, ERR_INJECTED = range(12)
+    ERR_TIMEOUT, ERR_NOMEM, ERR_UNSUPPORTED, ERR_INJECTED, ERR_BOUNDS = range(13)
 F32, BF16 = 0, 1
 FLAG_FUSED, FLAG_GELU, FLAG_TREE, FLAG_PARTIAL_OUT_DTYPE, FLAG_SIMT = 0x1, 0x2, 0x4, 0x8, 0x10
 FLAG_RANK_ORDER = 0x20
@@ -82,7 +84,7 @@ EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
            "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace",
            "shmm_selftest_wait_timeout", "shmm_choose_operand", "shmm_reshard", "shmm_layernorm",
-           "shmm_layernorm_all_gather", "shmm_run_host"]
+           "shmm_layernorm_all_gather", "shmm_run_host", "shmm_bounds_checked"]
 
 _lib = None
 
@@ -92,8 +94,9 @@ def lib():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError("libshmm.so is not built (%s); run partial_sum_reduction_gb300.build.build()"
-                               % LIB_PATH)
+            raise RuntimeError("%s is not built (%s); run partial_sum_reduction_gb300.build.build(%s)"
+                               % (os.path.basename(LIB_PATH), LIB_PATH,
+                                  "checked=True" if LIB_PATH.endswith("_checked.so") else ""))
         L = ctypes.CDLL(LIB_PATH)
         P = ctypes.c_void_p
         PP = ctypes.POINTER(ctypes.c_void_p)
@@ -455,6 +458,11 @@ def shmm_selftest_wait_timeout(limit_cycles: int, stream=None) -> None:
 
 def shmm_version() -> int:
     return lib().shmm_version()
+
+
+def shmm_bounds_checked() -> bool:
+    """True if the loaded library is the bounds-checked build."""
+    return bool(lib().shmm_bounds_checked())
 
 
 def shmm_kernel_launches() -> int:

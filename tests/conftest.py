@@ -34,3 +34,20 @@ def load_golden(name):
 @pytest.fixture(scope="session")
 def golden():
     return load_golden
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean(request):
+    """After every GPU test that loaded the library: no kernel left a timeout
+    (or, in the bounds-checked build, an out-of-bounds index) in the device
+    status word, and the library is the build SHMM_CHECKED asks for."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    from partial_sum_reduction_gb300 import shmm as m
+    if m._lib is None:
+        return
+    import torch
+    torch.cuda.synchronize()
+    m.shmm_sync_status()
+    assert m.shmm_bounds_checked() == (os.environ.get("SHMM_CHECKED") == "1")

@@ -57,6 +57,28 @@ def test_binding_constants_match_header(shmm):
     assert (shmm.F32, shmm.BF16) == (0, 1)
 
 
+def test_binding_status_codes_match_header(shmm):
+    """Every status code the header defines has the binding's value and the
+    library's name."""
+    src = open(os.path.join(ROOT, "include", "shmm.h")).read()
+    codes = dict(re.findall(r"SHMM_(OK|ERR_[A-Z_]+) = (\d+)", src))
+    assert len(codes) == 13
+    for name, val in codes.items():
+        assert getattr(shmm.shmm, name) == int(val), name
+        assert shmm.lib().shmm_status_string(int(val)).decode() == "SHMM_" + name
+
+
+def test_bounds_checked_build_exports_every_declared_symbol(shmm):
+    """The bounds-checked variant (same sources, SHMM_CHECKED) builds, exports
+    the same C ABI and says which build it is; the ordinary one says not."""
+    from partial_sum_reduction_gb300 import build
+    L = ctypes.CDLL(build.build(checked=True))
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert L.shmm_bounds_checked() == 1
+    assert ctypes.CDLL(build.LIB).shmm_bounds_checked() == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch):
     import partial_sum_reduction_gb300.shmm as m
     monkeypatch.setattr(m, "_lib", None)
