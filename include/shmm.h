@@ -323,10 +323,13 @@ shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const vo
  * reduction groups or ranks, each split into blocks of 256-row multiples
  * when there are fewer units than stages and a block of C rows needs only
  * the same rows of A.  A stage's uploads overlap the previous stage's GEMM
- * and its downloads overlap the next.
- * Copies run on three library-owned streams of the current device (uploads,
- * replica copies, downloads; created on first use, kept until exit),
- * ordered against `stream` by events: they start
+ * and its downloads overlap the next; consecutive stages' GEMMs alternate
+ * between `stream` and a second compute stream, so they may overlap too.
+ * A B box goes up whole at its first use, and its replicas are copied
+ * right after it.
+ * Copies and those GEMMs run on four library-owned streams of the current
+ * device (uploads, replica copies, downloads, compute; created on first
+ * use, kept until exit), ordered against `stream` by events: they start
  * after the work already enqueued on `stream`, and work enqueued on `stream`
  * after this call sees every copy complete.  Host buffers must stay valid
  * until then; page-locked host memory is needed for copies that overlap

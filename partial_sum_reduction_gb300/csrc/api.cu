@@ -244,8 +244,10 @@ shmm::GemmArgs unit_args(const shmm_plan_t *p, const void *const *A, const void 
 // life of the process: host-to-device uploads, device-to-device replica
 // copies (kept off the upload stream, which the host link limits) and
 // device-to-host downloads, each ordered against the others by events.
+// Per device, created once: uploads, replica copies, downloads, and a
+// second compute stream on which every other stage's GEMM runs.
 struct SideStreams {
-    cudaStream_t up = nullptr, rep = nullptr, down = nullptr;
+    cudaStream_t up = nullptr, rep = nullptr, down = nullptr, alt = nullptr;
 };
 cudaError_t side_streams(SideStreams *out) {
     static std::mutex mu;
@@ -256,21 +258,18 @@ cudaError_t side_streams(SideStreams *out) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!cache[dev].up) {
-        SideStreams s;
-        e = cudaStreamCreateWithFlags(&s.up, cudaStreamNonBlocking);
-        if (e != cudaSuccess) return e;
-        e = cudaStreamCreateWithFlags(&s.rep, cudaStreamNonBlocking);
-        if (e != cudaSuccess) {
-            cudaStreamDestroy(s.up);
-            return e;
+        cudaStream_t st[4] = {};
+        for (int i = 0; i < 4; ++i) {
+            e = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking);
+            if (e != cudaSuccess) {
+                for (int j = 0; j < i; ++j) cudaStreamDestroy(st[j]);
+                return e;
+            }
         }
-        e = cudaStreamCreateWithFlags(&s.down, cudaStreamNonBlocking);
-        if (e != cudaSuccess) {
-            cudaStreamDestroy(s.up);
-            cudaStreamDestroy(s.rep);
-            return e;
-        }
-        cache[dev] = s;
+        cache[dev].up = st[0];
+        cache[dev].rep = st[1];
+        cache[dev].down = st[2];
+        cache[dev].alt = st[3];
     }
     *out = cache[dev];
     return cudaSuccess;
@@ -710,25 +709,29 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
     cudaStream_t cs = (cudaStream_t)stream;
 
     std::vector<cudaEvent_t> events;
+    auto recorded = [&](cudaStream_t on, cudaEvent_t *ev) -> cudaError_t {
+        cudaError_t r = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (r != cudaSuccess) return r;
+        events.push_back(*ev);
+        return cudaEventRecord(*ev, on);
+    };
     auto record = [&](cudaStream_t on, cudaStream_t waiter) -> cudaError_t {
         cudaEvent_t ev;
-        cudaError_t r = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-        if (r != cudaSuccess) return r;
-        events.push_back(ev);
-        r = cudaEventRecord(ev, on);
+        const cudaError_t r = recorded(on, &ev);
         return r == cudaSuccess ? cudaStreamWaitEvent(waiter, ev, 0) : r;
     };
-    // Every exit joins both side streams back into the caller's stream, so
+    // Every exit joins the side streams back into the caller's stream, so
     // nothing this call enqueued outlives what the caller orders after it.
     auto finish = [&](shmm_status_t result) -> shmm_status_t {
         record(ss.up, cs);
         record(ss.rep, cs);
         record(ss.down, cs);
+        record(ss.alt, cs);
         for (cudaEvent_t ev : events) cudaEventDestroy(ev);  // released once complete
         return result;
     };
     if ((e = record(cs, ss.up)) != cudaSuccess || (e = record(cs, ss.rep)) != cudaSuccess ||
-        (e = record(cs, ss.down)) != cudaSuccess)
+        (e = record(cs, ss.down)) != cudaSuccess || (e = record(cs, ss.alt)) != cudaSuccess)
         return finish(cuda_fail(fn, e, "events"));
 
     // Each distinct shard (A: each row block of it) crosses the host link
@@ -742,6 +745,23 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
         size_t bytes;
     };
     std::vector<Replica> replicas;
+    // B crosses the link whole at its first use.  The ranks holding replicas
+    // of that box get their device copies right after it, on the replica
+    // stream, whatever stage they belong to; their GEMMs wait for their own
+    // copy's event only.  (Copying a replica in its own rank's stage held
+    // that stage's GEMM behind 0.47 GB of device copies.)
+    std::map<std::pair<int64_t, int64_t>, std::vector<int>> b_holders;
+    if (B_host)
+        for (int r = 0; r < p->nranks; ++r) {
+            const shmm::Box &b = p->boxes[SHMM_TENSOR_B][r];
+            if (b.numel()) b_holders[std::make_pair(b.off[0], b.off[1])].push_back(r);
+        }
+    struct EarlyCopy {
+        int rank;
+        Replica c;
+    };
+    std::vector<EarlyCopy> early;
+    std::vector<cudaEvent_t> b_ready(p->nranks, nullptr);
     // Rows [r0, r1) of box b, and where they start in its dense buffer.
     auto rows_of = [](const shmm::Box &b, int64_t r0, int64_t r1) {
         shmm::Box s = b;
@@ -778,6 +798,12 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
             if (it == o.first->end()) {
                 (*o.first)[key] = r;
                 r2 = upload_box(dst, o.host, b, o.cols, in_b, ss.up);
+                if (o.whole)
+                    for (int h : b_holders[std::make_pair(whole.off[0], whole.off[1])])
+                        if (!b_done[h]) {
+                            b_done[h] = 1;
+                            early.push_back({h, {static_cast<char *>(o.dev[h]) + at, dst, bytes}});
+                        }
             } else {
                 replicas.push_back({dst, static_cast<const char *>(o.dev[it->second]) + at, bytes});
                 r2 = cudaSuccess;
@@ -797,9 +823,14 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
         return download_box(C_host, src, rows_of(whole, r0, r1), p->K, out_b, ss.down);
     };
 
+    int si = 0;
     for (const Stage &stg : plan_stages) {
         shmm::Range phase("stage");
         const int u0 = stg.u0, u1 = stg.u1;
+        // Consecutive stages' GEMMs alternate between the caller's stream
+        // and a second one, so one stage's last partial wave of tiles
+        // overlaps the next stage's first.
+        cudaStream_t gs = staged && (si++ & 1) ? ss.alt : cs;
         std::vector<int> ranks;
         if (!staged) {
             for (int r = 0; r < p->nranks; ++r) ranks.push_back(r);
@@ -812,14 +843,24 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
         replicas.clear();
         for (int r : ranks)
             if ((e = upload(r, stg)) != cudaSuccess) return finish(cuda_fail(fn, e, "upload"));
-        if ((e = record(ss.up, cs)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
-        if (!replicas.empty()) {
+        if ((e = record(ss.up, gs)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
+        if (!replicas.empty() || !early.empty())
             if ((e = record(ss.up, ss.rep)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
+        if (!replicas.empty()) {
             for (const Replica &c : replicas)
                 if ((e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToDevice, ss.rep)) != cudaSuccess)
                     return finish(cuda_fail(fn, e, "replica copy"));
-            if ((e = record(ss.rep, cs)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
+            if ((e = record(ss.rep, gs)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
         }
+        for (const EarlyCopy &c : early) {
+            if ((e = cudaMemcpyAsync(c.c.dst, c.c.src, c.c.bytes, cudaMemcpyDeviceToDevice, ss.rep)) != cudaSuccess ||
+                (e = recorded(ss.rep, &b_ready[c.rank])) != cudaSuccess)
+                return finish(cuda_fail(fn, e, "replica copy"));
+        }
+        early.clear();
+        for (int r : ranks)  // every stage of a rank whose B is a device copy
+            if (b_ready[r] && (e = cudaStreamWaitEvent(gs, b_ready[r], 0)) != cudaSuccess)
+                return finish(cuda_fail(fn, e, "events"));
         if (staged) {
             UnitPtrs up;
             shmm::GemmArgs ga = unit_args(p, (const void *const *)A_r, (const void *const *)B_r, C_r, u0, u1, &up);
@@ -828,7 +869,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
                 for (auto &a : up.a) a = static_cast<const char *>(a) + stg.r0 * Kd * in_b;
                 for (auto &o : up.out) o = static_cast<char *>(o) + stg.r0 * c_cols * out_b;
             }
-            const int ge = run_gemm(p, ga, status, stream, &err);
+            const int ge = run_gemm(p, ga, status, gs, &err);
             if (ge) return finish(cuda_fail(fn, ge, err));
         } else {
             st = shmm_run(p, (const void *const *)A_r, (const void *const *)B_r, C_r, workspace,
@@ -838,7 +879,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
                 return finish(fail(st, std::string(fn) + ": " + m));
             }
         }
-        if ((e = record(cs, ss.down)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
+        if ((e = record(gs, ss.down)) != cudaSuccess) return finish(cuda_fail(fn, e, "events"));
         for (int r : ranks)
             if ((e = download(r, stg)) != cudaSuccess) return finish(cuda_fail(fn, e, "download"));
     }
