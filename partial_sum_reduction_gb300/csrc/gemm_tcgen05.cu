@@ -398,20 +398,21 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int r, const float *v, b
     }
 }
 
-// Final pass over one finished tile for one epilogue warp: output rows
-// row0..row0+31 (row0 < M), TMEM lanes from lane_s.  Each 32-column chunk is
+// Final pass over one finished 256-column sub-tile for one epilogue warp:
+// output rows row0..row0+31 (row0 < M), columns from col_base, TMEM lanes
+// from lane_s.  Each 32-column chunk is
 // loaded from TMEM, passed through GeLU if asked, rounded into the warp's
 // staging buffer and written by one bulk tensor store per destination: the
 // unit's block, the owner's block of a reduce-scatter, or every member's
 // copy of an all-reduce.  Stores clip at the output's edges.  `staged`
 // counts the warp's boxes (it picks the buffer).
-__device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, int row0, int nt, uint32_t lane_s,
-                                               uint32_t cbuf, uint32_t *staged, int lane) {
+__device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, int row0, int col_base,
+                                               uint32_t lane_s, uint32_t cbuf, uint32_t *staged, int lane) {
     constexpr int BN = 256;
     const bool f32 = k.out_f32 != 0;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = nt * BN + c * 32;
+        const int col0 = col_base + c * 32;
         if (col0 >= k.N) break;
         float v[32];
         tmem_ld32(lane_s + (uint32_t)(c * 32), v);
@@ -446,14 +447,16 @@ __device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, i
 // Epilogue of one warp (warps 2..5) over the tiles its CTA (or CTA pair)
 // owns: work items first, first + stride, ... < total; output rows
 // mt * tile_rows + row_base + [0, 32) of each tile, TMEM lanes from
-// lane_base.  Tile i's sum S sits in TMEM buffer i % 2.  In rank order the
-// group's later products arrive in the other buffer W and are folded into S
-// (fp32, ascending rank order), W handed back after each; accumulating, S
-// already holds the sum.  Then GeLU if asked, one rounding and the stores
-// (bulk tensor stores through the staging buffers at cbuf, or per thread),
-// and S is handed back.  full_bar(b): the barrier on which the MMA thread
-// reports a finished product in buffer b; release(b): hands buffer b back.
-template <typename FullBar, typename Release>
+// lane_base.  A tile is NH sub-tiles of 256 columns.  With NH = 1, tile i's
+// sum S sits in TMEM buffer i % 2; in rank order the group's later products
+// arrive in the other buffer W and are folded into S (fp32, ascending rank
+// order), W handed back after each; accumulating, S already holds the sum.
+// With NH = 2 (accumulating or unfused only), sub-tile h sits in buffer h.
+// Then GeLU if asked, one rounding and the stores (bulk tensor stores
+// through the staging buffers at cbuf, or per thread), and S is handed back.
+// full_bar(b): the barrier on which the MMA thread reports a finished
+// product in buffer b; release(b): hands buffer b back.
+template <int NH, typename FullBar, typename Release>
 __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride, int total, int Gq, int tile_rows,
                                             int row_base, uint32_t lane_base, uint32_t cbuf, int lane,
                                             volatile int *abort_flag, FullBar full_bar, Release release) {
@@ -475,55 +478,61 @@ __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride,
         return ok != 0;
     };
     int tile_iter = 0;
-    for (int t = first; t < total; t += stride, ++tile_iter) {
+    bool ok = true;
+    for (int t = first; t < total && ok; t += stride, ++tile_iter) {
         int unit, mt, nt;
         tile_coords(k, t, &unit, &mt, &nt);
-        const int bS = tile_iter & 1, bW = bS ^ 1;
-        const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
-        const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
-        if (!warp_wait_full(bS)) break;  // S = product of the group's first rank
-        bool ok = true;
-        const int folds = k.accum ? 1 : Gq;  // accum: S already holds the sum
-        for (int q = 1; q < folds; ++q) {
-            // S = S + P_q in fp32: the ascending-rank sequential sum
-            if (!warp_wait_full(bW)) {
+        for (int h = 0; h < NH && ok; ++h) {
+            const int bS = NH == 2 ? h : (tile_iter & 1), bW = bS ^ 1;
+            const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
+            const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
+            if (!warp_wait_full(bS)) {  // S = product of the group's first rank
                 ok = false;
                 break;
             }
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                float a[32], w[32];
-                tmem_ld32(s_base + (uint32_t)(c * 32), a);
-                tmem_ld32(w_base + (uint32_t)(c * 32), w);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = a[i] + w[i];
-                tmem_st32(s_base + (uint32_t)(c * 32), a);
-            }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            release(bW);  // W may take the next product
-        }
-        if (!ok) break;
-        const int row0 = mt * tile_rows + row_base;
-        if (k.tma_store) {
-            if (row0 < k.M) store_tile_tma(k, unit, Gq, row0, nt, s_base, cbuf, &staged, lane);
-        } else {
-            const int64_t row = (int64_t)row0 + lane;
-            const bool row_ok = row < k.M;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                float v[32];
-                tmem_ld32(s_base + (uint32_t)(c * 32), v);
-                if (k.gelu) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+            const int folds = k.accum || NH == 2 ? 1 : Gq;  // accum: S already holds the sum
+            for (int q = 1; q < folds; ++q) {
+                // S = S + P_q in fp32: the ascending-rank sequential sum
+                if (!warp_wait_full(bW)) {
+                    ok = false;
+                    break;
                 }
-                const int64_t col0 = (int64_t)nt * BN + c * 32;
-                if (!row_ok || col0 >= k.N) continue;
-                const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
-                store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float a[32], w[32];
+                    tmem_ld32(s_base + (uint32_t)(c * 32), a);
+                    tmem_ld32(w_base + (uint32_t)(c * 32), w);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = a[i] + w[i];
+                    tmem_st32(s_base + (uint32_t)(c * 32), a);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                release(bW);  // W may take the next product
             }
+            if (!ok) break;
+            const int row0 = mt * tile_rows + row_base;
+            const int col_base = (nt * NH + h) * BN;
+            if (k.tma_store) {
+                if (row0 < k.M) store_tile_tma(k, unit, Gq, row0, col_base, s_base, cbuf, &staged, lane);
+            } else {
+                const int64_t row = (int64_t)row0 + lane;
+                const bool row_ok = row < k.M;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(s_base + (uint32_t)(c * 32), v);
+                    if (k.gelu) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                    }
+                    const int64_t col0 = (int64_t)col_base + c * 32;
+                    if (!row_ok || col0 >= k.N) continue;
+                    const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
+                    store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
+                }
+            }
+            release(bS);  // S may take the next tile's products
         }
-        release(bS);  // S may take the next tile's products
     }
     if (lane == 0) bulk_wait_all();  // no store still reads staging at exit
     __syncwarp();
@@ -715,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int quad = warp % 4;
-        drain_tiles(k, blockIdx.x, gridDim.x, total, Gq, BM, quad * 32, tmem_base + ((uint32_t)(quad * 32) << 16),
+        drain_tiles<1>(k, blockIdx.x, gridDim.x, total, Gq, BM, quad * 32, tmem_base + ((uint32_t)(quad * 32) << 16),
                     smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes), lane, abort_flag,
                     [&](int b) { return accf_bar(b); },
                     [&](int b) {
@@ -734,29 +743,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 }
 
 
-// ---- CTA-pair kernel: 256x256 output tiles on two SMs ---------------------
+// ---- CTA-pair kernel: 256 x (256 NH) output tiles on two SMs --------------
 //
-// A cluster of two CTAs computes one 256x256 tile with tcgen05.mma
-// cta_group::2 (M = 256, N = 256, K = 16): each CTA stages its own 128 rows of
-// A and its 128 of the tile's 256 columns of B, so a CTA moves 32 KB per
-// k-block instead of the 48 KB of a 128x256 single-CTA tile, and the pair's
-// accumulator is split by rows over the two TMEMs.  The even CTA (the
-// leader) issues the MMAs; both CTAs' TMA loads complete on the leader's
-// full barrier; the leader's commits reach both CTAs' barriers.  Each CTA's
-// epilogue drains its own 128 rows exactly as in the single-CTA kernel.
+// A cluster of two CTAs computes one tile with tcgen05.mma cta_group::2
+// (M = 256, N = 256, K = 16): each CTA stages its own 128 rows of A and its
+// 128 of each 256-column half's columns of B, and the pair's accumulator is
+// split by rows over the two TMEMs.  The even CTA (the leader) issues the
+// MMAs; both CTAs' TMA loads complete on the leader's full barrier; the
+// leader's commits reach both CTAs' barriers.  Each CTA's epilogue drains
+// its own 128 rows exactly as in the single-CTA kernel.
+//
+// NH = 1: 256x256 tiles, 32 KB per CTA per k-block (6 stages), TMEM holds two
+// tiles so one tile's epilogue overlaps the next tile's MMAs.  NH = 2:
+// 256x512 tiles, two MMAs per K step sharing the A operand, 48 KB per CTA
+// per k-block (4 stages): a quarter fewer operand bytes per FLOP, for
+// products whose operand loads (not the tensor pipe) set the pace.  The
+// tile's two halves fill all of TMEM, so the next tile's MMAs into half h
+// wait until the epilogue has drained half h.  NH = 2 serves accumulating
+// or unfused launches only (no rank-order fold needs a spare buffer).
 
+template <int NH>
 struct Cfg2 {
-    static constexpr int A_BYTES = BM * BK * 2;   // 16 KB: this CTA's 128 rows
-    static constexpr int B_BYTES = BK * 128 * 2;  // 16 KB: this CTA's 128 columns
+    static constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's 128 rows
+    static constexpr int B_BYTES = NH * BK * 128 * 2;  // 16 KB per half: this CTA's 128 columns of it
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int STAGES = 6;
+    static constexpr int STAGES = NH == 1 ? 6 : 4;
     static constexpr int SMEM = STAGES * STAGE + kStagingBytes + 1024 /*align*/ + 1024 /*barriers, tables*/;
 };
 
+template <int NH>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcK k) {
-    using C = Cfg2;
+    using C = Cfg2<NH>;
     constexpr int S = C::STAGES;
-    constexpr int BN = 256;
+    constexpr int BN = 256;           // N of one MMA, and of one TMEM buffer
+    constexpr int TW = BN * NH;       // tile width
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -781,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
     const uint32_t cr = cluster_ctarank();  // 0: leader, 1: peer
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int Gq = k.fused ? k.G : 1;
-    const int tiles_per_unit = k.m_tiles * k.n_tiles;  // 256x256 tiles
+    const int tiles_per_unit = k.m_tiles * k.n_tiles;  // 256 x TW tiles
     const int total = k.units * tiles_per_unit;
 
     auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
@@ -849,9 +869,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
                         if (!k.gathered) {
                             tma_load_2d_pair(a_dst, &k.tmA[ri], bar, kb * BK, mt * 256 + (int)cr * BM);
 #pragma unroll
-                            for (int c = 0; c < 2; ++c)
-                                tma_load_2d_pair(b_dst + c * 8192, &k.tmB[ri], bar, nt * BN + (int)cr * 128 + c * 64,
-                                                 kb * BK);
+                            for (int h = 0; h < NH; ++h)
+#pragma unroll
+                                for (int c = 0; c < 2; ++c)
+                                    tma_load_2d_pair(b_dst + (h * 2 + c) * 8192, &k.tmB[ri], bar,
+                                                     nt * TW + h * BN + (int)cr * 128 + c * 64, kb * BK);
                         } else {
                             int32_t a_c, b_r, x;
                             const int a_p1 = shard_split(k.a_b1, k.a_bcols, (int64_t)kb * BK, &a_c);
@@ -859,12 +881,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
                                              a_r);
                             const int b_p0 = shard_split(k.b_b0, k.b_brows, (int64_t)kb * BK, &b_r);
 #pragma unroll
-                            for (int c = 0; c < 2; ++c) {
-                                const int b_p1 =
-                                    shard_split(k.b_b1, k.b_bcols, (int64_t)nt * BN + (int)cr * 128 + c * 64, &x);
-                                tma_load_2d_pair(b_dst + c * 8192,
-                                                 &k.tmB[s_bidx[ri * kMaxMaps + b_p0 * k.b_b1 + b_p1]], bar, x, b_r);
-                            }
+                            for (int h = 0; h < NH; ++h)
+#pragma unroll
+                                for (int c = 0; c < 2; ++c) {
+                                    const int b_p1 = shard_split(
+                                        k.b_b1, k.b_bcols, (int64_t)nt * TW + h * BN + (int)cr * 128 + c * 64, &x);
+                                    tma_load_2d_pair(b_dst + (h * 2 + c) * 8192,
+                                                     &k.tmB[s_bidx[ri * kMaxMaps + b_p0 * k.b_b1 + b_p1]], bar, x,
+                                                     b_r);
+                                }
                         }
                         last_parity[s] = (int)ph;
                     }
@@ -885,23 +910,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
         if (lane == 0 && cr == 0) {
             constexpr uint32_t idesc = instr_desc_pair(BN);
             uint32_t it = 0;
-            uint32_t fills0 = 0, fills1 = 0;
+            uint32_t fills[2] = {0, 0};  // products finished per TMEM buffer
             int tile_iter = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs, ++tile_iter) {
-                const int bS = tile_iter & 1;
+                // NH = 1: the tile's sum S in buffer tile_iter % 2 (rank order:
+                // later products in the other); NH = 2: half h in buffer h
+                const int bS = NH == 2 ? 0 : (tile_iter & 1);
                 for (int q = 0; q < Gq && ok; ++q) {
                     // accum: every rank's product continues the sum in S
                     const bool into_s = q == 0 || k.accum;
                     const int b = into_s ? bS : (bS ^ 1);
-                    const uint32_t nf = b ? fills1 : fills0;
-                    if ((q == 0 || !k.accum) && !mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
-                    for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
+                    const bool fresh = q == 0 || !k.accum;  // this product starts its buffers
+                    for (int kb = 0; kb < k.k_blocks && ok; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(full_bar(s), ph, abort_flag, k.status)) {
@@ -912,18 +933,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
                         const uint32_t a_addr = smem_u32(tiles + s * C::STAGE);
                         const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                            const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
-                            const uint64_t bd = smem_desc(b_addr + kk * 2048, 8192, 1024);
-                            umma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0 || (q > 0 && k.accum)) ? 1u : 0u);
+                        for (int h = 0; h < NH; ++h) {
+                            // a fresh buffer: the epilogue has handed back its previous fill
+                            // (half 0 of the next wide tile starts while half 1 drains)
+                            if (kb == 0 && fresh) {
+                                if (!mbar_wait(acce_bar(b + h), (fills[b + h] & 1) ^ 1, abort_flag, k.status)) {
+                                    ok = false;
+                                    break;
+                                }
+                                fence_after();
+                            }
+                            const uint32_t d_tmem = tmem_base + (uint32_t)((b + h) * BN);
+#pragma unroll
+                            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                                const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
+                                const uint64_t bd = smem_desc(b_addr + h * 16384 + kk * 2048, 8192, 1024);
+                                umma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0 || (q > 0 && k.accum)) ? 1u : 0u);
+                            }
                         }
+                        if (!ok) break;
                         umma2_commit_both(empty_bar(s));
                     }
                     if (!ok) break;
                     if (k.accum && q < Gq - 1) continue;  // S is not finished
-                    umma2_commit_both(accf_bar(b));
-                    if (b) ++fills1;
-                    else ++fills0;
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) {
+                        umma2_commit_both(accf_bar(b + h));
+                        ++fills[b + h];
+                    }
                 }
             }
             umma2_commit_both(drain_bar);
@@ -932,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
     } else {
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
         const int quad = warp % 4;
-        drain_tiles(k, pair, npairs, total, Gq, 256, (int)cr * BM + quad * 32,
+        drain_tiles<NH>(k, pair, npairs, total, Gq, 256, (int)cr * BM + quad * 32,
                     tmem_base + ((uint32_t)(quad * 32) << 16),
                     smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes), lane, abort_flag,
                     [&](int b) { return accf_bar(b); },
@@ -1064,17 +1101,22 @@ cudaError_t launch_bn(TcK &k, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// Launches the CTA-pair kernel: clusters of two, at most as many pairs as can
-// be resident at once (one CTA per SM).
-cudaError_t launch_pair(TcK &k, cudaStream_t s) {
-    using C = Cfg2;
+// CTA pairs of gemm_tc2_kernel<NH> that can be resident at once (one CTA
+// per SM); 0 if none.  Sets the kernel's shared-memory attribute on first use
+// per device.
+template <int NH>
+cudaError_t pair_capacity(int *pairs) {
+    using C = Cfg2<NH>;
+    static std::mutex mu;
     static bool attr_set[64] = {};
     static int max_pairs[64] = {};
     int dev = 0;
-    cudaGetDevice(&dev);
-    const bool cache = dev >= 0 && dev < 64;
-    if (!cache || !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(gemm_tc2_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t q = {};
         cudaLaunchAttribute qa[1];
@@ -1088,16 +1130,26 @@ cudaError_t launch_pair(TcK &k, cudaStream_t s) {
         q.attrs = qa;
         q.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &q);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<NH>, &q);
         if (e != cudaSuccess) return e;
-        if (!cache) return cudaErrorInvalidDevice;
         max_pairs[dev] = n < 0 ? 0 : n;
         attr_set[dev] = true;
     }
-    const int cap = max_pairs[dev];
+    *pairs = max_pairs[dev];
+    return cudaSuccess;
+}
+
+// Launches the CTA-pair kernel: clusters of two, at most as many pairs as can
+// be resident at once.
+template <int NH>
+cudaError_t launch_pair(TcK &k, cudaStream_t s) {
+    using C = Cfg2<NH>;
+    int cap = 0;
+    const cudaError_t ce = pair_capacity<NH>(&cap);
+    if (ce != cudaSuccess) return ce;
     if (cap < 1) return cudaErrorNotSupported;  // no pair can be resident: the caller falls back
     k.m_tiles = (int)((k.M + 255) / 256);
-    k.n_tiles = (int)((k.N + 255) / 256);
+    k.n_tiles = (int)((k.N + 256 * NH - 1) / (256 * NH));
     const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
     const int npairs = (int)(total < cap ? total : cap);
     cudaLaunchConfig_t cfg = {};
@@ -1113,12 +1165,39 @@ cudaError_t launch_pair(TcK &k, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     shmm::count_launch();
-    return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, k);
+    return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<NH>, k);
 }
 
 bool pair_kernel_enabled() {
     const char *e = getenv("SHMM_TC_PAIR");
     return !(e && e[0] == '0');
+}
+
+// Tile width of the pair kernel for this launch: 256 x 512 tiles (NH = 2)
+// move a quarter fewer operand bytes per FLOP, and on this GPU the 256 x 256
+// kernel's loads hold its MMAs back by about 12 % (its tensor pipe alone,
+// fed from stale shared memory, runs 1.13x faster; with a quarter of the
+// loads removed, 1.12x).  Wide tiles halve the tile count, so a launch of
+// few tiles can lose more to its last partial wave; and the next tile's
+// first MMAs wait for the epilogue to drain half a tile, about two wide
+// k-blocks.  Pick the smaller estimate: waves x work per tile x slowdown.
+// SHMM_TC_WIDE=0 / 1 forces 256- / 512-column tiles (tests compare them).
+int pair_halves(const TcK &k) {
+    if (k.fused && !k.accum && k.G > 1) return 1;  // the rank-order fold needs TMEM's second buffer
+    const char *env = getenv("SHMM_TC_WIDE");
+    if (env && env[0] == '0') return 1;
+    if (env && env[0] == '1') return 2;
+    if (k.N <= 256) return 1;
+    int cap1 = 0, cap2 = 0;
+    if (pair_capacity<1>(&cap1) != cudaSuccess || pair_capacity<2>(&cap2) != cudaSuccess || cap1 < 1 || cap2 < 1)
+        return 1;
+    const int64_t m_t = (k.M + 255) / 256;
+    const int64_t t1 = (int64_t)k.units * m_t * ((k.N + 255) / 256);
+    const int64_t t2 = (int64_t)k.units * m_t * ((k.N + 511) / 512);
+    const double kb = (double)k.k_blocks * (k.fused && k.accum ? k.G : 1);  // k-blocks per tile
+    const double narrow = (double)((t1 + cap1 - 1) / cap1) * 1.12;
+    const double wide = (double)((t2 + cap2 - 1) / cap2) * 2.0 * (1.0 + 2.0 / kb);
+    return wide < narrow ? 2 : 1;
 }
 
 }  // namespace
@@ -1236,7 +1315,7 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         k.k_blocks = (int)((a.Kd + BK - 1) / BK);
         // 256-row tiles on CTA pairs unless the local M fits one 128-row tile
         cudaError_t e = cudaErrorNotSupported;
-        if (a.M > BM && pair_kernel_enabled()) e = launch_pair(k, s);
+        if (a.M > BM && pair_kernel_enabled()) e = pair_halves(k) == 2 ? launch_pair<2>(k, s) : launch_pair<1>(k, s);
         if (e == cudaErrorNotSupported) {
             // single-CTA tiles when no CTA pair fits (or is wanted)
             k.m_tiles = (int)((a.M + BM - 1) / BM);

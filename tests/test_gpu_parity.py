@@ -377,6 +377,44 @@ def test_integer_bf16_tensor_core_bit_exact(s, flags, sC):
     compare(plan, gpu, ores, exact=True)
 
 
+# ------------------------------------------- 256 x 512 tiles on CTA pairs
+
+WIDE = [
+    # name, mesh, sA, sB, sC, I, J, K, flags, out dtype
+    ("case1_two_tiles", XY22, (("X",), ()), ((), ("Y",)), (("X",), ("Y",)), 768, 512, 1536, "0", "bf16"),
+    ("gelu_ragged_n", X8, ((), ()), ((), ("X",)), ((), ("X",)), 512, 256, 8 * 640, "GELU", "bf16"),
+    ("fused_all_reduce", XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ()), 1024, 1024, 1280, "FUSED", "bf16"),
+    ("fused_rs_rows", X8, ((), ("X",)), (("X",), ()), (("X",), ()), 2048, 1024, 1024, "FUSED", "f32"),
+    ("fused_rs_cols", [("X", 4)], ((), ("X",)), (("X",), ()), ((), ("X",)), 512, 512, 2048, "FUSED", "bf16"),
+    # owner blocks of 260 rows: per-thread stores instead of bulk tensor stores
+    ("fused_rs_rows_per_thread", [("X", 2)], ((), ("X",)), (("X",), ()), (("X",), ()), 520, 256, 1032, "FUSED",
+     "f32"),
+    ("in_place_gather_b", XY22, (("X",), ()), ((), ("X",)), (("X",), ()), 512, 384, 1280, "FUSED", "f32"),
+    ("ragged_m", Y2, ((), ("Y",)), (("Y",), ()), ((), ()), 300, 256, 1000, "FUSED", "bf16"),
+]
+
+
+@pytest.mark.parametrize("name,mesh,sA,sB,sC,I,J,K,flags,out", WIDE, ids=[w[0] for w in WIDE])
+def test_wide_tiles_equal_narrow_bitwise(s, name, mesh, sA, sB, sC, I, J, K, flags, out, monkeypatch):
+    """256 x 512 tiles (two MMAs per K step sharing the A operand, one tile
+    filling TMEM) add every output element's products over the same
+    k-blocks in the same order as 256 x 256 tiles, so both give the same
+    bits in every write mode; and both match the oracle."""
+    fl = 0
+    for f in flags.split("|"):
+        fl |= getattr(s, "FLAG_" + f) if f != "0" else 0
+    A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=I + K)
+    monkeypatch.setenv("SHMM_TC_WIDE", "0")
+    _, g1 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", out, fl)
+    monkeypatch.setenv("SHMM_TC_WIDE", "1")
+    p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", out, fl)
+    assert p2.info.tensor_core == 1 and p2.info.local_I > 128
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b), name
+    _, ores = oracle_run(mesh, sA, sB, sC, A, B, out, gelu="GELU" in flags)
+    compare(p2, g2, ores, exact=False, tol=BF16_TOL if out == "bf16" else F32P_TOL)
+
+
 def test_all_reduce_replicas_identical(s):
     A, B = shmm_inputs.scaled_normal_pair(256, 2048, 384, "bf16", seed=2)
     plan, gpu = run_gpu(X8, ((), ("X",)), (("X",), ()), ((), ()), A, B, "bf16", "bf16", s.FLAG_FUSED)
