@@ -110,8 +110,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // At most one committed store group may still be reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// At most `keep` (0, 1 or 3) committed store groups may still be reading
+// shared memory.
+__device__ __forceinline__ void bulk_wait_read(int keep) {
+    if (keep >= 3) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+    else if (keep == 1) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    else asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // Every committed store has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -360,11 +364,11 @@ __device__ __forceinline__ void tile_coords(const TcK &k, int t, int *unit, int 
     *nt = q / bm;
 }
 
-// Epilogue output staging: per epilogue warp two buffers of one 32 x 32 box
-// (4 KB at fp32), so a warp fills one while the previous box's store reads
-// the other.
-constexpr int kStageBoxBytes = 32 * 32 * 4;
-constexpr int kStagingBytes = 4 * 2 * kStageBoxBytes;
+// Epilogue output staging: 32 KB per CTA, shared evenly by the epilogue
+// warps (8 KB each with four warps, 4 KB with eight).  A warp cycles
+// through its share in 32 x 32 boxes (4 KB at fp32, 2 KB at bf16), so it
+// fills the next box while earlier boxes' stores still read theirs.
+constexpr int kStagingBytes = 32 * 1024;
 
 // Row r of a 32 x 32 output box into its staging buffer, in the swizzled
 // layout the output tensor maps declare: bf16 rows are 64 bytes and 16-byte
@@ -399,19 +403,22 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int r, const float *v, b
 }
 
 // Final pass over one finished 256-column sub-tile for one epilogue warp:
-// output rows row0..row0+31 (row0 < M), columns from col_base, TMEM lanes
-// from lane_s.  Each 32-column chunk is
-// loaded from TMEM, passed through GeLU if asked, rounded into the warp's
-// staging buffer and written by one bulk tensor store per destination: the
-// unit's block, the owner's block of a reduce-scatter, or every member's
-// copy of an all-reduce.  Stores clip at the output's edges.  `staged`
-// counts the warp's boxes (it picks the buffer).
-__device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, int row0, int col_base,
-                                               uint32_t lane_s, uint32_t cbuf, uint32_t *staged, int lane) {
-    constexpr int BN = 256;
+// output rows row0..row0+31 (row0 < M), the 32-column chunks c0..c1-1 of
+// the sub-tile starting at column col_base, TMEM lanes from lane_s.  Each
+// chunk is loaded from TMEM, passed through GeLU if asked, rounded into the
+// next box of the warp's staging share (`share` bytes at cbuf) and written
+// by one bulk tensor store per destination: the unit's block, the owner's
+// block of a reduce-scatter, or every member's copy of an all-reduce.
+// Stores clip at the output's edges.  `staged` counts the warp's boxes (it
+// picks the box).
+__device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, int row0, int col_base, int c0,
+                                               int c1, uint32_t lane_s, uint32_t cbuf, uint32_t share,
+                                               uint32_t *staged, int lane) {
     const bool f32 = k.out_f32 != 0;
+    const uint32_t box = f32 ? 4096u : 2048u;
+    const uint32_t nbuf = share / box;  // 1, 2 or 4
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = c0; c < c1; ++c) {
         const int col0 = col_base + c * 32;
         if (col0 >= k.N) break;
         float v[32];
@@ -420,8 +427,8 @@ __device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, i
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
         }
-        const uint32_t buf = cbuf + (*staged & 1u) * (uint32_t)kStageBoxBytes;
-        if (lane == 0) bulk_wait_read_1();  // the store two boxes back has read this buffer
+        const uint32_t buf = cbuf + (*staged % nbuf) * box;
+        if (lane == 0) bulk_wait_read((int)nbuf - 1);  // the store nbuf boxes back has read this box
         __syncwarp();
         stage_row(buf, lane, v, f32);
         fence_async_smem();
@@ -458,8 +465,9 @@ __device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, i
 // product in buffer b; release(b): hands buffer b back.
 template <int NH, typename FullBar, typename Release>
 __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride, int total, int Gq, int tile_rows,
-                                            int row_base, uint32_t lane_base, uint32_t cbuf, int lane,
-                                            volatile int *abort_flag, FullBar full_bar, Release release) {
+                                            int row_base, uint32_t lane_base, int c0, int c1, uint32_t cbuf,
+                                            uint32_t share, int lane, volatile int *abort_flag, FullBar full_bar,
+                                            Release release) {
     constexpr int BN = 256;
     const bool f32 = k.out_f32 != 0;
     const int64_t es = f32 ? 4 : 2;
@@ -498,7 +506,7 @@ __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride,
                     break;
                 }
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = c0; c < c1; ++c) {
                     float a[32], w[32];
                     tmem_ld32(s_base + (uint32_t)(c * 32), a);
                     tmem_ld32(w_base + (uint32_t)(c * 32), w);
@@ -513,12 +521,13 @@ __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride,
             const int row0 = mt * tile_rows + row_base;
             const int col_base = (nt * NH + h) * BN;
             if (k.tma_store) {
-                if (row0 < k.M) store_tile_tma(k, unit, Gq, row0, col_base, s_base, cbuf, &staged, lane);
+                if (row0 < k.M)
+                    store_tile_tma(k, unit, Gq, row0, col_base, c0, c1, s_base, cbuf, share, &staged, lane);
             } else {
                 const int64_t row = (int64_t)row0 + lane;
                 const bool row_ok = row < k.M;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = c0; c < c1; ++c) {
                     float v[32];
                     tmem_ld32(s_base + (uint32_t)(c * 32), v);
                     if (k.gelu) {
@@ -725,7 +734,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         // ---------------- epilogue (warps 2..5) ----------------
         const int quad = warp % 4;
         drain_tiles<1>(k, blockIdx.x, gridDim.x, total, Gq, BM, quad * 32, tmem_base + ((uint32_t)(quad * 32) << 16),
-                    smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes), lane, abort_flag,
+                       0, BN / 32, smem_u32(staging) + (uint32_t)((warp - 2) * (kStagingBytes / 4)),
+                       kStagingBytes / 4, lane, abort_flag,
                     [&](int b) { return accf_bar(b); },
                     [&](int b) {
                         fence_before();
@@ -769,10 +779,15 @@ struct Cfg2 {
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int STAGES = NH == 1 ? 6 : 4;
     static constexpr int SMEM = STAGES * STAGE + kStagingBytes + 1024 /*align*/ + 1024 /*barriers, tables*/;
+    // Epilogue warps: with a tile's drain exposed (NH = 2), two per TMEM lane
+    // quadrant, each draining half of the columns, so the drain takes half
+    // as long.
+    static constexpr int EPI_WARPS = NH == 2 ? 8 : 4;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
 };
 
 template <int NH>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcK k) {
+__global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __grid_constant__ TcK k) {
     using C = Cfg2<NH>;
     constexpr int S = C::STAGES;
     constexpr int BN = 256;           // N of one MMA, and of one TMEM buffer
@@ -817,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(accf_bar(s), 1);
-            mbar_init(acce_bar(s), 2 * 4 * 32);  // both CTAs' epilogue threads
+            mbar_init(acce_bar(s), 2 * C::EPI_WARPS * 32);  // both CTAs' epilogue threads
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -967,11 +982,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
             mbar_wait(drain_bar, 0, abort_flag, k.status, false);
         }
     } else {
-        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        // ---------------- epilogue (warps 2.., both CTAs) ----------------
+        // A warp reaches only its own TMEM lane quadrant (warp % 4); with
+        // eight epilogue warps, two share a quadrant and split the columns.
+        const int ew = warp - 2;
         const int quad = warp % 4;
+        constexpr int CH = (BN / 32) / (C::EPI_WARPS / 4);  // 32-column chunks per warp
+        const int c0 = (ew / 4) * CH;
+        constexpr uint32_t share = kStagingBytes / C::EPI_WARPS;
         drain_tiles<NH>(k, pair, npairs, total, Gq, 256, (int)cr * BM + quad * 32,
-                    tmem_base + ((uint32_t)(quad * 32) << 16),
-                    smem_u32(staging) + (uint32_t)((warp - 2) * 2 * kStageBoxBytes), lane, abort_flag,
+                    tmem_base + ((uint32_t)(quad * 32) << 16), c0, c0 + CH,
+                    smem_u32(staging) + (uint32_t)ew * share, share, lane, abort_flag,
                     [&](int b) { return accf_bar(b); },
                     [&](int b) {
                         fence_before();
@@ -1125,7 +1146,7 @@ cudaError_t pair_capacity(int *pairs) {
         qa[0].val.clusterDim.y = 1;
         qa[0].val.clusterDim.z = 1;
         q.gridDim = dim3((unsigned)(num_sms() & ~1));
-        q.blockDim = dim3(kThreads);
+        q.blockDim = dim3(C::THREADS);
         q.dynamicSmemBytes = C::SMEM;
         q.attrs = qa;
         q.numAttrs = 1;
@@ -1159,7 +1180,7 @@ cudaError_t launch_pair(TcK &k, cudaStream_t s) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(2 * npairs));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -1173,15 +1194,20 @@ bool pair_kernel_enabled() {
     return !(e && e[0] == '0');
 }
 
-// Tile width of the pair kernel for this launch: 256 x 512 tiles (NH = 2)
-// move a quarter fewer operand bytes per FLOP, and on this GPU the 256 x 256
-// kernel's loads hold its MMAs back by about 12 % (its tensor pipe alone,
-// fed from stale shared memory, runs 1.13x faster; with a quarter of the
-// loads removed, 1.12x).  Wide tiles halve the tile count, so a launch of
-// few tiles can lose more to its last partial wave; and the next tile's
-// first MMAs wait for the epilogue to drain half a tile, about two wide
-// k-blocks.  Pick the smaller estimate: waves x work per tile x slowdown.
-// SHMM_TC_WIDE=0 / 1 forces 256- / 512-column tiles (tests compare them).
+// Tile width of the pair kernel for this launch.  256 x 512 tiles (NH = 2)
+// move a quarter fewer operand bytes per FLOP; the 256 x 256 kernel's loads
+// hold its MMAs back (its tensor pipe alone, fed from stale shared memory,
+// runs 1.13x faster; with a quarter of its loads removed, 1.12x).  But a
+// wide tile fills TMEM, so each tile boundary idles the tensor pipe while
+// the epilogue drains (about 8 k cycles, some six wide k-blocks); and wide
+// tiles halve the tile count, so a launch of few tiles can lose more to its
+// last partial wave.  Measured on 8192^2 x K products (same wave counts),
+// wide / narrow time = 0.86 (1 + 6 / k-blocks per tile): 1.02 at K = 2048,
+// 0.94 at 4096, 0.91 at 8192, 0.88 at 16384.  A GeLU epilogue drains
+// slower: the MLP's first matmul (64 k-blocks) ran no faster wide, so it
+// counts ten k-blocks.  Pick the smaller estimate: waves x work per tile x
+// that factor.  SHMM_TC_WIDE=0 / 1 forces 256- / 512-column tiles (tests
+// compare them).
 int pair_halves(const TcK &k) {
     if (k.fused && !k.accum && k.G > 1) return 1;  // the rank-order fold needs TMEM's second buffer
     const char *env = getenv("SHMM_TC_WIDE");
@@ -1195,8 +1221,8 @@ int pair_halves(const TcK &k) {
     const int64_t t1 = (int64_t)k.units * m_t * ((k.N + 255) / 256);
     const int64_t t2 = (int64_t)k.units * m_t * ((k.N + 511) / 512);
     const double kb = (double)k.k_blocks * (k.fused && k.accum ? k.G : 1);  // k-blocks per tile
-    const double narrow = (double)((t1 + cap1 - 1) / cap1) * 1.12;
-    const double wide = (double)((t2 + cap2 - 1) / cap2) * 2.0 * (1.0 + 2.0 / kb);
+    const double narrow = (double)((t1 + cap1 - 1) / cap1);
+    const double wide = (double)((t2 + cap2 - 1) / cap2) * 2.0 * 0.86 * (1.0 + (k.gelu ? 10.0 : 6.0) / kb);
     return wide < narrow ? 2 : 1;
 }
 
