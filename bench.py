@@ -77,8 +77,8 @@ FOUR_CASES = [
 #       -k regex:gemm_tc2 -s 3 -c 1 python bench.py --steps 5 --warmup 3 --no-cpu-baseline),
 # valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "down_projection": {"kernel_sha256_16": "00ee927a4cf0a72e", "bytes": 3.979114240e9 + 0.262183936e9,
-                        "kernel": "gemm_tc2_kernel"},
+    "down_projection": {"kernel_sha256_16": "5df4a93fc6bb36a2", "bytes": 3.208675584e9 + 0.242411008e9,
+                        "kernel": "gemm_tc2_kernel<2> (256x512 tiles)"},
 }
 
 
@@ -765,7 +765,8 @@ def run_shmm(args, dist_ctx):
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "peak_nominal": NOMINAL_PEAKS["bf16_tflops"],
                      "frac_of_nominal": achieved / NOMINAL_PEAKS["bf16_tflops"],
-                     "kernel": ("gemm_tc2_kernel (CTA pair) with fused reduction epilogue"
+                     "kernel": ("gemm_tc2_kernel (CTA pairs, 256x256 or 256x512 tiles as the launcher "
+                                "picks) with fused reduction epilogue"
                                 if os.environ.get("SHMM_TC_PAIR", "1") != "0"
                                 else "gemm_tc_kernel<256> with fused reduction epilogue")},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
