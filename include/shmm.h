@@ -58,6 +58,16 @@
  * accumulator and adds them in ascending rank order, so it matches the
  * standalone sequential reduction bit for bit; the CUDA-core path always
  * does this.  Every path is deterministic: one input gives one result.
+ *
+ * Environment (read at each call; none is needed in normal use).
+ *   SHMM_TC_PAIR=0     tensor-core GEMMs on single CTAs (128-row tiles)
+ *                      instead of CTA pairs (256-row tiles).
+ *   SHMM_TC_WIDE=0|1   CTA-pair tiles 256 columns wide (0) or 512 (1)
+ *                      instead of the launcher's choice.  Both widths give
+ *                      the same bits.
+ *   SHMM_INJECT_FAIL=name[,name...]  the named entry points fail with
+ *                      SHMM_ERR_INJECTED before enqueuing anything (tests
+ *                      of error propagation).
  */
 #ifndef SHMM_H
 #define SHMM_H
