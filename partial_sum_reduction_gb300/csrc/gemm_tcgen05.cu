@@ -4,23 +4,28 @@
 // Z_i = X_i A_i), bf16 inputs, fp32 accumulation, optionally with the
 // partial-sum reduction fused into the epilogue (same page, step 4).
 //
-// Design (one persistent CTA per SM, 192 threads):
-//   warp 0      TMA producer: per k-block, one 128x64 tile of A (K-major,
-//               128-byte swizzle) and BN/64 tiles of 64x64 of B (B is
+// Two persistent kernels, one CTA per SM, with the same warp roles:
+//   warp 0      TMA producer: per k-block of 64, the CTA's rows of A (K-major,
+//               128-byte swizzle) and its columns of B in 64x64 boxes (B is
 //               row-major [J,K], i.e. MN-major for the MMA: no transpose)
-//               into an S-stage shared-memory ring guarded by mbarriers;
-//   warp 1      allocates the 512 TMEM columns and issues tcgen05.mma
-//               (M=128, N=BN, K=16) from one thread, committing each stage
-//               back to the producer and each finished tile to the epilogue;
-//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator (warp w reads
-//               TMEM lanes 32*(w%4)..+31, one output row per thread), then
-//               GeLU / conversion / store.
-// Work units are (rank, m-tile, n-tile) or, fused, (group, m-tile, n-tile):
-// the G ranks of a reduction group are multiplied one after another into G
-// separate TMEM accumulators and the epilogue adds them in ascending rank
-// order in fp32, so the fused result equals the unfused partials summed by
-// the standalone reduction bit for bit.  Each output tile is written once,
-// to its owner (reduce-scatter) or to every member (all-reduce).
+//               into a shared-memory ring of stages guarded by mbarriers;
+//   warp 1      allocates the 512 TMEM columns and issues tcgen05.mma from
+//               one thread, committing each stage back to the producer and
+//               each finished accumulator to the epilogue;
+//   warps 2..   epilogue: tcgen05.ld of the fp32 accumulator (warp w reads
+//               TMEM lanes 32*(w%4)..+31, one output row per thread), GeLU,
+//               rounding, and bulk tensor stores through shared memory.
+// gemm_tc2_kernel<NH> runs on CTA pairs (cta_group::2, M = 256) with
+// 256 x 256 (NH = 1) or 256 x 512 (NH = 2) tiles; gemm_tc_kernel<256> on
+// single CTAs with 128 x 256 tiles, for local M <= 128.
+// Work units are (rank, m-tile, n-tile) or, fused, (group, m-tile, n-tile).
+// Fused, the G ranks' products of a reduction group accumulate in one fp32
+// TMEM accumulator, rank after rank in ascending order (one contraction over
+// the group's concatenated J); with the rank-order option each rank's
+// product is its own accumulator and the epilogue adds them in ascending
+// rank order in fp32, equal to the standalone reduction bit for bit.  Each
+// output tile is written once, to its owner (reduce-scatter) or to every
+// member (all-reduce).
 //
 // Every mbarrier wait is bounded (~2 s of SM clock); on expiry the kernel
 // raises an abort flag, records SHMM_ERR_TIMEOUT in the device status word,
