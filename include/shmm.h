@@ -336,7 +336,7 @@ shmm_status_t shmm_run(const shmm_plan_t *plan, const void *const *A_r, const vo
  * and its downloads overlap the next; consecutive stages' GEMMs alternate
  * between `stream` and a second compute stream, so they may overlap too.
  * A B box goes up whole at its first use, and its replicas are copied
- * right after it.
+ * right after it (the staged GEMMs read the uploaded box itself).
  * Copies and those GEMMs run on four library-owned streams of the current
  * device (uploads, replica copies, downloads, compute; created on first
  * use, kept until exit), ordered against `stream` by events: they start

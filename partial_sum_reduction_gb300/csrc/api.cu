@@ -747,9 +747,10 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
     std::vector<Replica> replicas;
     // B crosses the link whole at its first use.  The ranks holding replicas
     // of that box get their device copies right after it, on the replica
-    // stream, whatever stage they belong to; their GEMMs wait for their own
-    // copy's event only.  (Copying a replica in its own rank's stage held
-    // that stage's GEMM behind 0.47 GB of device copies.)
+    // stream, whatever stage they belong to.  Staged GEMMs read the uploaded
+    // box itself (b_read), so they never wait for a replica; one shmm_run
+    // over every rank waits for the copies.  (Copying a replica in its own
+    // rank's stage held that stage's GEMM behind 0.47 GB of device copies.)
     std::map<std::pair<int64_t, int64_t>, std::vector<int>> b_holders;
     if (B_host)
         for (int r = 0; r < p->nranks; ++r) {
@@ -762,6 +763,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
     };
     std::vector<EarlyCopy> early;
     std::vector<cudaEvent_t> b_ready(p->nranks, nullptr);
+    std::vector<const void *> b_read(B_r, B_r + p->nranks);  // the B buffer each rank's GEMM reads
     // Rows [r0, r1) of box b, and where they start in its dense buffer.
     auto rows_of = [](const shmm::Box &b, int64_t r0, int64_t r1) {
         shmm::Box s = b;
@@ -803,6 +805,7 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
                         if (!b_done[h]) {
                             b_done[h] = 1;
                             early.push_back({h, {static_cast<char *>(o.dev[h]) + at, dst, bytes}});
+                            b_read[h] = dst;
                         }
             } else {
                 replicas.push_back({dst, static_cast<const char *>(o.dev[it->second]) + at, bytes});
@@ -858,12 +861,13 @@ shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void
                 return finish(cuda_fail(fn, e, "replica copy"));
         }
         early.clear();
-        for (int r : ranks)  // every stage of a rank whose B is a device copy
-            if (b_ready[r] && (e = cudaStreamWaitEvent(gs, b_ready[r], 0)) != cudaSuccess)
-                return finish(cuda_fail(fn, e, "events"));
+        if (!staged)  // shmm_run reads every rank's own B
+            for (int r : ranks)
+                if (b_ready[r] && (e = cudaStreamWaitEvent(gs, b_ready[r], 0)) != cudaSuccess)
+                    return finish(cuda_fail(fn, e, "events"));
         if (staged) {
             UnitPtrs up;
-            shmm::GemmArgs ga = unit_args(p, (const void *const *)A_r, (const void *const *)B_r, C_r, u0, u1, &up);
+            shmm::GemmArgs ga = unit_args(p, (const void *const *)A_r, b_read.data(), C_r, u0, u1, &up);
             if (stg.block) {  // a block of rows: the same rows of every slot's A and C
                 ga.M = stg.r1 - stg.r0;
                 for (auto &a : up.a) a = static_cast<const char *>(a) + stg.r0 * Kd * in_b;
