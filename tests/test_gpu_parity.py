@@ -24,6 +24,21 @@ def s():
     return lib()
 
 
+# Tensor-core GEMM variants: CTA pairs with the launcher's tile width, CTA
+# pairs forced to 256 x 256 or 256 x 512 tiles, and single CTAs.
+KERNELS = ["pair", "pair_narrow", "pair_wide", "single"]
+
+
+def use_kernel(monkeypatch, kernel):
+    monkeypatch.setenv("SHMM_TC_PAIR", "0" if kernel == "single" else "1")
+    if kernel == "pair_narrow":
+        monkeypatch.setenv("SHMM_TC_WIDE", "0")
+    elif kernel == "pair_wide":
+        monkeypatch.setenv("SHMM_TC_WIDE", "1")
+    else:
+        monkeypatch.delenv("SHMM_TC_WIDE", raising=False)
+
+
 # ------------------------------------------------- split-K integer, {Y:2}
 
 @pytest.mark.parametrize("flags", [0, "FUSED", "SIMT", "FUSED|SIMT", "TREE"])
@@ -75,13 +90,13 @@ def test_worked_example_on_gpu(s, golden):
 
 # --------------------------------------------- local GEMM (tensor cores)
 
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("pair", KERNELS)
 @pytest.mark.parametrize("M,Kd,N", [(128, 64, 256), (300, 200, 328), (520, 1032, 264), (7, 16, 8),
                                     (256, 4096, 512), (129, 72, 1000), (700, 136, 600)])
 def test_local_gemm_partials(s, M, Kd, N, pair, monkeypatch):
     """Several tiles, ragged tails in all three dims, partial k-blocks; the
     CTA-pair kernel (256-row tiles, for M > 128) and the single-CTA kernel."""
-    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    use_kernel(monkeypatch, pair)
     from partial_sum_reduction_gb300 import helpers as H
     A, B = shmm_inputs.scaled_normal_pair(M, 2 * Kd, N, "bf16", seed=M + N)
     p = s.Plan(Y2, ((), ("Y",)), (("Y",), ()), ((), ()), M, 2 * Kd, N, "bf16", "bf16")
@@ -123,9 +138,9 @@ FOUR = [
 
 @pytest.mark.parametrize("case,sA,sB,sC", FOUR)
 @pytest.mark.parametrize("fused", [False, True])
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("pair", KERNELS)
 def test_four_cases(s, case, sA, sB, sC, fused, pair, monkeypatch):
-    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    use_kernel(monkeypatch, pair)
     A, B = shmm_inputs.scaled_normal_pair(512, 384, 640, "bf16", seed=case)
     plan, gpu = run_gpu(XY22, sA, sB, sC, A, B, "bf16", "bf16", s.FLAG_FUSED if fused else 0)
     assert plan.info.case_id == case
@@ -321,11 +336,11 @@ def test_operand_all_gather_bit_exact(s):
 
 # -------------------------------------------------------------- invariants
 
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("pair", KERNELS)
 def test_fused_equals_unfused_bitwise(s, pair, monkeypatch):
     """SHMM_FLAG_RANK_ORDER: the fused epilogue adds per-rank partials in
     ascending rank order, exactly the standalone sequential reduction."""
-    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    use_kernel(monkeypatch, pair)
     A, B = shmm_inputs.scaled_normal_pair(640, 1024, 512, "bf16", seed=12)
     for mesh, sA, sB, sC in ((Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ())),
                              (XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ())),
@@ -337,14 +352,14 @@ def test_fused_equals_unfused_bitwise(s, pair, monkeypatch):
             assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("pair", KERNELS)
 def test_accumulating_fusion_is_one_contraction(s, pair, monkeypatch):
     """Default fused path: a reduction group's products accumulate in one
     fp32 accumulator, k-block after k-block in ascending rank order -- the
     same tensor-core operations as one unsharded GEMM over the whole J, so
     every output element has the same bits (J_r a multiple of the 64-wide
     k-block, so block edges coincide)."""
-    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    use_kernel(monkeypatch, pair)
     A, B = shmm_inputs.scaled_normal_pair(640, 1024, 512, "bf16", seed=13)
     _, full = run_gpu([("Y", 1)], ((), ()), ((), ()), ((), ()), A, B, "bf16", "f32")
     full = full[0]
@@ -499,11 +514,11 @@ GATHERS = [
 
 
 @pytest.mark.parametrize("name,mesh,sA,sB,sC,I,J,K", GATHERS)
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("pair", KERNELS)
 def test_in_place_gather_equals_explicit_gather(s, name, mesh, sA, sB, sC, I, J, K, pair, monkeypatch):
     """Operands read from their owners' shards inside the GEMM give the same
     bits as all-gathering them first, and match the oracle."""
-    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    use_kernel(monkeypatch, pair)
     A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=I + J)
     p1, g1 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", 0)
     p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED | s.FLAG_RANK_ORDER)
@@ -628,7 +643,7 @@ def test_sequence_parallel_mlp_block(s, fused):
         assert np.abs(got - ref).max() <= BF16_TOL * np.abs(ref).max()
 
 
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("pair", KERNELS)
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("mesh,sA,sB,sC,I,J,K", [
     (Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), 300, 2000, 264),          # J_r = 1000 = 15 k-blocks + 40
@@ -638,7 +653,7 @@ def test_ragged_contraction(s, pair, fused, mesh, sA, sB, sC, I, J, K, monkeypat
     """Per-rank contraction lengths that are not a multiple of the 64-wide
     k-block (the last block is zero-filled by TMA), with ragged M and N, on
     both GEMM kernels, fused and unfused, against the oracle."""
-    monkeypatch.setenv("SHMM_TC_PAIR", pair)
+    use_kernel(monkeypatch, pair)
     A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=I + K)
     plan, gpu = run_gpu(mesh, sA, sB, sC, A, B, "bf16", "f32", s.FLAG_FUSED if fused else 0)
     assert plan.info.tensor_core == 1
