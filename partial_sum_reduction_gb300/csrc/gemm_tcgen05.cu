@@ -942,7 +942,52 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                     const bool into_s = q == 0 || k.accum;
                     const int b = into_s ? bS : (bS ^ 1);
                     const bool fresh = q == 0 || !k.accum;  // this product starts its buffers
-                    for (int kb = 0; kb < k.k_blocks && ok; ++kb, ++it) {
+                    int kb = 0;
+                    if (NH == 2 && fresh) {
+                        // Half 0 runs ahead over the first R loaded stages while the
+                        // epilogue still drains half 1 of the previous tile, then half 1
+                        // catches up on the same stages; each half still adds its
+                        // k-blocks in ascending order.
+                        auto issue = [&](int st, int h) {
+                            const uint32_t a_addr = smem_u32(tiles + st * C::STAGE);
+                            const uint32_t b_addr = a_addr + C::A_BYTES;
+                            const uint32_t d_tmem = tmem_base + (uint32_t)((b + h) * BN);
+#pragma unroll
+                            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                                const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
+                                const uint64_t bd = smem_desc(b_addr + h * 16384 + kk * 2048, 8192, 1024);
+                                umma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        };
+                        const int R = k.k_blocks < S ? k.k_blocks : S;
+                        if (!mbar_wait(acce_bar(b), (fills[b] & 1) ^ 1, abort_flag, k.status)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+                        for (kb = 0; kb < R; ++kb) {
+                            const uint32_t u = it + (uint32_t)kb;
+                            if (!mbar_wait(full_bar((int)(u % S)), (u / S) & 1, abort_flag, k.status)) {
+                                ok = false;
+                                break;
+                            }
+                            fence_after();
+                            issue((int)(u % S), 0);
+                        }
+                        if (!ok) break;
+                        if (!mbar_wait(acce_bar(b + 1), (fills[b + 1] & 1) ^ 1, abort_flag, k.status)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+                        for (kb = 0; kb < R; ++kb) {
+                            const int st = (int)((it + (uint32_t)kb) % S);
+                            issue(st, 1);
+                            umma2_commit_both(empty_bar(st));
+                        }
+                        it += (uint32_t)R;
+                    }
+                    for (; kb < k.k_blocks && ok; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(full_bar(s), ph, abort_flag, k.status)) {
@@ -1204,15 +1249,14 @@ bool pair_kernel_enabled() {
 // hold its MMAs back (its tensor pipe alone, fed from stale shared memory,
 // runs 1.13x faster; with a quarter of its loads removed, 1.12x).  But a
 // wide tile fills TMEM, so each tile boundary idles the tensor pipe while
-// the epilogue drains (about 8 k cycles, some six wide k-blocks); and wide
-// tiles halve the tile count, so a launch of few tiles can lose more to its
-// last partial wave.  Measured on 8192^2 x K products (same wave counts),
-// wide / narrow time = 0.86 (1 + 6 / k-blocks per tile): 1.02 at K = 2048,
-// 0.94 at 4096, 0.91 at 8192, 0.88 at 16384.  A GeLU epilogue drains
-// slower: the MLP's first matmul (64 k-blocks) ran no faster wide, so it
-// counts ten k-blocks.  Pick the smaller estimate: waves x work per tile x
-// that factor.  SHMM_TC_WIDE=0 / 1 forces 256- / 512-column tiles (tests
-// compare them).
+// the epilogue drains half 0 (half 0 of the next tile then runs ahead over
+// the loaded stages while half 1 drains); and wide tiles halve the tile
+// count, so a launch of few tiles can lose more to its last partial wave.
+// Measured on 8192^2 x K products (same wave counts), wide / narrow time =
+// 0.88 (1 + 4 / k-blocks per tile): 0.99 at K = 2048, 0.93 at 4096, 0.91 at
+// 16384 (the MLP's GeLU matmul, 64 k-blocks: 0.98 across 27 and 14 waves).
+// Pick the smaller estimate: waves x work per tile x that factor.
+// SHMM_TC_WIDE=0 / 1 forces 256- / 512-column tiles (tests compare them).
 int pair_halves(const TcK &k) {
     if (k.fused && !k.accum && k.G > 1) return 1;  // the rank-order fold needs TMEM's second buffer
     const char *env = getenv("SHMM_TC_WIDE");
@@ -1227,7 +1271,7 @@ int pair_halves(const TcK &k) {
     const int64_t t2 = (int64_t)k.units * m_t * ((k.N + 511) / 512);
     const double kb = (double)k.k_blocks * (k.fused && k.accum ? k.G : 1);  // k-blocks per tile
     const double narrow = (double)((t1 + cap1 - 1) / cap1);
-    const double wide = (double)((t2 + cap2 - 1) / cap2) * 2.0 * 0.86 * (1.0 + (k.gelu ? 10.0 : 6.0) / kb);
+    const double wide = (double)((t2 + cap2 - 1) / cap2) * 2.0 * 0.88 * (1.0 + 4.0 / kb);
     return wide < narrow ? 2 : 1;
 }
 
