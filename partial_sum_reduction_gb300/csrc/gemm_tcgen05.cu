@@ -942,29 +942,38 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                     const bool into_s = q == 0 || k.accum;
                     const int b = into_s ? bS : (bS ^ 1);
                     const bool fresh = q == 0 || !k.accum;  // this product starts its buffers
+                    // The four K=16 MMAs of the k-block in stage st into buffer
+                    // buf, half h of the stage's B; `first` starts the buffer's
+                    // sum instead of adding to it.
+                    auto issue = [&](int st, int buf, int h, bool first) {
+                        const uint32_t a_addr = smem_u32(tiles + st * C::STAGE);
+                        const uint32_t b_addr = a_addr + C::A_BYTES + (uint32_t)(h * 16384);
+                        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
+                            const uint64_t bd = smem_desc(b_addr + kk * 2048, 8192, 1024);
+                            umma2_f16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
+                        }
+                    };
+                    // A fresh buffer waits until the epilogue has handed back
+                    // its previous fill.
+                    auto wait_free = [&](int buf) -> bool {
+                        if (!mbar_wait(acce_bar(buf), (fills[buf] & 1) ^ 1, abort_flag, k.status)) return false;
+                        fence_after();
+                        return true;
+                    };
                     int kb = 0;
                     if (NH == 2 && fresh) {
                         // Half 0 runs ahead over the first R loaded stages while the
                         // epilogue still drains half 1 of the previous tile, then half 1
                         // catches up on the same stages; each half still adds its
                         // k-blocks in ascending order.
-                        auto issue = [&](int st, int h) {
-                            const uint32_t a_addr = smem_u32(tiles + st * C::STAGE);
-                            const uint32_t b_addr = a_addr + C::A_BYTES;
-                            const uint32_t d_tmem = tmem_base + (uint32_t)((b + h) * BN);
-#pragma unroll
-                            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                                const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
-                                const uint64_t bd = smem_desc(b_addr + h * 16384 + kk * 2048, 8192, 1024);
-                                umma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                            }
-                        };
                         const int R = k.k_blocks < S ? k.k_blocks : S;
-                        if (!mbar_wait(acce_bar(b), (fills[b] & 1) ^ 1, abort_flag, k.status)) {
+                        if (!wait_free(b)) {
                             ok = false;
                             break;
                         }
-                        fence_after();
                         for (kb = 0; kb < R; ++kb) {
                             const uint32_t u = it + (uint32_t)kb;
                             if (!mbar_wait(full_bar((int)(u % S)), (u / S) & 1, abort_flag, k.status)) {
@@ -972,17 +981,15 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                                 break;
                             }
                             fence_after();
-                            issue((int)(u % S), 0);
+                            issue((int)(u % S), b, 0, kb == 0);
                         }
-                        if (!ok) break;
-                        if (!mbar_wait(acce_bar(b + 1), (fills[b + 1] & 1) ^ 1, abort_flag, k.status)) {
+                        if (!ok || !wait_free(b + 1)) {
                             ok = false;
                             break;
                         }
-                        fence_after();
                         for (kb = 0; kb < R; ++kb) {
                             const int st = (int)((it + (uint32_t)kb) % S);
-                            issue(st, 1);
+                            issue(st, b + 1, 1, kb == 0);
                             umma2_commit_both(empty_bar(st));
                         }
                         it += (uint32_t)R;
@@ -995,26 +1002,13 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                             break;
                         }
                         fence_after();
-                        const uint32_t a_addr = smem_u32(tiles + s * C::STAGE);
-                        const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
                         for (int h = 0; h < NH; ++h) {
-                            // a fresh buffer: the epilogue has handed back its previous fill
-                            // (half 0 of the next wide tile starts while half 1 drains)
-                            if (kb == 0 && fresh) {
-                                if (!mbar_wait(acce_bar(b + h), (fills[b + h] & 1) ^ 1, abort_flag, k.status)) {
-                                    ok = false;
-                                    break;
-                                }
-                                fence_after();
+                            if (kb == 0 && fresh && !wait_free(b + h)) {  // 256x256 tiles only
+                                ok = false;
+                                break;
                             }
-                            const uint32_t d_tmem = tmem_base + (uint32_t)((b + h) * BN);
-#pragma unroll
-                            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                                const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
-                                const uint64_t bd = smem_desc(b_addr + h * 16384 + kk * 2048, 8192, 1024);
-                                umma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0 || (q > 0 && k.accum)) ? 1u : 0u);
-                            }
+                            issue(s, b + h, h, kb == 0 && !(q > 0 && k.accum));
                         }
                         if (!ok) break;
                         umma2_commit_both(empty_bar(s));
