@@ -79,6 +79,19 @@ def test_bounds_checked_build_exports_every_declared_symbol(shmm):
     assert ctypes.CDLL(build.LIB).shmm_bounds_checked() == 0
 
 
+def test_every_environment_knob_is_documented():
+    """Each variable the library reads with getenv is described in the
+    header, so a user of the C ABI alone can find it."""
+    import glob
+    header = open(os.path.join(ROOT, "include", "shmm.h")).read()
+    used = set()
+    for f in glob.glob(os.path.join(ROOT, "partial_sum_reduction_gb300", "csrc", "*")):
+        used |= set(re.findall(r'getenv\("(SHMM_[A-Z_]+)"\)', open(f).read()))
+    assert used >= {"SHMM_TC_PAIR", "SHMM_TC_WIDE", "SHMM_INJECT_FAIL"}
+    for name in used:
+        assert name in header, name
+
+
 def test_binding_fails_loudly_without_library(monkeypatch):
     import partial_sum_reduction_gb300.shmm as m
     monkeypatch.setattr(m, "_lib", None)
