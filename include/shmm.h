@@ -436,7 +436,10 @@ shmm_status_t shmm_choose_operand(int64_t B, int64_t D, int64_t F, int axis_size
  *     are rejected with SHMM_ERR_NOMEM before anything is enqueued.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  Host threads may make first calls at the
+ *     same time.  The address stays cached for the process, so reset no
+ *     device (cudaDeviceReset) while the library is in use; devices with an
+ *     index of 64 or more are rejected with SHMM_ERR_CUDA.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents; nothing in it needs to start at zero (each use
  *     writes every byte it later reads).  Calls that overlap on the GPU

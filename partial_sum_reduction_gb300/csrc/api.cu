@@ -29,45 +29,51 @@ static __device__ __align__(256) unsigned char g_shmm_static_workspace[SHMM_STAT
 
 namespace {
 
-int *status_ptr(std::string *err) {
-    static int *cached[64] = {};
+// The current device, or -1 with a message in *err.
+int current_device(std::string *err) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        *err = "no CUDA device";
-        return nullptr;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return -1;
     }
-    if (!cached[dev]) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_shmm_status_word);
-        if (e != cudaSuccess) {
-            *err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
-            return nullptr;
-        }
-        cached[dev] = static_cast<int *>(p);
+    if (dev < 0 || dev >= shmm::kMaxDevices) {
+        *err = "device " + std::to_string(dev) + " is beyond the " + std::to_string(shmm::kMaxDevices) +
+               " devices this library supports";
+        return -1;
     }
-    return cached[dev];
+    return dev;
 }
 
-// Device address of g_shmm_static_workspace on the current device.  Host
-// code cannot use the array's name as a device pointer, so the address is
-// looked up once per device (with that device current) and cached.
-void *static_workspace_ptr(std::string *err) {
-    static void *cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        *err = "no CUDA device";
+// Device address of a __device__ variable on the current device.  Host code
+// cannot use the variable's name as a device pointer, so the address is
+// looked up once per device (with that device current) and cached; after a
+// cudaDeviceReset the cached address is stale, so reset no device while
+// this library is in use.
+template <typename T>
+void *symbol_ptr(shmm::PerDevice<void *> &cache, const T &symbol, std::string *err) {
+    const int dev = current_device(err);
+    if (dev < 0) return nullptr;
+    void *p = cache.get(dev);
+    if (p) return p;
+    const cudaError_t e = cudaGetSymbolAddress(&p, symbol);
+    if (e != cudaSuccess) {
+        *err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
         return nullptr;
     }
-    if (!cached[dev]) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_shmm_static_workspace);
-        if (e != cudaSuccess) {
-            *err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
-            return nullptr;
-        }
-        cached[dev] = p;
-    }
-    return cached[dev];
+    cache.set(dev, p);
+    return p;
+}
+
+int *status_ptr(std::string *err) {
+    static shmm::PerDevice<void *> cache;
+    return static_cast<int *>(symbol_ptr(cache, g_shmm_status_word, err));
+}
+
+// Address of g_shmm_static_workspace on the current device.
+void *static_workspace_ptr(std::string *err) {
+    static shmm::PerDevice<void *> cache;
+    return symbol_ptr(cache, g_shmm_static_workspace, err);
 }
 
 // A wait on an mbarrier that nothing ever arrives at, through the same
@@ -629,6 +635,7 @@ shmm_status_t shmm_run_static_workspace(const shmm_plan_t *p, const void *const 
                                         const void *const *B_r, void *const *C_r, void *stream) {
     static const char *fn = "shmm_run_static_workspace";
     shmm::clear_error();
+    shmm::Range range(fn);
     if (!p) return fail(SHMM_ERR_NULL, std::string(fn) + ": plan is NULL");
     if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
     size_t need = 0;

@@ -237,6 +237,36 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Bounded wait whose success makes the releasing side's earlier writes
+// (from any CTA of the cluster) visible: for hand-offs between the pair.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int *status) {
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > kWaitLimit) {
+            atomicExch(status, (int)SHMM_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Counts `bytes` as arrived on a barrier of this CTA without a copy.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair (here: the leader's).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
@@ -806,6 +836,10 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
     // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    // The peer producer's final load count, handed to the leader through
+    // handoff_bar (both used in the leader CTA only).
+    volatile uint32_t *peer_issued = tmem_holder + 2;
+    uint64_t *handoff = reinterpret_cast<uint64_t *>(tmem_holder + 4);
     // In-place gathers only: block -> shard-map tables, copied once from the
     // parameters into the shared-memory tail (a byte load from the parameter
     // block on every TMA issue stalls the producer).
@@ -819,6 +853,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t cr = cluster_ctarank();  // 0: leader, 1: peer
+    const uint32_t handoff_bar = smem_u32(handoff);
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int Gq = k.fused ? k.G : 1;
     const int tiles_per_unit = k.m_tiles * k.n_tiles;  // 256 x TW tiles
@@ -840,7 +875,9 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
             mbar_init(acce_bar(s), 2 * C::EPI_WARPS * 32);  // both CTAs' epilogue threads
         }
         mbar_init(drain_bar, 1);
+        mbar_init(handoff_bar, 1);
         *abort_flag = 0;
+        *peer_issued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -864,9 +901,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
         if (lane == 0) {
             for (int i = 0; i < k.n_maps_a; ++i) prefetch_map(&k.tmA[i]);
             for (int i = 0; i < k.n_maps_b; ++i) prefetch_map(&k.tmB[i]);
-            uint32_t it = 0;
-            int last_parity[8];
-            for (int s = 0; s < 8; ++s) last_parity[s] = -1;
+            uint32_t it = 0;  // stages loaded
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
                 int unit, mt, nt;
@@ -911,18 +946,34 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                                                      b_r);
                                 }
                         }
-                        last_parity[s] = (int)ph;
                     }
                 }
             }
-            if (cr == 0) {
-                // both CTAs' loads of a stage complete on the leader's barrier
-                for (int s = 0; s < S; ++s)
-                    if (last_parity[s] >= 0)
-                        mbar_wait(full_bar(s), (uint32_t)last_parity[s], abort_flag, k.status, false);
-            } else if (!ok) {
-                // aborted: let this CTA's own loads land before it can exit
-                for (int i = 0; i < 200; ++i) __nanosleep(1000);
+            // Both CTAs' loads of a stage complete on the leader's barrier, so
+            // the leader alone can tell when every load of the pair has
+            // landed; the peer cannot leave before it does (the cluster
+            // barrier at the end).  The peer hands over how many stages it
+            // loaded.  Without an abort both CTAs loaded the same stages; after
+            // one they may differ by up to S stages (each loads stage i only
+            // after the MMAs freed stage i - S, which needed the leader to
+            // have armed it): the leader arms the peer's extra stages for the
+            // peer's half, and stands in for the half the peer never loaded,
+            // so every stage's last phase completes once the loads that were
+            // issued have landed.
+            if (cr == 1) {
+                st_cluster_u32(mapa_shared(smem_u32((const void *)peer_issued), 0), it);
+                mbar_arrive_cluster(mapa_shared(handoff_bar, 0));
+            } else {
+                uint32_t it_peer = it;
+                if (mbar_wait_cluster(handoff_bar, 0, k.status)) it_peer = *peer_issued;
+                const uint32_t it_max = it_peer > it ? it_peer : it;
+                for (uint32_t i = it_peer < it ? it_peer : it; i < it_max; ++i) {
+                    const int s = (int)(i % S);
+                    if (i >= it) mbar_expect_tx(full_bar(s), C::STAGE);  // the peer's half only
+                    else mbar_complete_tx(full_bar(s), C::STAGE);        // the half never loaded
+                }
+                for (uint32_t i = it_max > (uint32_t)S ? it_max - S : 0; i < it_max; ++i)
+                    mbar_wait(full_bar((int)(i % S)), (i / S) & 1, abort_flag, k.status, false);
             }
         }
     } else if (warp == 1) {
@@ -1136,27 +1187,28 @@ bool cached_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, int64_t rows
 }
 
 int num_sms() {
-    static int cached[64] = {};
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        n = 148;
-    if (dev >= 0 && dev < 64) cached[dev] = n;
+    static shmm::PerDevice<int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= shmm::kMaxDevices) return 148;
+    int n = cache.get(dev);
+    if (n) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache.set(dev, n);
     return n;
 }
 
 template <int BN>
 cudaError_t launch_bn(TcK &k, cudaStream_t s) {
     using C = Cfg<BN>;
-    static bool attr_set[64] = {};
+    static shmm::PerDevice<int> attr_set;
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= shmm::kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set.get(dev)) {
+        e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set.set(dev, 1);
     }
     k.n_tiles = (int)((k.N + BN - 1) / BN);
     const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;

@@ -4,6 +4,7 @@
 
 #include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -11,6 +12,18 @@
 #include "shmm.h"
 
 namespace shmm {
+
+// A value per CUDA device, looked up once with that device current and kept
+// for the life of the process.  Host threads may make their first calls on a
+// device at the same time: each may look the value up, and every one stores
+// the same value, through atomics.  Devices 0 .. kMaxDevices-1 only.
+constexpr int kMaxDevices = 64;
+template <typename T>
+struct PerDevice {
+    std::atomic<T> slot[kMaxDevices];
+    T get(int dev) const { return slot[dev].load(std::memory_order_acquire); }
+    void set(int dev, T v) { slot[dev].store(v, std::memory_order_release); }
+};
 
 // Ordered list of mesh axis indices splitting one array dim (first = major).
 struct AxisList {

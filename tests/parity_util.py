@@ -16,6 +16,17 @@ def lib():
     return s
 
 
+def tile_rows(n_rows, tile=256, salt=0):
+    """One output row in every ``tile``-row block of [0, n_rows), at an
+    offset inside the block that changes from block to block (so both
+    128-row halves of a CTA pair's tile and every lane quadrant are hit over
+    the blocks), plus the first and last rows."""
+    rows = {0, n_rows - 1}
+    for t in range((n_rows + tile - 1) // tile):
+        rows.add(min(n_rows - 1, t * tile + (t * 89 + 37 * salt + 3) % tile))
+    return sorted(rows)
+
+
 def run_gpu(mesh, sA, sB, sC, A, B, in_dtype, out_dtype, flags=0, fill=float("nan")):
     """A, B: global CPU tensors in the input dtype.  Returns (plan, per-rank
     CPU outputs)."""

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import shmm_inputs
-from parity_util import BF16_TOL, F32P_TOL, compare, lib, oracle_run, run_gpu
+from parity_util import BF16_TOL, F32P_TOL, compare, lib, oracle_run, run_gpu, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -154,7 +154,7 @@ def test_four_cases_full_size_sampled(s, case, sA, sB, sC):
     rank's block is checked against the oracle."""
     A, B = shmm_inputs.scaled_normal_pair(2048, 2048, 2048, "bf16", seed=0)
     plan, gpu = run_gpu(XY22, sA, sB, sC, A, B, "bf16", "bf16", s.FLAG_FUSED)
-    rows = list(range(0, 2048, 97)) + [1023, 1024, 2047]
+    rows = sorted(set(tile_rows(2048, tile=128, salt=case) + [1023, 1024]))
     _, ores = oracle_run(XY22, sA, sB, sC, A, B, "bf16", rows=rows)
     compare(plan, gpu, ores, exact=False, rows=rows)
 
@@ -179,7 +179,9 @@ def test_down_projection_full_size_sampled(s):
     A, B = shmm_inputs.scaled_normal_pair(8192, 28672, 8192, "bf16", seed=0)
     sA, sB, sC = (("X",), ("Y",)), (("Y",), ()), (("X",), ())
     plan, gpu = run_gpu(XY42, sA, sB, sC, A, B, "bf16", "bf16", s.FLAG_FUSED)
-    rows = [0, 1, 2047, 2048, 4100, 6143, 6144, 8191]
+    # one row in every 256-row m-tile of every rank block (32 tiles), at a
+    # varying offset, plus the rank-block edges
+    rows = sorted(set(tile_rows(8192) + [2047, 2048, 6143, 6144]))
     _, ores = oracle_run(XY42, sA, sB, sC, A, B, "bf16", rows=rows)
     compare(plan, gpu, ores, exact=False, rows=rows)
 
@@ -235,7 +237,9 @@ def test_mlp_pair_small(s, sY, fused):
 @pytest.mark.slow
 @pytest.mark.parametrize("sY", [((), ()), (("X",), ())])
 def test_mlp_pair_full_size_sampled(s, sY):
-    _mlp(s, 8192, 4096, 16384, sY, True, rows=[0, 1, 1023, 1024, 5000, 8191])
+    # one token row in every 256-row m-tile of both matmuls (32 tiles), at a
+    # varying offset, plus the reduce-scatter block edges
+    _mlp(s, 8192, 4096, 16384, sY, True, rows=sorted(set(tile_rows(8192, salt=1) + [1023, 1024])))
 
 
 # -------------------------------------------- collectives on given partials
@@ -300,6 +304,55 @@ def test_collectives_scalar_path(s, G, dtype, order):
     for q in range(G):
         np.testing.assert_array_equal(rs[q].float().cpu().numpy(), ref_rs[q])
         np.testing.assert_array_equal(ar[q].float().cpu().numpy(), ref_ar[q])
+
+
+def _bits_equal(got, ref, what):
+    """Bit-for-bit equality of fp32 arrays (so +0 and -0 differ too)."""
+    g = np.ascontiguousarray(got, dtype=np.float32).view(np.uint32)
+    r = np.ascontiguousarray(ref, dtype=np.float32).view(np.uint32)
+    assert g.shape == r.shape, what
+    bad = np.flatnonzero(g.ravel() != r.ravel())
+    assert bad.size == 0, "%s: %d elements differ, first at %d" % (what, bad.size, bad[0])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_collectives_at_one_gib_per_rank(s, dtype):
+    """Two ranks with 1 GiB partial buffers each, the largest size of the
+    collective sweep, through the same launchers and grids the benchmark
+    times: reduce-scatter over rows, all-reduce, and the all-gather of the
+    owner blocks, bit for bit against the oracle's sequential rank sum."""
+    from partial_sum_reduction_gb300 import helpers as H
+    G, eb = 2, (4 if dtype == "f32" else 2)
+    numel = (1 << 30) // eb
+    cols = 4096
+    rows = numel // cols
+    bufs = [b.reshape(rows, cols) for b in shmm_inputs.partial_buffers(G, numel, dtype, seed=30)]
+    mesh = [("X", G)]
+    fl = s.FLAG_PARTIAL_OUT_DTYPE
+    p_rs = s.Plan(mesh, ((), ("X",)), (("X",), ()), (("X",), ()), rows, G, cols, dtype, dtype, fl)
+    p_ar = s.Plan(mesh, ((), ("X",)), (("X",), ()), ((), ()), rows, G, cols, dtype, dtype, fl)
+    pg = s.Plan(mesh, (("X",), ()), ((), ()), ((), ()), rows, 8, cols, dtype, dtype)
+    P_r = [b.cuda() for b in bufs]
+    rs = H.alloc(p_rs, s.TENSOR_C, fill=float("nan"))
+    p_rs.reduce_scatter(P_r, rs)
+    ar = H.alloc(p_ar, s.TENSOR_C, fill=float("nan"))
+    p_ar.all_reduce(P_r, ar)
+    ag = H.alloc(pg, s.TENSOR_C, fill=float("nan"))
+    pg.all_gather(s.TENSOR_C, rs, ag)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    del P_r
+    host = [b.float().numpy() for b in bufs]
+    del bufs
+    ref = oracle.collective_reduce(host, "reduce_scatter", dtype)
+    for q in range(G):
+        _bits_equal(rs[q].float().cpu().numpy(), ref[q], "reduce-scatter owner %d" % q)
+    del ref
+    ref = oracle.collective_reduce(host, "all_reduce", dtype)[0]
+    for q in range(G):
+        _bits_equal(ar[q].float().cpu().numpy(), ref, "all-reduce member %d" % q)
+        _bits_equal(ag[q].float().cpu().numpy(), ref, "all-gather member %d" % q)
 
 
 @pytest.mark.parametrize("G", [2, 4])

@@ -79,6 +79,56 @@ def test_worked_example_payload_bytes():
     assert ar["total"] == g["payload_bytes_total"]
 
 
+# Operand all-gather payload, counted by hand at the sender ("Sharded matrix
+# multiplication and result ownership", Engineering example: a sent payload
+# counts once; "Sharding Matrix Multiply", AllGather: every member ends with
+# the whole operand, so each rank sends its own shard to the G-1 others).
+# I = J = K = 2048, bf16 (2 bytes).
+OPERAND_AG_BY_HAND = [
+    # case 2 on {X:2,Y:2}: A[I,J_X] -> shard [2048,1024] = 4 MiB, one peer
+    (XY22, ((), ("X",)), ((), ()), ((), ()), 2048 * 1024 * 2 * 1),
+    # case 4 on {X:2,Y:2}: B[J,K_X] -> shard [2048,1024] = 4 MiB, one peer
+    (XY22, (("X",), ()), ((), ("X",)), (("X",), ()), 2048 * 1024 * 2 * 1),
+    # case 2 on {X:4,Y:2}: A[I,J_X] -> shard [2048,512] = 2 MiB, three peers
+    (XY42, ((), ("X",)), ((), ()), ((), ()), 2048 * 512 * 2 * 3),
+    # case 2, both operands J-sharded on different axes: A[I,J_X] shard
+    # [2048,1024] to one X peer, B[J_Y,K] shard [1024,2048] to one Y peer
+    (XY22, ((), ("X",)), (("Y",), ()), ((), ()), 2048 * 1024 * 2 + 1024 * 2048 * 2),
+    # case 3 with case 4's gather: B[J_Y,K_X] shard [1024,1024] = 2 MiB,
+    # gathered over X along K to one peer; A[I_X,J_Y] is not moved
+    (XY22, (("X",), ("Y",)), (("Y",), ("X",)), (("X",), ()), 1024 * 1024 * 2 * 1),
+]
+
+
+@pytest.mark.parametrize("mesh,sA,sB,sC,expected", OPERAND_AG_BY_HAND)
+def test_operand_all_gather_payload_by_hand(mesh, sA, sB, sC, expected):
+    pay = oracle.payload_bytes(mesh, sA, sB, sC, 2048, 2048, 2048, "bf16", "bf16")
+    assert pay["operand_all_gather"] == expected
+
+
+@pytest.mark.parametrize("mesh,sA,sB,sC,expected", OPERAND_AG_BY_HAND)
+def test_operand_all_gather_payload_counted_at_the_receivers(mesh, sA, sB, sC, expected):
+    """The same bytes counted the other way, on small shapes: every element a
+    rank holds after the gather but not before was received from a peer, and
+    every byte received was sent once, so the total over ranks must equal N
+    times the per-rank sent payload."""
+    I, J, K = 8, 16, 24
+    N = oracle.mesh_size(mesh)
+    plan = oracle.plan_matmul(mesh, sA, sB, sC)
+    received = 0
+    for before, after, shape in ((sA, plan.local_A, (I, J)), (sB, plan.local_B, (J, K))):
+        for r in range(N):
+            (b0, b1), (bn0, bn1) = oracle.shard_box(mesh, before, shape, r)
+            (a0, a1), (an0, an1) = oracle.shard_box(mesh, after, shape, r)
+            for i in range(a0, a0 + an0):
+                for j in range(a1, a1 + an1):
+                    if not (b0 <= i < b0 + bn0 and b1 <= j < b1 + bn1):
+                        received += 2
+    pay = oracle.payload_bytes(mesh, sA, sB, sC, I, J, K, "bf16", "bf16")
+    assert pay["operand_all_gather"] * N == received
+    assert received > 0
+
+
 def test_concatenating_partials_is_not_the_result():
     g = load_golden("p2_worked_example.txt")
     cat = np.concatenate([np.array(g["partial_rank0"]), np.array(g["partial_rank1"])])
