@@ -35,6 +35,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("sharded-matmul TFLOP/s (% bf16 peak) and reduce-scatter GB/s (% HBM) on 1 GB300")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# device-side delay (SM cycles, ~0.1 ms) enqueued before a timed collective
+SLEEP_CYCLES = 200000
+L2_BYTES = 129 << 20
 # datasheet figures of one GB300, reported beside the measured denominators
 NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
@@ -77,7 +80,7 @@ FOUR_CASES = [
 #       -k regex:gemm_tc2 -s 3 -c 1 python bench.py --steps 5 --warmup 3 --no-cpu-baseline),
 # valid only for the kernel code it was taken on (kernel_source_hash).
 NCU_TRAFFIC = {
-    "down_projection": {"kernel_sha256_16": "df34699dd43de0c3", "bytes": 3.701169664e9 + 0.243414784e9,
+    "down_projection": {"kernel_sha256_16": "00e3a1f8014c8bef", "bytes": 3.472135424e9 + 0.243932416e9,
                         "kernel": "gemm_tc2_kernel<2> (256x512 tiles)"},
 }
 
@@ -192,7 +195,7 @@ class Workload:
     """Plans, per-rank device buffers and pinned host copies of one workload;
     ``step()`` enqueues one pass of the hot path."""
 
-    def __init__(self, name, device):
+    def __init__(self, name, device, rank_order=False, sm_split=True):
         import torch
         import partial_sum_reduction_gb300 as s
         import shmm_inputs
@@ -202,22 +205,38 @@ class Workload:
         c = self.cfg
         self.steps_spec = []   # (plan, A list, B list, C list, ws)
         self.flops = 0
+        FUSED = s.FLAG_FUSED | (s.FLAG_RANK_ORDER if rank_order else 0)
         if name in ("down_projection", "down_projection_quarter"):
             A, B = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
             self.host_globals = (A, B)
-            self._add(c["mesh"], c["sA"], c["sB"], c["sC"], A, B, s.FLAG_FUSED if c["fused"] else 0, device)
+            self._add(c["mesh"], c["sA"], c["sB"], c["sC"], A, B, FUSED if c["fused"] else 0, device)
         elif name == "four_case":
             A, B = shmm_inputs.scaled_normal_pair(c["I"], c["J"], c["K"], "bf16", seed=0)
             self.host_globals = (A, B)
             for sA, sB, sC in FOUR_CASES:
-                self._add(c["mesh"], sA, sB, sC, A, B, s.FLAG_FUSED, device)
+                self._add(c["mesh"], sA, sB, sC, A, B, FUSED, device)
+            # The four cases are independent and run on their own streams.
+            # Each alone is 1-2 waves of tiles and would take every SM with a
+            # partial last wave, so the GPU is split among them by their
+            # share of the FLOPs (whole CTA pairs, at least one each): the
+            # four then run side by side and end together.
+            self.sm_split = None
+            if sm_split:
+                sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+                fl = [p.info.flops_per_rank * p.nranks for p, *_ in self.steps_spec]
+                pairs = [max(1, int(round(sms // 2 * f / sum(fl)))) for f in fl]
+                while sum(pairs) > sms // 2:
+                    pairs[pairs.index(max(pairs))] -= 1
+                self.sm_split = [2 * n for n in pairs]
+                for (p, *_), n in zip(self.steps_spec, self.sm_split):
+                    p.set_sm_limit(n)
         elif name == "mlp_pair":
             X, W1, W2 = shmm_inputs.mlp_pair(c["T"], c["D"], c["F"], seed=0)
             self.host_globals = (X, W1, W2)
             p1 = self._add(c["mesh"], ((), ()), ((), ("X",)), ((), ("X",)), X, W1, s.FLAG_GELU, device)
             H_r = self.steps_spec[0][3]
             p2 = s.Plan(c["mesh"], ((), ("X",)), (("X",), ()), ((), ()), c["T"], c["F"], c["D"], "bf16", "bf16",
-                        s.FLAG_FUSED)
+                        FUSED)
             W2_r = H.shard(p2, s.TENSOR_B, W2, device)
             Y_r = H.alloc(p2, s.TENSOR_C, device)
             self.steps_spec.append((p2, H_r, W2_r, Y_r, H.workspace(p2, device)))
@@ -228,7 +247,7 @@ class Workload:
             self._add(c["mesh"], ((), ()), ((), ("X",)), ((), ("X",)), X, W1, s.FLAG_GELU, device)
             H_r = self.steps_spec[0][3]
             p2 = s.Plan(c["mesh"], ((), ("X",)), (("X",), ()), (("X",), ()), c["T"], c["F"], c["D"], "bf16",
-                        "bf16", s.FLAG_FUSED)
+                        "bf16", FUSED)
             W2_r = H.shard(p2, s.TENSOR_B, W2, device)
             Y_r = H.alloc(p2, s.TENSOR_C, device)
             self.steps_spec.append((p2, H_r, W2_r, Y_r, H.workspace(p2, device)))
@@ -240,7 +259,7 @@ class Workload:
         elif name == "split_k_integer":
             A, B = shmm_inputs.split_k_integer(c["I"], c["J"], c["K"], seed=0)
             self.host_globals = (A, B)
-            self._add(c["mesh"], ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, s.FLAG_FUSED, device,
+            self._add(c["mesh"], ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, FUSED, device,
                       dt="f32")
         torch.cuda.synchronize()
 
@@ -457,41 +476,60 @@ def time_e2e(wl, steps, dist_ctx, windows=5):
     return per_window, h2d, d2h
 
 
-def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False):
+def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False, stream_rate=True):
     """Bandwidth of one standalone collective on {X:G} partial buffers of
-    ``mib`` MiB per rank (the full logical array V per rank)."""
-    import shmm_inputs
+    ``mib`` MiB per rank (the full logical array V per rank).
+
+    Two timings.  ``ms_median``: one launch at a time, L2 flushed before each,
+    the device kept busy while the host enqueues it, so the events bracket
+    one collective's device time including its launch.  ``stream_ms``: the
+    collective over rotating buffer sets (together more than twice the L2,
+    so no launch finds its inputs in L2 from an earlier one), launched back to
+    back from a captured CUDA graph; the time per launch is the rate a stream
+    of collectives sustains, with each launch's start overlapping the
+    previous one's end.  CUDA events on this GPU tick in steps of about 2 us,
+    which a graph of 32 or more launches averages out."""
     eb = 4 if dtype == "f32" else 2
-    numel = mib * (1 << 20) // eb
-    cols = 4096
+    numel = int(mib * (1 << 20)) // eb
+    cols = 4096 if numel >= 4096 * 16 else 256
     rows = numel // cols
     mesh = [("X", G)]
     fl = s.FLAG_PARTIAL_OUT_DTYPE | (s.FLAG_TREE if tree else 0)
+    tdt = H.TORCH_DTYPES[dtype]
+    V = rows * cols * eb
     if op == "all_to_all":
-        # A[I, J_X] -> A[I_X, J]: each rank reads and writes its V/G once
-        src = [torch.empty((rows, cols // G), dtype=H.TORCH_DTYPES[dtype], device="cuda").uniform_(-1, 1)
-               for _ in range(G)]
-        dst = [torch.empty((rows // G, cols), dtype=H.TORCH_DTYPES[dtype], device="cuda") for _ in range(G)]
-        run = lambda: s.shmm_reshard(mesh, ((), ("X",)), (("X",), ()), rows, cols, dtype, src, dst)
-        V = rows * cols * eb          # the logical array; each rank holds V/G
-        nbytes = 2 * V
-    elif op == "all_gather":
-        p = s.Plan(mesh, (("X",), ()), ((), ()), ((), ()), rows, 8, cols, dtype, dtype)
-        src = [torch.empty((rows // G, cols), dtype=H.TORCH_DTYPES[dtype], device="cuda").uniform_(-1, 1)
-               for _ in range(G)]
-        dst = H.alloc(p, s.TENSOR_C)
-        run = lambda: p.all_gather(s.TENSOR_C, src, dst)
-        V = rows * cols * eb
+        nbytes = 2 * V               # A[I, J_X] -> A[I_X, J]: each rank reads and writes its V/G once
+    elif op in ("all_gather", "layernorm_all_gather"):
         nbytes = V + G * V           # read V (each shard once), write G copies of V
     else:
+        nbytes = G * V + (V if op == "reduce_scatter" else G * V)
+
+    def make_set():
+        if op == "all_to_all":
+            src = [torch.empty((rows, cols // G), dtype=tdt, device="cuda").uniform_(-1, 1) for _ in range(G)]
+            dst = [torch.empty((rows // G, cols), dtype=tdt, device="cuda") for _ in range(G)]
+            return lambda st=None: s.shmm_reshard(mesh, ((), ("X",)), (("X",), ()), rows, cols, dtype, src, dst,
+                                                  stream=st)
+        if op in ("all_gather", "layernorm_all_gather"):
+            p = s.Plan(mesh, (("X",), ()), ((), ()), ((), ()), rows, 8, cols, dtype, dtype)
+            src = [torch.empty((rows // G, cols), dtype=tdt, device="cuda").uniform_(-1, 1) for _ in range(G)]
+            dst = H.alloc(p, s.TENSOR_C)
+            if op == "all_gather":
+                return lambda st=None: p.all_gather(s.TENSOR_C, src, dst, stream=st)
+            # sequence parallelism's LayerNorm of each token row fused with the
+            # all-gather (gamma, beta: cols fp32 each, read once per thread)
+            gamma = torch.ones(cols, dtype=torch.float32, device="cuda")
+            beta = torch.zeros(cols, dtype=torch.float32, device="cuda")
+            return lambda st=None: p.layernorm_all_gather(src, gamma, beta, dst, stream=st)
         sC = (("X",), ()) if op == "reduce_scatter" else ((), ())
         p = s.Plan(mesh, ((), ("X",)), (("X",), ()), sC, rows, G, cols, dtype, dtype, fl)
-        src = [torch.empty((rows, cols), dtype=H.TORCH_DTYPES[dtype], device="cuda").uniform_(-1, 1)
-               for _ in range(G)]
+        src = [torch.empty((rows, cols), dtype=tdt, device="cuda").uniform_(-1, 1) for _ in range(G)]
         dst = H.alloc(p, s.TENSOR_C)
-        run = (lambda: p.reduce_scatter(src, dst)) if op == "reduce_scatter" else (lambda: p.all_reduce(src, dst))
-        V = rows * cols * eb
-        nbytes = G * V + (V if op == "reduce_scatter" else G * V)
+        if op == "reduce_scatter":
+            return lambda st=None: p.reduce_scatter(src, dst, stream=st)
+        return lambda st=None: p.all_reduce(src, dst, stream=st)
+
+    run = make_set()
     # L2 flush by READING a buffer twice the L2 size: clean lines, so no
     # write-back of the flush itself lands inside the timed kernel
     flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
@@ -501,6 +539,10 @@ def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False):
     times = []
     for _ in range(reps):
         flush.sum()
+        # keep the device busy while the host enqueues the start event and the
+        # collective (argument checks and marshalling take tens of
+        # microseconds), so the events bracket the device's work alone
+        torch.cuda._sleep(SLEEP_CYCLES)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         run()
@@ -513,10 +555,45 @@ def time_collective(s, H, torch, op, G, mib, dtype, reps=20, tree=False):
     # matmuls and collectives on a torus", payload accounting): RS and AG
     # (G-1)/G of V, AR both, all-to-all (G-1)/G of the rank's V/G
     payload = {"all_reduce": 2 * (G - 1) * V // G, "all_to_all": (G - 1) * V // (G * G)}.get(op, (G - 1) * V // G)
-    return {"op": op, "ranks": G, "MiB_per_rank": mib, "dtype": dtype, "order": "tree" if tree else "sequential",
-            "ms_median": t, "ms_best": min(times), "GB_s": nbytes / (t * 1e-3) / 1e9,
-            "bytes": nbytes, "busbw_GB_s": (V / (t * 1e-3) / 1e9) * busbw_factor,
-            "payload_bytes_per_rank": payload}
+    out = {"op": op, "ranks": G, "MiB_per_rank": mib, "dtype": dtype, "order": "tree" if tree else "sequential",
+           "ms_median": t, "ms_mean": statistics.mean(times), "ms_best": min(times),
+           "GB_s": nbytes / (t * 1e-3) / 1e9,
+           "l2_resident": G * V < 2 * L2_BYTES if op != "all_to_all" else V < 2 * L2_BYTES,
+           "bytes": nbytes, "busbw_GB_s": (V / (t * 1e-3) / 1e9) * busbw_factor,
+           "payload_bytes_per_rank": payload}
+    if stream_rate:
+        del run
+        touched = nbytes  # bytes one launch reads and writes
+        nsets = max(1, min(128, -(-4 * L2_BYTES // touched)))
+        sets = [make_set() for _ in range(nsets)]
+        launches = max(32, nsets)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for f in sets:
+                f(side.cuda_stream)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream().cuda_stream
+            for i in range(launches):
+                sets[i % nsets](cs)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        st = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            b.synchronize()
+            st.append(a.elapsed_time(b) / launches)
+        ts = statistics.median(st)
+        out.update({"stream_ms": ts, "stream_GB_s": nbytes / (ts * 1e-3) / 1e9, "stream_sets": nsets})
+        del g, sets
+    return out
 
 
 # --------------------------------------------------------------- oracle
@@ -741,7 +818,7 @@ def run_shmm(args, dist_ctx):
     import partial_sum_reduction_gb300 as s
     from partial_sum_reduction_gb300 import helpers as H
     peaks, peak_kind = load_peaks()
-    wl = Workload(args.workload, "cuda")
+    wl = Workload(args.workload, "cuda", rank_order=args.rank_order, sm_split=not args.no_sm_split)
     total_ms, per_step, launches, clocks = time_device(wl, args.steps, args.warmup, dist_ctx, graph=args.graph)
     ms = total_ms / args.steps
     N = dist_ctx.world
@@ -760,7 +837,7 @@ def run_shmm(args, dist_ctx):
     e2e_windows, h2d, d2h = time_e2e(wl, e2e_steps, dist_ctx)
     e2e_ms = statistics.median(e2e_windows)
     e2e_value = wl.flops * N / (e2e_ms * 1e-3) / 1e12
-    rs = time_collective(s, H, torch, "reduce_scatter", 8, 256, "f32")
+    rs = time_collective(s, H, torch, "reduce_scatter", 8, 256, "f32", stream_rate=False)
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": N, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "ms_median_step": statistics.median(per_step),
@@ -768,6 +845,10 @@ def run_shmm(args, dist_ctx):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload]["text"], "name": args.workload,
                    "launch": "CUDA graph replay" if args.graph else "direct shmm_run calls",
+                   "sm_split": getattr(wl, "sm_split", None),
+                   "fused_reduction": ("each rank's fp32 partial added in ascending rank order"
+                                       if args.rank_order else
+                                       "the group's products accumulated in one fp32 accumulator"),
                    "l2": "inputs larger than L2 (%.2f GB of per-rank operands per step)" % (wl.input_bytes() / 1e9),
                    "flop_per_step": wl.flops, "replicas": N},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -862,16 +943,21 @@ def run_sweep(args):
     import partial_sum_reduction_gb300 as s
     from partial_sum_reduction_gb300 import helpers as H
     peaks, kind = load_peaks()
-    sizes = [int(x) for x in args.sizes.split(",")]
-    for op in ("reduce_scatter", "all_reduce", "all_gather", "all_to_all"):
-        for dtype in ("f32", "bf16"):
-            for G in (2, 4, 8, 16):
+    sizes = [float(x) if "." in x else int(x) for x in args.sizes.split(",")]
+    ranks = [int(x) for x in args.ranks.split(",")]
+    orders = {"sequential": (False,), "tree": (True,), "both": (False, True)}[args.orders]
+    for op in args.ops.split(","):
+        for dtype in args.dtypes.split(","):
+            for G in ranks:
                 for mib in sizes:
                     if G * mib * (2 if op == "all_reduce" else 1) > 40 * 1024:
                         continue
-                    for tree in ((False, True) if op in ("reduce_scatter", "all_reduce") else (False,)):
-                        r = time_collective(s, H, torch, op, G, mib, dtype, tree=tree)
+                    for tree in (orders if op in ("reduce_scatter", "all_reduce") else (False,)):
+                        r = time_collective(s, H, torch, op, G, mib, dtype, reps=args.reps, tree=tree,
+                                            stream_rate=not args.no_stream_rate)
                         r["frac_hbm"] = r["GB_s"] / peaks["hbm_gbs"]
+                        if "stream_GB_s" in r:
+                            r["stream_frac_hbm"] = r["stream_GB_s"] / peaks["hbm_gbs"]
                         r["peak_kind"] = kind
                         print(json.dumps(r), flush=True)
 
@@ -884,7 +970,22 @@ def main():
     ap.add_argument("--impl", default="shmm", choices=["shmm", "reference"])
     ap.add_argument("--workload", default="down_projection", choices=sorted(WORKLOADS))
     ap.add_argument("--sweep", default=None, choices=[None, "collectives", "gemm"])
-    ap.add_argument("--sizes", default="1,16,256,1024")
+    ap.add_argument("--sizes", default="1,16,256,1024",
+                    help="--sweep: MiB per rank (fractions allowed: 0.015625 is 16 KiB, the launch floor)")
+    ap.add_argument("--ranks", default="2,4,8,16", help="--sweep collectives: group sizes")
+    ap.add_argument("--ops", default="reduce_scatter,all_reduce,all_gather,all_to_all,layernorm_all_gather",
+                    help="--sweep collectives: which collectives")
+    ap.add_argument("--dtypes", default="f32,bf16", help="--sweep collectives: buffer types")
+    ap.add_argument("--orders", default="both", choices=["sequential", "tree", "both"],
+                    help="--sweep collectives: summation orders of RS and AR")
+    ap.add_argument("--reps", type=int, default=20, help="--sweep collectives: single-launch repetitions")
+    ap.add_argument("--no-stream-rate", action="store_true",
+                    help="--sweep collectives: skip the back-to-back (graph-replayed) rate")
+    ap.add_argument("--no-sm-split", action="store_true",
+                    help="four_case: every case's GEMM may take all SMs (no split of the GPU among the cases)")
+    ap.add_argument("--rank-order", action="store_true",
+                    help="fused reductions add each rank's fp32 partial in ascending rank order "
+                         "(SHMM_FLAG_RANK_ORDER) instead of accumulating the group in one accumulator")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="replay one captured CUDA graph per step (small workloads are host-bound)")

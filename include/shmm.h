@@ -236,6 +236,16 @@ shmm_status_t shmm_plan(const shmm_mesh_t *mesh, const shmm_spec_t *spec_A,
 /* Frees a plan (NULL is accepted). */
 shmm_status_t shmm_plan_destroy(shmm_plan_t *plan);
 
+/* Caps how many SMs the plan's tensor-core GEMM launches occupy: at most
+ * max_sms / 2 CTA pairs (or max_sms single CTAs) take the plan's tiles, in
+ * the same tile order.  0 (the default) lets a launch take every SM.  The
+ * cap lets independent plans run side by side on separate streams, each on
+ * its own share of the SMs, instead of queueing whole-GPU launches with a
+ * partial last wave each; results do not depend on it.  It has no effect on
+ * the CUDA-core GEMM or the collective kernels.  Not thread-safe against a
+ * concurrent shmm_run on the same plan.  Errors: NULL, SHAPE (max_sms < 0). */
+shmm_status_t shmm_plan_set_sm_limit(shmm_plan_t *plan, int max_sms);
+
 /* Fills `info` with the plan's classification, shapes and byte counts. */
 shmm_status_t shmm_plan_query(const shmm_plan_t *plan, shmm_plan_info_t *info);
 

@@ -145,6 +145,7 @@ shmm::GemmArgs gemm_args(const shmm_plan_t *p) {
     g.Kd = al.ext[1];
     g.N = bl.ext[1];
     g.in_dt = p->in_dt;
+    g.max_sms = p->max_sms;
     return g;
 }
 

@@ -1198,7 +1198,7 @@ int num_sms() {
 }
 
 template <int BN>
-cudaError_t launch_bn(TcK &k, cudaStream_t s) {
+cudaError_t launch_bn(TcK &k, cudaStream_t s, int max_sms) {
     using C = Cfg<BN>;
     static shmm::PerDevice<int> attr_set;
     int dev = 0;
@@ -1212,7 +1212,9 @@ cudaError_t launch_bn(TcK &k, cudaStream_t s) {
     }
     k.n_tiles = (int)((k.N + BN - 1) / BN);
     const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
-    const int grid = (int)(total < num_sms() ? total : num_sms());
+    int ctas = num_sms();
+    if (max_sms > 0 && max_sms < ctas) ctas = max_sms;
+    const int grid = (int)(total < ctas ? total : ctas);
     shmm::count_launch();
     gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, s>>>(k);
     return cudaGetLastError();
@@ -1256,15 +1258,26 @@ cudaError_t pair_capacity(int *pairs) {
     return cudaSuccess;
 }
 
+// Pairs a launch may use: the resident capacity, capped by the plan's SM
+// limit (two SMs per pair; at least one pair).
+int limit_pairs(int cap, int max_sms) {
+    if (max_sms > 0 && cap > 0) {
+        const int lim = max_sms / 2 > 0 ? max_sms / 2 : 1;
+        if (lim < cap) return lim;
+    }
+    return cap;
+}
+
 // Launches the CTA-pair kernel: clusters of two, at most as many pairs as can
-// be resident at once.
+// be resident at once (and as the plan's SM limit allows).
 template <int NH>
-cudaError_t launch_pair(TcK &k, cudaStream_t s) {
+cudaError_t launch_pair(TcK &k, cudaStream_t s, int max_sms) {
     using C = Cfg2<NH>;
     int cap = 0;
     const cudaError_t ce = pair_capacity<NH>(&cap);
     if (ce != cudaSuccess) return ce;
     if (cap < 1) return cudaErrorNotSupported;  // no pair can be resident: the caller falls back
+    cap = limit_pairs(cap, max_sms);
     k.m_tiles = (int)((k.M + 255) / 256);
     k.n_tiles = (int)((k.N + 256 * NH - 1) / (256 * NH));
     const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
@@ -1303,7 +1316,7 @@ bool pair_kernel_enabled() {
 // 16384 (the MLP's GeLU matmul, 64 k-blocks: 0.98 across 27 and 14 waves).
 // Pick the smaller estimate: waves x work per tile x that factor.
 // SHMM_TC_WIDE=0 / 1 forces 256- / 512-column tiles (tests compare them).
-int pair_halves(const TcK &k) {
+int pair_halves(const TcK &k, int max_sms) {
     if (k.fused && !k.accum && k.G > 1) return 1;  // the rank-order fold needs TMEM's second buffer
     const char *env = getenv("SHMM_TC_WIDE");
     if (env && env[0] == '0') return 1;
@@ -1312,6 +1325,8 @@ int pair_halves(const TcK &k) {
     int cap1 = 0, cap2 = 0;
     if (pair_capacity<1>(&cap1) != cudaSuccess || pair_capacity<2>(&cap2) != cudaSuccess || cap1 < 1 || cap2 < 1)
         return 1;
+    cap1 = limit_pairs(cap1, max_sms);
+    cap2 = limit_pairs(cap2, max_sms);
     const int64_t m_t = (k.M + 255) / 256;
     const int64_t t1 = (int64_t)k.units * m_t * ((k.N + 255) / 256);
     const int64_t t2 = (int64_t)k.units * m_t * ((k.N + 511) / 512);
@@ -1436,11 +1451,12 @@ int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::strin
         k.k_blocks = (int)((a.Kd + BK - 1) / BK);
         // 256-row tiles on CTA pairs unless the local M fits one 128-row tile
         cudaError_t e = cudaErrorNotSupported;
-        if (a.M > BM && pair_kernel_enabled()) e = pair_halves(k) == 2 ? launch_pair<2>(k, s) : launch_pair<1>(k, s);
+        if (a.M > BM && pair_kernel_enabled())
+            e = pair_halves(k, a.max_sms) == 2 ? launch_pair<2>(k, s, a.max_sms) : launch_pair<1>(k, s, a.max_sms);
         if (e == cudaErrorNotSupported) {
             // single-CTA tiles when no CTA pair fits (or is wanted)
             k.m_tiles = (int)((a.M + BM - 1) / BM);
-            e = launch_bn<bn>(k, s);
+            e = launch_bn<bn>(k, s, a.max_sms);
         }
         if (e != cudaSuccess) return (int)e;
     }

@@ -345,6 +345,14 @@ shmm_status_t shmm_plan_destroy(shmm_plan_t *plan) {
     return SHMM_OK;
 }
 
+shmm_status_t shmm_plan_set_sm_limit(shmm_plan_t *plan, int max_sms) {
+    shmm::clear_error();
+    if (!plan) return shmm::fail(SHMM_ERR_NULL, "shmm_plan_set_sm_limit: plan is NULL");
+    if (max_sms < 0) return shmm::fail(SHMM_ERR_SHAPE, "shmm_plan_set_sm_limit: max_sms < 0");
+    plan->max_sms = max_sms;
+    return SHMM_OK;
+}
+
 shmm_status_t shmm_workspace_size(const shmm_plan_t *p, size_t *bytes) {
     if (!p || !bytes) return shmm::fail(SHMM_ERR_NULL, "shmm_workspace_size: NULL argument");
     auto slot = [](int64_t b) { return (size_t)((b + 255) / 256 * 256); };

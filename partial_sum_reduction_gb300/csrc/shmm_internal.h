@@ -91,6 +91,7 @@ struct shmm_plan {
     // reduce, and (on tensor cores) at most 16 ranks per group, the operand
     // descriptors one launch carries.
     bool fused = false;
+    int max_sms = 0;  // SMs the plan's tensor-core GEMM launches may occupy (0: all)
     std::vector<shmm::Box> boxes[7];          // [shmm_tensor_t][rank]
     shmm::Groups red_groups, gA_groups, gB_groups, gC_groups;
 };
@@ -177,6 +178,7 @@ struct GemmArgs {
     bool rank_order = false;  // fused: per-rank partials added in q order
     int mode = 2;           // fused write mode (0/1 RS dim, 2 AR)
     bool gelu = false;
+    int max_sms = 0;        // tensor cores: SMs a launch may occupy (0: all)
     int64_t M = 0, N = 0, Kd = 0;
     shmm_dtype_t in_dt = SHMM_BF16, out_dt = SHMM_F32;
     const void *const *A = nullptr;

@@ -80,7 +80,7 @@ class ShmmError(RuntimeError):
 
 
 EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_box",
-           "shmm_plan_group", "shmm_workspace_size", "shmm_local_matmul", "shmm_reduce_scatter",
+           "shmm_plan_set_sm_limit", "shmm_plan_group", "shmm_workspace_size", "shmm_local_matmul", "shmm_reduce_scatter",
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
            "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace",
            "shmm_selftest_wait_timeout", "shmm_choose_operand", "shmm_reshard", "shmm_layernorm",
@@ -106,6 +106,7 @@ def lib():
                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_uint32, ctypes.POINTER(P)]
         L.shmm_plan_destroy.argtypes = [P]
+        L.shmm_plan_set_sm_limit.argtypes = [P, ctypes.c_int]
         L.shmm_plan_query.argtypes = [P, ctypes.POINTER(shmm_plan_info_t)]
         L.shmm_plan_rank_box.argtypes = [P, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
@@ -288,6 +289,10 @@ class Plan:
     def handle(self):
         return self._h
 
+    def set_sm_limit(self, max_sms: int):
+        """Caps the SMs this plan's tensor-core GEMM launches occupy (0: all)."""
+        _check(lib().shmm_plan_set_sm_limit(self._h, int(max_sms)))
+
     def query(self) -> shmm_plan_info_t:
         info = shmm_plan_info_t()
         _check(lib().shmm_plan_query(self._h, ctypes.byref(info)))
@@ -374,6 +379,10 @@ def shmm_plan(mesh, spec_A, spec_B, spec_C, I, J, K, in_dtype="bf16", out_dtype=
 
 def shmm_plan_destroy(plan: Plan) -> None:
     plan.close()
+
+
+def shmm_plan_set_sm_limit(plan: Plan, max_sms: int) -> None:
+    plan.set_sm_limit(max_sms)
 
 
 def shmm_plan_query(plan: Plan) -> shmm_plan_info_t:

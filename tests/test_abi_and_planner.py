@@ -348,3 +348,13 @@ def test_reshard_argument_checks(shmm, monkeypatch):
     with pytest.raises(shmm.ShmmError) as e:
         shmm.shmm_reshard("{X:2}", "I,J_X", "I_X,J", 4, 4, "f32", good, good, stream=0)
     assert e.value.status == shmm.shmm.ERR_INJECTED
+
+
+def test_sm_limit_argument_checks(shmm):
+    p = shmm.Plan("{X:2,Y:2}", "I_X,J", "J,K_Y", "I_X,K_Y", 512, 256, 512, "bf16", "bf16")
+    p.set_sm_limit(32)
+    p.set_sm_limit(0)
+    with pytest.raises(shmm.ShmmError) as e:
+        p.set_sm_limit(-1)
+    assert e.value.status == shmm.shmm.ERR_SHAPE
+    assert shmm.lib().shmm_plan_set_sm_limit(None, 4) == shmm.shmm.ERR_NULL

@@ -714,6 +714,38 @@ def test_ragged_contraction(s, pair, fused, mesh, sA, sB, sC, I, J, K, monkeypat
     compare(plan, gpu, ores, exact=False, tol=F32P_TOL)
 
 
+@pytest.mark.parametrize("case,sA,sB,sC", FOUR)
+@pytest.mark.parametrize("limit", [2, 34, 150])
+def test_sm_limit_keeps_the_bits(s, case, sA, sB, sC, limit, monkeypatch):
+    """A plan capped to a few SMs (one CTA pair, a share of the GPU, odd and
+    above the pair count) gives the same bits as the plan on every SM, in
+    both tile widths, while other plans run on their own streams beside it."""
+    from partial_sum_reduction_gb300 import helpers as H
+    A, B = shmm_inputs.scaled_normal_pair(1024, 512, 768, "bf16", seed=case + 40)
+    for wide in ("0", "1"):
+        monkeypatch.setenv("SHMM_TC_WIDE", wide)
+        outs = []
+        for lim in (0, limit):
+            plan = s.Plan(XY22, sA, sB, sC, 1024, 512, 768, "bf16", "bf16", s.FLAG_FUSED)
+            plan.set_sm_limit(lim)
+            A_r, B_r = H.shard(plan, s.TENSOR_A, A), H.shard(plan, s.TENSOR_B, B)
+            C_r = H.alloc(plan, s.TENSOR_C, fill=float("nan"))
+            side = torch.cuda.Stream()
+            other = s.Plan(XY22, sA, sB, sC, 1024, 512, 768, "bf16", "bf16", s.FLAG_FUSED)
+            other.set_sm_limit(max(2, 152 - limit))
+            oC = H.alloc(other, s.TENSOR_C)
+            side.wait_stream(torch.cuda.current_stream())
+            other.run(A_r, B_r, oC, H.workspace(other), stream=side)
+            plan.run(A_r, B_r, C_r, H.workspace(plan))
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            outs.append([c.cpu() for c in C_r])
+            for c, o in zip(C_r, oC):
+                assert torch.equal(c, o)
+        for a, b in zip(*outs):
+            assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("flags", ["FUSED", "FUSED|RANK_ORDER", "0"])
 def test_repeated_runs_give_identical_bits(s, flags):
     """Every path is deterministic: one input gives one result, run after run
