@@ -92,6 +92,27 @@ __device__ __forceinline__ int shard_split(int blocks, int64_t extent, int64_t x
     return p;
 }
 
+// The in-place gather's walk along the contracted dim: the shard holding
+// k-block kb and the coordinate inside it, advanced one k-block at a time
+// (shard edges along K fall on k-block edges), so the producer divides only
+// once per tile.  Past the last shard the coordinate keeps growing, as in
+// shard_split.
+struct KWalk {
+    int p;
+    int32_t local;
+    __device__ __forceinline__ void start(int blocks, int64_t extent) { p = shard_split(blocks, extent, 0, &local); }
+    // true when the walk entered the next shard
+    __device__ __forceinline__ bool advance(int blocks, int64_t extent, int step) {
+        local += step;
+        if (p < blocks - 1 && local >= extent) {
+            local -= (int32_t)extent;
+            ++p;
+            return true;
+        }
+        return false;
+    }
+};
+
 // ---- PTX wrappers ------------------------------------------------------
 
 using namespace shmm_dev;
@@ -669,6 +690,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     const int ri = unit * Gq + q;
                     int32_t a_r;
                     const int a_p0 = shard_split(k.a_b0, k.a_brows, (int64_t)mt * BM, &a_r);
+                    // In-place gathers: the row of A and each B box's column
+                    // shard are fixed for the tile; the K shards advance.
+                    constexpr int NB = BN / 64;
+                    KWalk wa, wb;
+                    int32_t bx[NB];
+                    int bp1[NB];
+                    const CUtensorMap *map_a = &k.tmA[ri];
+                    const CUtensorMap *map_b[NB];
+                    if (k.gathered) {
+                        wa.start(k.a_b1, k.a_bcols);
+                        wb.start(k.b_b0, k.b_brows);
+                        map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + wa.p]];
+#pragma unroll
+                        for (int c = 0; c < NB; ++c) {
+                            bp1[c] = shard_split(k.b_b1, k.b_bcols, (int64_t)nt * BN + c * 64, &bx[c]);
+                            map_b[c] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * k.b_b1 + bp1[c]]];
+                        }
+                    }
                     for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
@@ -685,17 +724,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                             for (int c = 0; c < BN / 64; ++c)
                                 tma_load_2d(b_dst + c * 8192, &k.tmB[ri], full_bar(s), nt * BN + c * 64, kb * BK);
                         } else {
-                            int32_t a_c, b_r, x;
-                            const int a_p1 = shard_split(k.a_b1, k.a_bcols, (int64_t)kb * BK, &a_c);
-                            tma_load_2d(a_dst, &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + a_p1]], full_bar(s),
-                                        a_c, a_r);
-                            const int b_p0 = shard_split(k.b_b0, k.b_brows, (int64_t)kb * BK, &b_r);
+                            tma_load_2d(a_dst, map_a, full_bar(s), wa.local, a_r);
 #pragma unroll
-                            for (int c = 0; c < BN / 64; ++c) {
-                                const int b_p1 = shard_split(k.b_b1, k.b_bcols, (int64_t)nt * BN + c * 64, &x);
-                                tma_load_2d(b_dst + c * 8192,
-                                            &k.tmB[s_bidx[ri * kMaxMaps + b_p0 * k.b_b1 + b_p1]], full_bar(s), x, b_r);
-                            }
+                            for (int c = 0; c < NB; ++c)
+                                tma_load_2d(b_dst + c * 8192, map_b[c], full_bar(s), bx[c], wb.local);
+                            if (wa.advance(k.a_b1, k.a_bcols, BK))
+                                map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + wa.p]];
+                            if (wb.advance(k.b_b0, k.b_brows, BK))
+#pragma unroll
+                                for (int c = 0; c < NB; ++c)
+                                    map_b[c] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * k.b_b1 + bp1[c]]];
                         }
                         last_parity[s] = (int)ph;
                     }
@@ -910,6 +948,25 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                     const int ri = unit * Gq + q;
                     int32_t a_r;
                     const int a_p0 = shard_split(k.a_b0, k.a_brows, (int64_t)mt * 256 + (int)cr * BM, &a_r);
+                    // In-place gathers: the row of A and each B box's column
+                    // shard are fixed for the tile; the K shards advance.
+                    constexpr int NB = 2 * NH;
+                    KWalk wa, wb;
+                    int32_t bx[NB];
+                    int bp1[NB];
+                    const CUtensorMap *map_a = &k.tmA[ri];
+                    const CUtensorMap *map_b[NB];
+                    if (k.gathered) {
+                        wa.start(k.a_b1, k.a_bcols);
+                        wb.start(k.b_b0, k.b_brows);
+                        map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + wa.p]];
+#pragma unroll
+                        for (int j = 0; j < NB; ++j) {
+                            bp1[j] = shard_split(k.b_b1, k.b_bcols,
+                                                 (int64_t)nt * TW + (j / 2) * BN + (int)cr * 128 + (j % 2) * 64, &bx[j]);
+                            map_b[j] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * k.b_b1 + bp1[j]]];
+                        }
+                    }
                     for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
@@ -930,21 +987,16 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                                     tma_load_2d_pair(b_dst + (h * 2 + c) * 8192, &k.tmB[ri], bar,
                                                      nt * TW + h * BN + (int)cr * 128 + c * 64, kb * BK);
                         } else {
-                            int32_t a_c, b_r, x;
-                            const int a_p1 = shard_split(k.a_b1, k.a_bcols, (int64_t)kb * BK, &a_c);
-                            tma_load_2d_pair(a_dst, &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + a_p1]], bar, a_c,
-                                             a_r);
-                            const int b_p0 = shard_split(k.b_b0, k.b_brows, (int64_t)kb * BK, &b_r);
+                            tma_load_2d_pair(a_dst, map_a, bar, wa.local, a_r);
 #pragma unroll
-                            for (int h = 0; h < NH; ++h)
+                            for (int j = 0; j < NB; ++j)
+                                tma_load_2d_pair(b_dst + j * 8192, map_b[j], bar, bx[j], wb.local);
+                            if (wa.advance(k.a_b1, k.a_bcols, BK))
+                                map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + wa.p]];
+                            if (wb.advance(k.b_b0, k.b_brows, BK))
 #pragma unroll
-                                for (int c = 0; c < 2; ++c) {
-                                    const int b_p1 = shard_split(
-                                        k.b_b1, k.b_bcols, (int64_t)nt * TW + h * BN + (int)cr * 128 + c * 64, &x);
-                                    tma_load_2d_pair(b_dst + (h * 2 + c) * 8192,
-                                                     &k.tmB[s_bidx[ri * kMaxMaps + b_p0 * k.b_b1 + b_p1]], bar, x,
-                                                     b_r);
-                                }
+                                for (int j = 0; j < NB; ++j)
+                                    map_b[j] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * k.b_b1 + bp1[j]]];
                         }
                     }
                 }
