@@ -355,6 +355,41 @@ def test_collectives_at_one_gib_per_rank(s, dtype):
         _bits_equal(ag[q].float().cpu().numpy(), ref, "all-gather member %d" % q)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("dtype,order", [("f32", "sequential"), ("bf16", "sequential"), ("f32", "pairwise")])
+def test_collectives_eight_ranks_at_256_mib(s, dtype, order):
+    """Eight ranks of 256 MiB partials: the reduce-scatter bench.py times
+    beside every benchmark line (fp32, rank order), with the grid and
+    unrolling of the eight-rank kernels, bit for bit against the oracle."""
+    from partial_sum_reduction_gb300 import helpers as H
+    G, eb = 8, (4 if dtype == "f32" else 2)
+    numel = (256 << 20) // eb
+    cols = 4096
+    rows = numel // cols
+    bufs = [b.reshape(rows, cols) for b in shmm_inputs.partial_buffers(G, numel, dtype, seed=31)]
+    mesh = [("X", G)]
+    fl = s.FLAG_PARTIAL_OUT_DTYPE | (s.FLAG_TREE if order == "pairwise" else 0)
+    p_rs = s.Plan(mesh, ((), ("X",)), (("X",), ()), (("X",), ()), rows, G, cols, dtype, dtype, fl)
+    p_ar = s.Plan(mesh, ((), ("X",)), (("X",), ()), ((), ()), rows, G, cols, dtype, dtype, fl)
+    P_r = [b.cuda() for b in bufs]
+    rs = H.alloc(p_rs, s.TENSOR_C, fill=float("nan"))
+    p_rs.reduce_scatter(P_r, rs)
+    ar = H.alloc(p_ar, s.TENSOR_C, fill=float("nan"))
+    p_ar.all_reduce(P_r, ar)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    del P_r
+    host = [b.float().numpy() for b in bufs]
+    del bufs
+    ref = oracle.collective_reduce(host, "reduce_scatter", dtype, order=order)
+    for q in range(G):
+        _bits_equal(rs[q].float().cpu().numpy(), ref[q], "reduce-scatter owner %d" % q)
+    del ref
+    ref = oracle.collective_reduce(host, "all_reduce", dtype, order=order)[0]
+    for q in range(G):
+        _bits_equal(ar[q].float().cpu().numpy(), ref, "all-reduce member %d" % q)
+
+
 @pytest.mark.parametrize("G", [2, 4])
 def test_reduce_scatter_onto_columns(s, G):
     from partial_sum_reduction_gb300 import helpers as H
