@@ -195,7 +195,7 @@ class Workload:
     """Plans, per-rank device buffers and pinned host copies of one workload;
     ``step()`` enqueues one pass of the hot path."""
 
-    def __init__(self, name, device, rank_order=False, sm_split=True):
+    def __init__(self, name, device, rank_order=False, sm_split=True, batch=True):
         import torch
         import partial_sum_reduction_gb300 as s
         import shmm_inputs
@@ -215,13 +215,15 @@ class Workload:
             self.host_globals = (A, B)
             for sA, sB, sC in FOUR_CASES:
                 self._add(c["mesh"], sA, sB, sC, A, B, FUSED, device)
-            # The four cases are independent and run on their own streams.
-            # Each alone is 1-2 waves of tiles and would take every SM with a
-            # partial last wave, so the GPU is split among them by their
-            # share of the FLOPs (whole CTA pairs, at least one each): the
-            # four then run side by side and end together.
+            # The four cases are independent.  Each alone is 1-2 waves of
+            # tiles and would take every SM with a partial last wave.  By
+            # default one shmm_run_batch call runs their GEMMs as one launch
+            # (one tile walk over all four); otherwise they run on their own
+            # streams with the GPU split among them by their share of the
+            # FLOPs (whole CTA pairs, at least one each).
+            self.batch = batch
             self.sm_split = None
-            if sm_split:
+            if sm_split and not batch:
                 sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
                 fl = [p.info.flops_per_rank * p.nranks for p, *_ in self.steps_spec]
                 pairs = [max(1, int(round(sms // 2 * f / sum(fl)))) for f in fl]
@@ -275,6 +277,11 @@ class Workload:
         return p
 
     def step(self, stream):
+        if self.name == "four_case" and self.batch:
+            sp = self.steps_spec
+            self.s.shmm_run_batch([x[0] for x in sp], [x[1] for x in sp], [x[2] for x in sp], [x[3] for x in sp],
+                                  [x[4] for x in sp], stream=stream)
+            return
         if self.name == "four_case":
             # four independent sharded matmuls: forked onto their own streams
             # so one case's last partial wave overlaps the next case's work
@@ -818,7 +825,8 @@ def run_shmm(args, dist_ctx):
     import partial_sum_reduction_gb300 as s
     from partial_sum_reduction_gb300 import helpers as H
     peaks, peak_kind = load_peaks()
-    wl = Workload(args.workload, "cuda", rank_order=args.rank_order, sm_split=not args.no_sm_split)
+    wl = Workload(args.workload, "cuda", rank_order=args.rank_order, sm_split=not args.no_sm_split,
+                  batch=not args.no_batch)
     total_ms, per_step, launches, clocks = time_device(wl, args.steps, args.warmup, dist_ctx, graph=args.graph)
     ms = total_ms / args.steps
     N = dist_ctx.world
@@ -845,7 +853,10 @@ def run_shmm(args, dist_ctx):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload]["text"], "name": args.workload,
                    "launch": "CUDA graph replay" if args.graph else "direct shmm_run calls",
-                   "sm_split": getattr(wl, "sm_split", None),
+                   "four_case_launch": (None if args.workload != "four_case" else
+                                        "shmm_run_batch: the four GEMMs in one launch" if wl.batch else
+                                        "four streams, SMs split %s" % wl.sm_split if wl.sm_split else
+                                        "four streams, whole-GPU launches"),
                    "fused_reduction": ("each rank's fp32 partial added in ascending rank order"
                                        if args.rank_order else
                                        "the group's products accumulated in one fp32 accumulator"),
@@ -981,6 +992,8 @@ def main():
     ap.add_argument("--reps", type=int, default=20, help="--sweep collectives: single-launch repetitions")
     ap.add_argument("--no-stream-rate", action="store_true",
                     help="--sweep collectives: skip the back-to-back (graph-replayed) rate")
+    ap.add_argument("--no-batch", action="store_true",
+                    help="four_case: four shmm_run calls on four streams instead of one shmm_run_batch")
     ap.add_argument("--no-sm-split", action="store_true",
                     help="four_case: every case's GEMM may take all SMs (no split of the GPU among the cases)")
     ap.add_argument("--rank-order", action="store_true",

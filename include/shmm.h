@@ -430,7 +430,33 @@ typedef struct {
 shmm_status_t shmm_choose_operand(int64_t B, int64_t D, int64_t F, int axis_size, int elem_bytes,
                                   const shmm_device_model_t *device, shmm_operand_choice_t *out);
 
-/* Size of the fixed device workspace behind shmm_run_static_workspace. */
+/* Runs n independent sharded matmuls, as n calls of shmm_run would, with
+ * their local GEMMs sharing launches: every plan whose shmm_run is a single
+ * tensor-core GEMM launch (operands read whole or gathered in place, a
+ * fused reduction or none, no all-gather of the result) joins one
+ * persistent tile walk over all their tiles (up to 4 plans and 16 operand
+ * slots and outputs per launch; more take further launches). Sharing a
+ * launch pays its fixed cost once and fills the last wave of tiles with
+ * other plans' work. Plans that do not qualify run through shmm_run first,
+ * on the same stream. Each plan's results are bit for bit those of its own
+ * shmm_run. The plans must be independent: no output buffer of one may be
+ * an input or output of another. SM limits (shmm_plan_set_sm_limit) apply
+ * only when every joined plan has one; the launch then takes the largest.
+ *   n                 in: number of plans (0: nothing to do)
+ *   plans             in: n plans
+ *   A_r, B_r, C_r     in: per plan, its per-rank pointer array, as shmm_run
+ *   workspaces        in: per plan, its workspace (NULL entries, or a NULL
+ *                         array, where no plan needs one)
+ *   workspace_bytes   in: per plan, the workspace sizes (or NULL)
+ *   stream            in: cudaStream_t
+ * Every plan and pointer is checked before anything is enqueued.
+ * Errors: those of shmm_run (the message names the plan's index), and
+ * SHAPE (n < 0), NULL (NULL arrays). */
+shmm_status_t shmm_run_batch(int n, const shmm_plan_t *const *plans, const void *const *const *A_r,
+                             const void *const *const *B_r, void *const *const *C_r,
+                             void *const *workspaces, const size_t *workspace_bytes, void *stream);
+
+/* Size of the fixed device workspace behind shmm_run_static_workspace. *//* Size of the fixed device workspace behind shmm_run_static_workspace. */
 #define SHMM_STATIC_WORKSPACE_BYTES (64u << 20)
 
 /* shmm_run for callers that cannot allocate device memory: a plugin or host

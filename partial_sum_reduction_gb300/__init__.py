@@ -7,6 +7,6 @@ from .shmm import (  # noqa: F401
     ShmmError, TENSOR_A, TENSOR_A_LOCAL, TENSOR_B, TENSOR_B_LOCAL, TENSOR_C, TENSOR_C_REDUCED, TENSOR_P, lib,
     parse_mesh, parse_spec, shmm_all_gather, shmm_all_reduce, shmm_bounds_checked, shmm_choose_operand,
     shmm_kernel_launches, shmm_layernorm, shmm_local_matmul, shmm_plan, shmm_plan_destroy, shmm_plan_query,
-    shmm_plan_rank_box, shmm_plan_set_sm_limit, shmm_reduce_scatter, shmm_reshard, shmm_run, shmm_run_host,
-    shmm_selftest_wait_timeout, shmm_sync_status, shmm_version, shmm_workspace_size)
+    shmm_plan_rank_box, shmm_plan_set_sm_limit, shmm_reduce_scatter, shmm_reshard, shmm_run, shmm_run_batch,
+    shmm_run_host, shmm_selftest_wait_timeout, shmm_sync_status, shmm_version, shmm_workspace_size)
 from . import helpers  # noqa: F401

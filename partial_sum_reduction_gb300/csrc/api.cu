@@ -150,7 +150,7 @@ shmm::GemmArgs gemm_args(const shmm_plan_t *p) {
 }
 
 int run_gemm(const shmm_plan_t *p, const shmm::GemmArgs &g, int *status, void *stream, std::string *msg) {
-    if (p->tensor_core && shmm::tcgen05_supported(g)) return shmm::launch_gemm_tcgen05(g, status, stream, msg);
+    if (p->tensor_core && shmm::tcgen05_supported(g)) return shmm::launch_gemm_tcgen05(&g, 1, status, stream, msg);
     if (g.A_src || g.B_src) {  // in-place gathers exist only on the tensor-core path
         *msg = "in-place operand gather needs the tensor-core GEMM";
         return (int)cudaErrorNotSupported;
@@ -245,6 +245,40 @@ shmm::GemmArgs unit_args(const shmm_plan_t *p, const void *const *A, const void 
     ga.B = ptrs->b.data();
     ga.out = ptrs->out.data();
     return ga;
+}
+
+// In-place gather (the plan's fused_gather): per GEMM operand slot (a rank),
+// the shard of each block of its all-gather group, in grid order, into
+// a_src / b_src, which must outlive the launch.
+void attach_gather(const shmm_plan_t *p, const void *const *A_r, const void *const *B_r,
+                   const std::vector<int> &slot_rank, shmm::GemmArgs *ga, std::vector<const void *> *a_src,
+                   std::vector<const void *> *b_src) {
+    if (!p->fused_gather) return;
+    auto shard_table = [&](const shmm::Groups &g, const void *const *shards, std::vector<const void *> *out) {
+        out->assign(slot_rank.size() * g.size, nullptr);
+        for (size_t i = 0; i < slot_rank.size(); ++i) {
+            int gi = 0;
+            for (size_t j = 0; j < g.members.size(); ++j)
+                if (g.members[j] == slot_rank[i]) gi = (int)j / g.size;
+            for (int q = 0; q < g.size; ++q) (*out)[i * g.size + q] = shards[g.by_block[gi * g.size + q]];
+        }
+    };
+    if (p->gA.n) {
+        shard_table(p->gA_groups, A_r, a_src);
+        ga->A_src = a_src->data();
+        ga->a_b0 = p->gA_groups.blocks0;
+        ga->a_b1 = p->gA_groups.blocks1;
+        ga->a_brows = p->boxes[SHMM_TENSOR_A][0].ext[0];
+        ga->a_bcols = p->boxes[SHMM_TENSOR_A][0].ext[1];
+    }
+    if (p->gB.n) {
+        shard_table(p->gB_groups, B_r, b_src);
+        ga->B_src = b_src->data();
+        ga->b_b0 = p->gB_groups.blocks0;
+        ga->b_b1 = p->gB_groups.blocks1;
+        ga->b_brows = p->boxes[SHMM_TENSOR_B][0].ext[0];
+        ga->b_bcols = p->boxes[SHMM_TENSOR_B][0].ext[1];
+    }
 }
 
 // Streams shmm_run_host copies on, created once per device and kept for the
@@ -476,38 +510,7 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         if (e) return cuda_fail(fn, e, "gather B");
         for (int r = 0; r < p->nranks; ++r) B_loc[r] = wb[r];
     }
-    // In-place gather: per GEMM operand slot (a rank), the shard of each
-    // block of its all-gather group, in grid order.
     std::vector<const void *> a_src, b_src;
-    auto shard_table = [&](const shmm::Groups &g, const void *const *shards, const std::vector<int> &slot_rank,
-                           std::vector<const void *> *out) {
-        out->assign(slot_rank.size() * g.size, nullptr);
-        for (size_t i = 0; i < slot_rank.size(); ++i) {
-            int gi = 0;
-            for (size_t j = 0; j < g.members.size(); ++j)
-                if (g.members[j] == slot_rank[i]) gi = (int)j / g.size;
-            for (int q = 0; q < g.size; ++q) (*out)[i * g.size + q] = shards[g.by_block[gi * g.size + q]];
-        }
-    };
-    auto attach_gather = [&](shmm::GemmArgs *ga, const std::vector<int> &slot_rank) {
-        if (!p->fused_gather) return;
-        if (p->gA.n) {
-            shard_table(p->gA_groups, A_r, slot_rank, &a_src);
-            ga->A_src = a_src.data();
-            ga->a_b0 = p->gA_groups.blocks0;
-            ga->a_b1 = p->gA_groups.blocks1;
-            ga->a_brows = p->boxes[SHMM_TENSOR_A][0].ext[0];
-            ga->a_bcols = p->boxes[SHMM_TENSOR_A][0].ext[1];
-        }
-        if (p->gB.n) {
-            shard_table(p->gB_groups, B_r, slot_rank, &b_src);
-            ga->B_src = b_src.data();
-            ga->b_b0 = p->gB_groups.blocks0;
-            ga->b_b1 = p->gB_groups.blocks1;
-            ga->b_brows = p->boxes[SHMM_TENSOR_B][0].ext[0];
-            ga->b_bcols = p->boxes[SHMM_TENSOR_B][0].ext[1];
-        }
-    };
     const bool fused = p->fused;
     if (p->U.n && !fused) carve(SHMM_TENSOR_P, shmm::elem_bytes(p->part_dt), &wp);
     std::vector<void *> dst(C_r, C_r + p->nranks);
@@ -519,13 +522,13 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
     if (!p->U.n) {
         shmm::Range phase("local matmul");
         shmm::GemmArgs ga = unit_args(p, A_loc.data(), B_loc.data(), dst.data(), 0, p->nranks, &up);
-        attach_gather(&ga, up.slot_rank);
+        attach_gather(p, A_r, B_r, up.slot_rank, &ga, &a_src, &b_src);
         e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
     } else if (fused) {
         shmm::Range phase("local matmul + fused reduction");
         shmm::GemmArgs ga = unit_args(p, A_loc.data(), B_loc.data(), dst.data(), 0, p->red_groups.count, &up);
-        attach_gather(&ga, up.slot_rank);
+        attach_gather(p, A_r, B_r, up.slot_rank, &ga, &a_src, &b_src);
         e = run_gemm(p, ga, status, stream, &err);
         if (e) return cuda_fail(fn, e, err);
     } else {
@@ -538,7 +541,7 @@ shmm_status_t shmm_run(const shmm_plan_t *p, const void *const *A_r, const void 
         ga.out = wp.data();
         std::vector<int> by_rank(p->nranks);
         for (int r = 0; r < p->nranks; ++r) by_rank[r] = r;
-        attach_gather(&ga, by_rank);
+        attach_gather(p, A_r, B_r, by_rank, &ga, &a_src, &b_src);
         {
             shmm::Range phase("local matmul");
             e = run_gemm(p, ga, status, stream, &err);
@@ -653,6 +656,71 @@ shmm_status_t shmm_run_static_workspace(const shmm_plan_t *p, const void *const 
         if (!ws) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
     }
     return shmm_run(p, A_r, B_r, C_r, ws, need, stream);
+}
+
+shmm_status_t shmm_run_batch(int n, const shmm_plan_t *const *plans, const void *const *const *A_r,
+                             const void *const *const *B_r, void *const *const *C_r, void *const *workspaces,
+                             const size_t *workspace_bytes, void *stream) {
+    static const char *fn = "shmm_run_batch";
+    shmm::clear_error();
+    shmm::Range range(fn);
+    if (n < 0) return fail(SHMM_ERR_SHAPE, std::string(fn) + ": n < 0");
+    if (n == 0) return SHMM_OK;
+    if (!plans || !A_r || !B_r || !C_r) return fail(SHMM_ERR_NULL, std::string(fn) + ": NULL array");
+    if (injected(fn)) return fail(SHMM_ERR_INJECTED, std::string(fn) + ": injected failure");
+    // Everything is checked before anything is enqueued.
+    for (int i = 0; i < n; ++i) {
+        const shmm_plan_t *p = plans[i];
+        const std::string at = std::string(fn) + " (plan " + std::to_string(i) + ")";
+        if (!p) return fail(SHMM_ERR_NULL, at + ": plan is NULL");
+        shmm_status_t st;
+        if ((st = check_ptrs(p, A_r[i], SHMM_TENSOR_A, at.c_str(), "A_r")) != SHMM_OK) return st;
+        if ((st = check_ptrs(p, B_r[i], SHMM_TENSOR_B, at.c_str(), "B_r")) != SHMM_OK) return st;
+        if ((st = check_ptrs(p, (const void *const *)C_r[i], SHMM_TENSOR_C, at.c_str(), "C_r")) != SHMM_OK)
+            return st;
+        if ((st = check_workspace(p, workspaces ? workspaces[i] : nullptr, workspace_bytes ? workspace_bytes[i] : 0,
+                                  at.c_str())) != SHMM_OK)
+            return st;
+    }
+    std::string err;
+    int *status = status_ptr(&err);
+    if (!status) return fail(SHMM_ERR_CUDA, std::string(fn) + ": " + err);
+    // A plan whose shmm_run is one tensor-core GEMM launch (operands read in
+    // place or whole, a fused reduction or none, the result where the GEMM
+    // writes it) joins the shared launch; any other plan runs as shmm_run.
+    std::vector<int> joined;
+    for (int i = 0; i < n; ++i) {
+        const shmm_plan_t *p = plans[i];
+        const bool one_launch = p->tensor_core && (!p->gA.n || p->fused_gather) &&
+                                (!p->gB.n || p->fused_gather) && (!p->U.n || p->fused) && !p->gC.n &&
+                                shmm::tcgen05_supported(gemm_args(p));
+        if (one_launch) {
+            joined.push_back(i);
+            continue;
+        }
+        const shmm_status_t st = shmm_run(p, A_r[i], B_r[i], C_r[i], workspaces ? workspaces[i] : nullptr,
+                                          workspace_bytes ? workspace_bytes[i] : 0, stream);
+        if (st != SHMM_OK) return st;
+    }
+    if (joined.empty()) return SHMM_OK;
+    // Per joined plan: its GEMM arguments and the pointer tables they refer
+    // to (kept alive until the launch is enqueued).
+    std::vector<UnitPtrs> up(joined.size());
+    std::vector<std::vector<const void *>> a_src(joined.size()), b_src(joined.size());
+    std::vector<shmm::GemmArgs> ga(joined.size());
+    for (size_t j = 0; j < joined.size(); ++j) {
+        const int i = joined[j];
+        const shmm_plan_t *p = plans[i];
+        ga[j] = unit_args(p, A_r[i], B_r[i], C_r[i], 0, p->U.n ? p->red_groups.count : p->nranks, &up[j]);
+        attach_gather(p, A_r[i], B_r[i], up[j].slot_rank, &ga[j], &a_src[j], &b_src[j]);
+    }
+    int e;
+    {
+        shmm::Range phase("local matmuls of the batch");
+        e = shmm::launch_gemm_tcgen05(ga.data(), (int)ga.size(), status, stream, &err);
+    }
+    if (e) return cuda_fail(fn, e, err);
+    return SHMM_OK;
 }
 
 shmm_status_t shmm_run_host(const shmm_plan_t *p, const void *A_host, const void *B_host, void *C_host,

@@ -676,17 +676,19 @@ __global__ void __launch_bounds__(256) copy_rects_kernel(const __grid_constant__
             for (int u = 0; u < U; ++u)
                 if (ok[u]) __stcs(reinterpret_cast<uint4 *>(R.dst) + doff[u], x[u]);
         }
-        return;
-    }
-    for (IT v = (IT)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (IT)gridDim.x * blockDim.x) {
-        const IT row = v / per_row, c = v - row * per_row;
-        if (!in_bounds(k.status, (int64_t)(row * sld + c), 1, sroom) ||
-            !in_bounds(k.status, (int64_t)(row * dld + c), 1, droom))
-            continue;
-        if (elem == 4) {
-            reinterpret_cast<uint32_t *>(R.dst)[row * dld + c] = reinterpret_cast<const uint32_t *>(R.src)[row * sld + c];
-        } else {
-            reinterpret_cast<uint16_t *>(R.dst)[row * dld + c] = reinterpret_cast<const uint16_t *>(R.src)[row * sld + c];
+    } else {
+        for (IT v = (IT)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (IT)gridDim.x * blockDim.x) {
+            const IT row = v / per_row, c = v - row * per_row;
+            if (!in_bounds(k.status, (int64_t)(row * sld + c), 1, sroom) ||
+                !in_bounds(k.status, (int64_t)(row * dld + c), 1, droom))
+                continue;
+            if (elem == 4) {
+                reinterpret_cast<uint32_t *>(R.dst)[row * dld + c] =
+                    reinterpret_cast<const uint32_t *>(R.src)[row * sld + c];
+            } else {
+                reinterpret_cast<uint16_t *>(R.dst)[row * dld + c] =
+                    reinterpret_cast<const uint16_t *>(R.src)[row * sld + c];
+            }
         }
     }
 }

@@ -40,6 +40,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "checked.cuh"
 #include "device_wait.cuh"
@@ -53,28 +54,50 @@ constexpr int UMMA_K = 16;       // K of one tcgen05.mma kind::f16
 constexpr int kMaxMaps = 16;     // rank operand pairs per launch
 constexpr int kThreads = 192;
 
-struct TcK {
-    CUtensorMap tmA[kMaxMaps];   // one map per distinct A shard of the launch
-    CUtensorMap tmB[kMaxMaps];
-    void *out[kMaxMaps];
-    CUtensorMap tmC[kMaxMaps];  // output i as the epilogue's TMA stores see it
-    int *status;
+constexpr int kMaxSegs = 4;      // products (sharded matmuls) per launch
+
+// One product of a launch: its units' local GEMMs (ranks, or reduction
+// groups when fused), shapes and output mode.  A launch runs the work items
+// of its segments one after another in one persistent tile walk.
+struct TcSeg {
+    int tile_base;   // first work item of the segment
     int units, G, mode;
     int fused, gelu, out_f32;
     int accum;  // fused: the group's products accumulate in one TMEM buffer
     int64_t M, N, Kd;
     int m_tiles, n_tiles, k_blocks;
-    // operand slot i's block p (row-major over a b0 x b1 grid of brows x bcols
-    // shards) is map a_idx[i][p]; an operand read whole has one 1x1 block
-    uint8_t a_idx[kMaxMaps][kMaxMaps];
-    uint8_t b_idx[kMaxMaps][kMaxMaps];
+    int slot_base;   // operand slots slot_base + unit * Gq + q
+    int out_base;    // outputs out_base + unit (unfused) or + unit * G + b
+    // each operand slot is a b0 x b1 grid of brows x bcols shards (1 x 1
+    // when the operand is read whole)
     int a_b0, a_b1, b_b0, b_b1;
     int64_t a_brows, a_bcols, b_brows, b_bcols;
-    int n_maps_a, n_maps_b;
-    int gathered;  // 0: map i is operand slot i's own buffer
     int tma_store;  // 1: the epilogue stores through tmC, else per-thread stores
     int64_t out_n;  // elements per output buffer (per-thread stores, bounds-checked build)
 };
+
+struct TcK {
+    CUtensorMap tmA[kMaxMaps];   // one map per distinct A buffer or shard of the launch
+    CUtensorMap tmB[kMaxMaps];
+    void *out[kMaxMaps];
+    CUtensorMap tmC[kMaxMaps];  // output i as the epilogue's TMA stores see it
+    int *status;
+    // operand slot i's block p (row-major over its segment's b0 x b1 grid) is
+    // map a_idx[i][p]
+    uint8_t a_idx[kMaxMaps][kMaxMaps];
+    uint8_t b_idx[kMaxMaps][kMaxMaps];
+    int n_maps_a, n_maps_b;
+    int nseg, total;  // segments; work items of all segments
+    TcSeg seg[kMaxSegs];
+};
+
+// The segment holding work item t.
+__device__ __forceinline__ int seg_of(const TcK &k, int t) {
+    int si = 0;
+    for (int i = 1; i < k.nseg; ++i)
+        if (t >= k.seg[i].tile_base) si = i;
+    return si;
+}
 
 // Operands read in place from an all-gather group's shards: which shard of
 // the b0 x b1 grid holds coordinate `x` along one dim, and the coordinate
@@ -365,56 +388,60 @@ __device__ __forceinline__ void store_run(void *p, const float *v, int n, bool f
 // unit `unit`: the rank's own block (unfused), the owner's block of a
 // reduce-scatter along rows (mode 0) or columns (mode 1), or every group
 // member's copy (mode 2).
-__device__ __forceinline__ void store_tile_row(const TcK &k, int unit, int Gq, int64_t row, int64_t col0,
-                                               const float *v, int n, bool f32, int64_t es) {
-    if (!k.fused) {
-        const int64_t off = row * k.N + col0;
-        if (!in_bounds(k.status, off, n, k.out_n)) return;
-        store_run((char *)k.out[unit] + off * es, v, n, f32, true);
-    } else if (k.mode == 0) {
-        const int64_t per = k.M / Gq;
+__device__ __forceinline__ void store_tile_row(const TcK &k, const TcSeg &g, int unit, int Gq, int64_t row,
+                                               int64_t col0, const float *v, int n, bool f32, int64_t es) {
+    void *const *out = k.out + g.out_base;
+    if (!g.fused) {
+        const int64_t off = row * g.N + col0;
+        if (!in_bounds(k.status, off, n, g.out_n)) return;
+        store_run((char *)out[unit] + off * es, v, n, f32, true);
+    } else if (g.mode == 0) {
+        const int64_t per = g.M / Gq;
         const int b = (int)(row / per);
-        const int64_t off = (row - b * per) * k.N + col0;
-        if (!in_bounds(k.status, off, n, k.out_n)) return;
-        store_run((char *)k.out[unit * Gq + b] + off * es, v, n, f32, true);
-    } else if (k.mode == 1) {
-        const int64_t per = k.N / Gq;
+        const int64_t off = (row - b * per) * g.N + col0;
+        if (!in_bounds(k.status, off, n, g.out_n)) return;
+        store_run((char *)out[unit * Gq + b] + off * es, v, n, f32, true);
+    } else if (g.mode == 1) {
+        const int64_t per = g.N / Gq;
         if ((per % 32) == 0) {
             const int b = (int)(col0 / per);
             const int64_t off = row * per + (col0 - b * per);
-            if (!in_bounds(k.status, off, n, k.out_n)) return;
-            store_run((char *)k.out[unit * Gq + b] + off * es, v, n, f32, true);
+            if (!in_bounds(k.status, off, n, g.out_n)) return;
+            store_run((char *)out[unit * Gq + b] + off * es, v, n, f32, true);
         } else {
             for (int i = 0; i < n; ++i) {
                 const int64_t col = col0 + i;
                 const int b = (int)(col / per);
                 const int64_t off = row * per + (col - b * per);
-                if (!in_bounds(k.status, off, 1, k.out_n)) continue;
-                store_run((char *)k.out[unit * Gq + b] + off * es, v + i, 1, f32, false);
+                if (!in_bounds(k.status, off, 1, g.out_n)) continue;
+                store_run((char *)out[unit * Gq + b] + off * es, v + i, 1, f32, false);
             }
         }
     } else {
-        const int64_t off = row * k.N + col0;
-        if (!in_bounds(k.status, off, n, k.out_n)) return;
-        for (int b = 0; b < Gq; ++b) store_run((char *)k.out[unit * Gq + b] + off * es, v, n, f32, true);
+        const int64_t off = row * g.N + col0;
+        if (!in_bounds(k.status, off, n, g.out_n)) return;
+        for (int b = 0; b < Gq; ++b) store_run((char *)out[unit * Gq + b] + off * es, v, n, f32, true);
     }
 }
 
-// Work item t -> (unit, m-tile, n-tile).  Within a unit the tiles run in
+// Work item t -> (segment, unit, m-tile, n-tile).  Within a unit the tiles run in
 // bands of kBandM m-tiles: m fastest inside a band, then n, then the next
 // band.  The CTAs working at one time then cover a roughly square block of
 // the output (about 8 x 9.5 tiles for 76 CTA pairs) instead of a few whole
 // columns, so each wave streams fewer A row panels and B column panels from
 // DRAM.
 constexpr int kBandM = 8;
-__device__ __forceinline__ void tile_coords(const TcK &k, int t, int *unit, int *mt, int *nt) {
-    const int per_unit = k.m_tiles * k.n_tiles;
+__device__ __forceinline__ void tile_coords(const TcK &k, int t, int *si, int *unit, int *mt, int *nt) {
+    *si = seg_of(k, t);
+    const TcSeg &g = k.seg[*si];
+    t -= g.tile_base;
+    const int per_unit = g.m_tiles * g.n_tiles;
     *unit = t / per_unit;
     const int r = t - *unit * per_unit;
-    const int band_tiles = kBandM * k.n_tiles;
+    const int band_tiles = kBandM * g.n_tiles;
     const int band = r / band_tiles;
     const int m0 = band * kBandM;
-    const int bm = k.m_tiles - m0 < kBandM ? k.m_tiles - m0 : kBandM;  // the last band may be short
+    const int bm = g.m_tiles - m0 < kBandM ? g.m_tiles - m0 : kBandM;  // the last band may be short
     const int q = r - band * band_tiles;
     *mt = m0 + q % bm;
     *nt = q / bm;
@@ -467,19 +494,20 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int r, const float *v, b
 // block of a reduce-scatter, or every member's copy of an all-reduce.
 // Stores clip at the output's edges.  `staged` counts the warp's boxes (it
 // picks the box).
-__device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, int row0, int col_base, int c0,
-                                               int c1, uint32_t lane_s, uint32_t cbuf, uint32_t share,
-                                               uint32_t *staged, int lane) {
-    const bool f32 = k.out_f32 != 0;
+__device__ __forceinline__ void store_tile_tma(const TcK &k, const TcSeg &g, int unit, int Gq, int row0,
+                                               int col_base, int c0, int c1, uint32_t lane_s, uint32_t cbuf,
+                                               uint32_t share, uint32_t *staged, int lane) {
+    const bool f32 = g.out_f32 != 0;
+    const CUtensorMap *tmC = k.tmC + g.out_base;
     const uint32_t box = f32 ? 4096u : 2048u;
     const uint32_t nbuf = share / box;  // 1, 2 or 4
 #pragma unroll 1
     for (int c = c0; c < c1; ++c) {
         const int col0 = col_base + c * 32;
-        if (col0 >= k.N) break;
+        if (col0 >= g.N) break;
         float v[32];
         tmem_ld32(lane_s + (uint32_t)(c * 32), v);
-        if (k.gelu) {
+        if (g.gelu) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
         }
@@ -490,16 +518,16 @@ __device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, i
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (!k.fused) {
-                tma_store_2d(&k.tmC[unit], buf, col0, row0);
-            } else if (k.mode == 0) {
-                const int per = (int)(k.M / Gq), b = row0 / per;
-                tma_store_2d(&k.tmC[unit * Gq + b], buf, col0, row0 - b * per);
-            } else if (k.mode == 1) {
-                const int per = (int)(k.N / Gq), b = col0 / per;
-                tma_store_2d(&k.tmC[unit * Gq + b], buf, col0 - b * per, row0);
+            if (!g.fused) {
+                tma_store_2d(&tmC[unit], buf, col0, row0);
+            } else if (g.mode == 0) {
+                const int per = (int)(g.M / Gq), b = row0 / per;
+                tma_store_2d(&tmC[unit * Gq + b], buf, col0, row0 - b * per);
+            } else if (g.mode == 1) {
+                const int per = (int)(g.N / Gq), b = col0 / per;
+                tma_store_2d(&tmC[unit * Gq + b], buf, col0 - b * per, row0);
             } else {
-                for (int b = 0; b < Gq; ++b) tma_store_2d(&k.tmC[unit * Gq + b], buf, col0, row0);
+                for (int b = 0; b < Gq; ++b) tma_store_2d(&tmC[unit * Gq + b], buf, col0, row0);
             }
             bulk_commit();
         }
@@ -520,13 +548,10 @@ __device__ __forceinline__ void store_tile_tma(const TcK &k, int unit, int Gq, i
 // full_bar(b): the barrier on which the MMA thread reports a finished
 // product in buffer b; release(b): hands buffer b back.
 template <int NH, typename FullBar, typename Release>
-__device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride, int total, int Gq, int tile_rows,
-                                            int row_base, uint32_t lane_base, int c0, int c1, uint32_t cbuf,
-                                            uint32_t share, int lane, volatile int *abort_flag, FullBar full_bar,
-                                            Release release) {
+__device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride, int tile_rows, int row_base,
+                                            uint32_t lane_base, int c0, int c1, uint32_t cbuf, uint32_t share,
+                                            int lane, volatile int *abort_flag, FullBar full_bar, Release release) {
     constexpr int BN = 256;
-    const bool f32 = k.out_f32 != 0;
-    const int64_t es = f32 ? 4 : 2;
     uint32_t staged = 0;
     uint32_t used0 = 0, used1 = 0;  // finished products consumed per buffer
     // One lane waits; the warp reconverges before the .sync.aligned TMEM
@@ -543,9 +568,13 @@ __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride,
     };
     int tile_iter = 0;
     bool ok = true;
-    for (int t = first; t < total && ok; t += stride, ++tile_iter) {
-        int unit, mt, nt;
-        tile_coords(k, t, &unit, &mt, &nt);
+    for (int t = first; t < k.total && ok; t += stride, ++tile_iter) {
+        int si, unit, mt, nt;
+        tile_coords(k, t, &si, &unit, &mt, &nt);
+        const TcSeg &g = k.seg[si];
+        const int Gq = g.fused ? g.G : 1;
+        const bool f32 = g.out_f32 != 0;
+        const int64_t es = f32 ? 4 : 2;
         for (int h = 0; h < NH && ok; ++h) {
             const int bS = NH == 2 ? h : (tile_iter & 1), bW = bS ^ 1;
             const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
@@ -554,7 +583,7 @@ __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride,
                 ok = false;
                 break;
             }
-            const int folds = k.accum || NH == 2 ? 1 : Gq;  // accum: S already holds the sum
+            const int folds = g.accum || NH == 2 ? 1 : Gq;  // accum: S already holds the sum
             for (int q = 1; q < folds; ++q) {
                 // S = S + P_q in fp32: the ascending-rank sequential sum
                 if (!warp_wait_full(bW)) {
@@ -576,24 +605,24 @@ __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride,
             if (!ok) break;
             const int row0 = mt * tile_rows + row_base;
             const int col_base = (nt * NH + h) * BN;
-            if (k.tma_store) {
-                if (row0 < k.M)
-                    store_tile_tma(k, unit, Gq, row0, col_base, c0, c1, s_base, cbuf, share, &staged, lane);
+            if (g.tma_store) {
+                if (row0 < g.M)
+                    store_tile_tma(k, g, unit, Gq, row0, col_base, c0, c1, s_base, cbuf, share, &staged, lane);
             } else {
                 const int64_t row = (int64_t)row0 + lane;
-                const bool row_ok = row < k.M;
+                const bool row_ok = row < g.M;
 #pragma unroll 1
                 for (int c = c0; c < c1; ++c) {
                     float v[32];
                     tmem_ld32(s_base + (uint32_t)(c * 32), v);
-                    if (k.gelu) {
+                    if (g.gelu) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
                     }
                     const int64_t col0 = (int64_t)col_base + c * 32;
-                    if (!row_ok || col0 >= k.N) continue;
-                    const int n = (int)((k.N - col0) < 32 ? (k.N - col0) : 32);
-                    store_tile_row(k, unit, Gq, row, col0, v, n, f32, es);
+                    if (!row_ok || col0 >= g.N) continue;
+                    const int n = (int)((g.N - col0) < 32 ? (g.N - col0) : 32);
+                    store_tile_row(k, g, unit, Gq, row, col0, v, n, f32, es);
                 }
             }
             release(bS);  // S may take the next tile's products
@@ -625,21 +654,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-    // In-place gathers only: block -> shard-map tables, copied once from the
-    // parameters into the shared-memory tail (a byte load from the parameter
-    // block on every TMA issue stalls the producer).
+    // Operand slot -> map tables, copied once from the parameters into the
+    // shared-memory tail (the producer looks a tile's maps up there).
     uint8_t *s_aidx = reinterpret_cast<uint8_t *>(tmem_holder + 16);
     uint8_t *s_bidx = s_aidx + kMaxMaps * kMaxMaps;
-    if (k.gathered)
-        for (int i = threadIdx.x; i < kMaxMaps * kMaxMaps; i += blockDim.x) {
-            s_aidx[i] = k.a_idx[i / kMaxMaps][i % kMaxMaps];
-            s_bidx[i] = k.b_idx[i / kMaxMaps][i % kMaxMaps];
-        }
+    for (int i = threadIdx.x; i < kMaxMaps * kMaxMaps; i += blockDim.x) {
+        s_aidx[i] = k.a_idx[i / kMaxMaps][i % kMaxMaps];
+        s_bidx[i] = k.b_idx[i / kMaxMaps][i % kMaxMaps];
+    }
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int Gq = k.fused ? k.G : 1;
-    const int tiles_per_unit = k.m_tiles * k.n_tiles;
-    const int total = k.units * tiles_per_unit;
+    const int total = k.total;
 
     auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
     auto empty_bar = [&](int s) { return smem_u32(&bars[S + s]); };
@@ -672,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    auto decode = [&](int t, int *unit, int *mt, int *nt) { tile_coords(k, t, unit, mt, nt); };
+    auto decode = [&](int t, int *si, int *unit, int *mt, int *nt) { tile_coords(k, t, si, unit, mt, nt); };
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -684,31 +709,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             for (int s = 0; s < 8; ++s) last_parity[s] = -1;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                int unit, mt, nt;
-                decode(t, &unit, &mt, &nt);
+                int si, unit, mt, nt;
+                decode(t, &si, &unit, &mt, &nt);
+                const TcSeg &g = k.seg[si];
+                const int Gq = g.fused ? g.G : 1;
                 for (int q = 0; q < Gq && ok; ++q) {
-                    const int ri = unit * Gq + q;
-                    int32_t a_r;
-                    const int a_p0 = shard_split(k.a_b0, k.a_brows, (int64_t)mt * BM, &a_r);
-                    // In-place gathers: the row of A and each B box's column
-                    // shard are fixed for the tile; the K shards advance.
+                    const int ri = g.slot_base + unit * Gq + q;
+                    // The slot's maps are looked up once per tile: the row of A
+                    // and each B box's column shard are fixed for it; the K
+                    // shards (in-place gathers split K) advance.
                     constexpr int NB = BN / 64;
-                    KWalk wa, wb;
-                    int32_t bx[NB];
+                    int32_t a_r, bx[NB];
                     int bp1[NB];
-                    const CUtensorMap *map_a = &k.tmA[ri];
+                    const int a_p0 = shard_split(g.a_b0, g.a_brows, (int64_t)mt * BM, &a_r);
+                    KWalk wa, wb;
+                    wa.start(g.a_b1, g.a_bcols);
+                    wb.start(g.b_b0, g.b_brows);
+                    const CUtensorMap *map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * g.a_b1 + wa.p]];
                     const CUtensorMap *map_b[NB];
-                    if (k.gathered) {
-                        wa.start(k.a_b1, k.a_bcols);
-                        wb.start(k.b_b0, k.b_brows);
-                        map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + wa.p]];
 #pragma unroll
-                        for (int c = 0; c < NB; ++c) {
-                            bp1[c] = shard_split(k.b_b1, k.b_bcols, (int64_t)nt * BN + c * 64, &bx[c]);
-                            map_b[c] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * k.b_b1 + bp1[c]]];
-                        }
+                    for (int c = 0; c < NB; ++c) {
+                        bp1[c] = shard_split(g.b_b1, g.b_bcols, (int64_t)nt * BN + c * 64, &bx[c]);
+                        map_b[c] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * g.b_b1 + bp1[c]]];
                     }
-                    for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
+                    for (int kb = 0; kb < g.k_blocks; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, k.status)) {
@@ -718,23 +742,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         mbar_expect_tx(full_bar(s), C::STAGE);
                         const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
                         const uint32_t b_dst = a_dst + C::A_BYTES;
-                        if (!k.gathered) {
-                            tma_load_2d(a_dst, &k.tmA[ri], full_bar(s), kb * BK, mt * BM);
+                        tma_load_2d(a_dst, map_a, full_bar(s), wa.local, a_r);
 #pragma unroll
-                            for (int c = 0; c < BN / 64; ++c)
-                                tma_load_2d(b_dst + c * 8192, &k.tmB[ri], full_bar(s), nt * BN + c * 64, kb * BK);
-                        } else {
-                            tma_load_2d(a_dst, map_a, full_bar(s), wa.local, a_r);
+                        for (int c = 0; c < NB; ++c) tma_load_2d(b_dst + c * 8192, map_b[c], full_bar(s), bx[c], wb.local);
+                        if (wa.advance(g.a_b1, g.a_bcols, BK))
+                            map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * g.a_b1 + wa.p]];
+                        if (wb.advance(g.b_b0, g.b_brows, BK))
 #pragma unroll
-                            for (int c = 0; c < NB; ++c)
-                                tma_load_2d(b_dst + c * 8192, map_b[c], full_bar(s), bx[c], wb.local);
-                            if (wa.advance(k.a_b1, k.a_bcols, BK))
-                                map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + wa.p]];
-                            if (wb.advance(k.b_b0, k.b_brows, BK))
-#pragma unroll
-                                for (int c = 0; c < NB; ++c)
-                                    map_b[c] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * k.b_b1 + bp1[c]]];
-                        }
+                            for (int c = 0; c < NB; ++c) map_b[c] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * g.b_b1 + bp1[c]]];
                         last_parity[s] = (int)ph;
                     }
                 }
@@ -760,19 +775,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int tile_iter = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_iter) {
+                const TcSeg &g = k.seg[seg_of(k, t)];
+                const int Gq = g.fused ? g.G : 1;
+                const bool accum = g.accum != 0;
+                const int k_blocks = g.k_blocks;
                 const int bS = tile_iter & 1;
                 for (int q = 0; q < Gq && ok; ++q) {
                     // accum: every rank's product continues the sum in S
-                    const bool into_s = q == 0 || k.accum;
+                    const bool into_s = q == 0 || accum;
                     const int b = into_s ? bS : (bS ^ 1);
                     const uint32_t nf = b ? fills1 : fills0;
-                    if ((q == 0 || !k.accum) && !mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
+                    if ((q == 0 || !accum) && !mbar_wait(acce_bar(b), (nf & 1) ^ 1, abort_flag, k.status)) {
                         ok = false;
                         break;
                     }
                     fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
-                    for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
+                    for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(full_bar(s), ph, abort_flag, k.status)) {
@@ -788,12 +807,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                             // swizzle row.  B: MN-major, 16 k rows = 2 atoms.
                             const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
                             const uint64_t bd = smem_desc(b_addr + kk * 2048, 8192, 1024);
-                            umma_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0 || (q > 0 && k.accum)) ? 1u : 0u);
+                            umma_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0 || (q > 0 && accum)) ? 1u : 0u);
                         }
                         umma_commit(empty_bar(s));
                     }
                     if (!ok) break;
-                    if (k.accum && q < Gq - 1) continue;  // S is not finished
+                    if (accum && q < Gq - 1) continue;  // S is not finished
                     umma_commit(accf_bar(b));
                     if (b) ++fills1;
                     else ++fills0;
@@ -806,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int quad = warp % 4;
-        drain_tiles<1>(k, blockIdx.x, gridDim.x, total, Gq, BM, quad * 32, tmem_base + ((uint32_t)(quad * 32) << 16),
+        drain_tiles<1>(k, blockIdx.x, gridDim.x, BM, quad * 32, tmem_base + ((uint32_t)(quad * 32) << 16),
                        0, BN / 32, smem_u32(staging) + (uint32_t)((warp - 2) * (kStagingBytes / 4)),
                        kStagingBytes / 4, lane, abort_flag,
                     [&](int b) { return accf_bar(b); },
@@ -878,24 +897,20 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
     // handoff_bar (both used in the leader CTA only).
     volatile uint32_t *peer_issued = tmem_holder + 2;
     uint64_t *handoff = reinterpret_cast<uint64_t *>(tmem_holder + 4);
-    // In-place gathers only: block -> shard-map tables, copied once from the
-    // parameters into the shared-memory tail (a byte load from the parameter
-    // block on every TMA issue stalls the producer).
+    // Operand slot -> map tables, copied once from the parameters into the
+    // shared-memory tail (the producer looks a tile's maps up there).
     uint8_t *s_aidx = reinterpret_cast<uint8_t *>(tmem_holder + 16);
     uint8_t *s_bidx = s_aidx + kMaxMaps * kMaxMaps;
-    if (k.gathered)
-        for (int i = threadIdx.x; i < kMaxMaps * kMaxMaps; i += blockDim.x) {
-            s_aidx[i] = k.a_idx[i / kMaxMaps][i % kMaxMaps];
-            s_bidx[i] = k.b_idx[i / kMaxMaps][i % kMaxMaps];
-        }
+    for (int i = threadIdx.x; i < kMaxMaps * kMaxMaps; i += blockDim.x) {
+        s_aidx[i] = k.a_idx[i / kMaxMaps][i % kMaxMaps];
+        s_bidx[i] = k.b_idx[i / kMaxMaps][i % kMaxMaps];
+    }
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t cr = cluster_ctarank();  // 0: leader, 1: peer
     const uint32_t handoff_bar = smem_u32(handoff);
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    const int Gq = k.fused ? k.G : 1;
-    const int tiles_per_unit = k.m_tiles * k.n_tiles;  // 256 x TW tiles
-    const int total = k.units * tiles_per_unit;
+    const int total = k.total;  // 256 x TW tiles of every segment
 
     auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
     auto empty_bar = [&](int s) { return smem_u32(&bars[S + s]); };
@@ -932,7 +947,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    auto decode = [&](int t, int *unit, int *mt, int *nt) { tile_coords(k, t, unit, mt, nt); };
+    auto decode = [&](int t, int *si, int *unit, int *mt, int *nt) { tile_coords(k, t, si, unit, mt, nt); };
 
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
@@ -942,32 +957,31 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
             uint32_t it = 0;  // stages loaded
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                int unit, mt, nt;
-                decode(t, &unit, &mt, &nt);
+                int si, unit, mt, nt;
+                decode(t, &si, &unit, &mt, &nt);
+                const TcSeg &g = k.seg[si];
+                const int Gq = g.fused ? g.G : 1;
                 for (int q = 0; q < Gq && ok; ++q) {
-                    const int ri = unit * Gq + q;
-                    int32_t a_r;
-                    const int a_p0 = shard_split(k.a_b0, k.a_brows, (int64_t)mt * 256 + (int)cr * BM, &a_r);
-                    // In-place gathers: the row of A and each B box's column
-                    // shard are fixed for the tile; the K shards advance.
+                    const int ri = g.slot_base + unit * Gq + q;
+                    // The slot's maps are looked up once per tile: the row of A
+                    // and each B box's column shard are fixed for it; the K
+                    // shards (in-place gathers split K) advance.
                     constexpr int NB = 2 * NH;
-                    KWalk wa, wb;
-                    int32_t bx[NB];
+                    int32_t a_r, bx[NB];
                     int bp1[NB];
-                    const CUtensorMap *map_a = &k.tmA[ri];
+                    const int a_p0 = shard_split(g.a_b0, g.a_brows, (int64_t)mt * 256 + (int)cr * BM, &a_r);
+                    KWalk wa, wb;
+                    wa.start(g.a_b1, g.a_bcols);
+                    wb.start(g.b_b0, g.b_brows);
+                    const CUtensorMap *map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * g.a_b1 + wa.p]];
                     const CUtensorMap *map_b[NB];
-                    if (k.gathered) {
-                        wa.start(k.a_b1, k.a_bcols);
-                        wb.start(k.b_b0, k.b_brows);
-                        map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + wa.p]];
 #pragma unroll
-                        for (int j = 0; j < NB; ++j) {
-                            bp1[j] = shard_split(k.b_b1, k.b_bcols,
-                                                 (int64_t)nt * TW + (j / 2) * BN + (int)cr * 128 + (j % 2) * 64, &bx[j]);
-                            map_b[j] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * k.b_b1 + bp1[j]]];
-                        }
+                    for (int j = 0; j < NB; ++j) {
+                        bp1[j] = shard_split(g.b_b1, g.b_bcols,
+                                             (int64_t)nt * TW + (j / 2) * BN + (int)cr * 128 + (j % 2) * 64, &bx[j]);
+                        map_b[j] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * g.b_b1 + bp1[j]]];
                     }
-                    for (int kb = 0; kb < k.k_blocks; ++kb, ++it) {
+                    for (int kb = 0; kb < g.k_blocks; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, k.status)) {
@@ -978,26 +992,14 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                         const uint32_t bar = mapa_shared(full_bar(s), 0);
                         const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
                         const uint32_t b_dst = a_dst + C::A_BYTES;
-                        if (!k.gathered) {
-                            tma_load_2d_pair(a_dst, &k.tmA[ri], bar, kb * BK, mt * 256 + (int)cr * BM);
+                        tma_load_2d_pair(a_dst, map_a, bar, wa.local, a_r);
 #pragma unroll
-                            for (int h = 0; h < NH; ++h)
+                        for (int j = 0; j < NB; ++j) tma_load_2d_pair(b_dst + j * 8192, map_b[j], bar, bx[j], wb.local);
+                        if (wa.advance(g.a_b1, g.a_bcols, BK))
+                            map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * g.a_b1 + wa.p]];
+                        if (wb.advance(g.b_b0, g.b_brows, BK))
 #pragma unroll
-                                for (int c = 0; c < 2; ++c)
-                                    tma_load_2d_pair(b_dst + (h * 2 + c) * 8192, &k.tmB[ri], bar,
-                                                     nt * TW + h * BN + (int)cr * 128 + c * 64, kb * BK);
-                        } else {
-                            tma_load_2d_pair(a_dst, map_a, bar, wa.local, a_r);
-#pragma unroll
-                            for (int j = 0; j < NB; ++j)
-                                tma_load_2d_pair(b_dst + j * 8192, map_b[j], bar, bx[j], wb.local);
-                            if (wa.advance(k.a_b1, k.a_bcols, BK))
-                                map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * k.a_b1 + wa.p]];
-                            if (wb.advance(k.b_b0, k.b_brows, BK))
-#pragma unroll
-                                for (int j = 0; j < NB; ++j)
-                                    map_b[j] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * k.b_b1 + bp1[j]]];
-                        }
+                            for (int j = 0; j < NB; ++j) map_b[j] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * g.b_b1 + bp1[j]]];
                     }
                 }
             }
@@ -1037,14 +1039,18 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
             int tile_iter = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs, ++tile_iter) {
+                const TcSeg &g = k.seg[seg_of(k, t)];
+                const int Gq = g.fused ? g.G : 1;
+                const bool accum = g.accum != 0;
+                const int k_blocks = g.k_blocks;
                 // NH = 1: the tile's sum S in buffer tile_iter % 2 (rank order:
                 // later products in the other); NH = 2: half h in buffer h
                 const int bS = NH == 2 ? 0 : (tile_iter & 1);
                 for (int q = 0; q < Gq && ok; ++q) {
                     // accum: every rank's product continues the sum in S
-                    const bool into_s = q == 0 || k.accum;
+                    const bool into_s = q == 0 || accum;
                     const int b = into_s ? bS : (bS ^ 1);
-                    const bool fresh = q == 0 || !k.accum;  // this product starts its buffers
+                    const bool fresh = q == 0 || !accum;  // this product starts its buffers
                     // The four K=16 MMAs of the k-block in stage st into buffer
                     // buf, half h of the stage's B; `first` starts the buffer's
                     // sum instead of adding to it.
@@ -1072,7 +1078,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                         // epilogue still drains half 1 of the previous tile, then half 1
                         // catches up on the same stages; each half still adds its
                         // k-blocks in ascending order.
-                        const int R = k.k_blocks < S ? k.k_blocks : S;
+                        const int R = k_blocks < S ? k_blocks : S;
                         if (!wait_free(b)) {
                             ok = false;
                             break;
@@ -1097,7 +1103,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                         }
                         it += (uint32_t)R;
                     }
-                    for (; kb < k.k_blocks && ok; ++kb, ++it) {
+                    for (; kb < k_blocks && ok; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(full_bar(s), ph, abort_flag, k.status)) {
@@ -1111,13 +1117,13 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                                 ok = false;
                                 break;
                             }
-                            issue(s, b + h, h, kb == 0 && !(q > 0 && k.accum));
+                            issue(s, b + h, h, kb == 0 && !(q > 0 && accum));
                         }
                         if (!ok) break;
                         umma2_commit_both(empty_bar(s));
                     }
                     if (!ok) break;
-                    if (k.accum && q < Gq - 1) continue;  // S is not finished
+                    if (accum && q < Gq - 1) continue;  // S is not finished
 #pragma unroll
                     for (int h = 0; h < NH; ++h) {
                         umma2_commit_both(accf_bar(b + h));
@@ -1137,7 +1143,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
         constexpr int CH = (BN / 32) / (C::EPI_WARPS / 4);  // 32-column chunks per warp
         const int c0 = (ew / 4) * CH;
         constexpr uint32_t share = kStagingBytes / C::EPI_WARPS;
-        drain_tiles<NH>(k, pair, npairs, total, Gq, 256, (int)cr * BM + quad * 32,
+        drain_tiles<NH>(k, pair, npairs, 256, (int)cr * BM + quad * 32,
                     tmem_base + ((uint32_t)(quad * 32) << 16), c0, c0 + CH,
                     smem_u32(staging) + (uint32_t)ew * share, share, lane, abort_flag,
                     [&](int b) { return accf_bar(b); },
@@ -1249,6 +1255,20 @@ int num_sms() {
     return n;
 }
 
+// Tile grid of every segment for tiles of tile_rows x tile_cols: the
+// segments' work items follow one another in segment order.
+void set_tiles(TcK &k, int tile_rows, int tile_cols) {
+    int base = 0;
+    for (int i = 0; i < k.nseg; ++i) {
+        TcSeg &g = k.seg[i];
+        g.m_tiles = (int)((g.M + tile_rows - 1) / tile_rows);
+        g.n_tiles = (int)((g.N + tile_cols - 1) / tile_cols);
+        g.tile_base = base;
+        base += g.units * g.m_tiles * g.n_tiles;
+    }
+    k.total = base;
+}
+
 template <int BN>
 cudaError_t launch_bn(TcK &k, cudaStream_t s, int max_sms) {
     using C = Cfg<BN>;
@@ -1262,8 +1282,8 @@ cudaError_t launch_bn(TcK &k, cudaStream_t s, int max_sms) {
         if (e != cudaSuccess) return e;
         attr_set.set(dev, 1);
     }
-    k.n_tiles = (int)((k.N + BN - 1) / BN);
-    const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
+    set_tiles(k, BM, BN);
+    const int64_t total = k.total;
     int ctas = num_sms();
     if (max_sms > 0 && max_sms < ctas) ctas = max_sms;
     const int grid = (int)(total < ctas ? total : ctas);
@@ -1330,9 +1350,8 @@ cudaError_t launch_pair(TcK &k, cudaStream_t s, int max_sms) {
     if (ce != cudaSuccess) return ce;
     if (cap < 1) return cudaErrorNotSupported;  // no pair can be resident: the caller falls back
     cap = limit_pairs(cap, max_sms);
-    k.m_tiles = (int)((k.M + 255) / 256);
-    k.n_tiles = (int)((k.N + 256 * NH - 1) / (256 * NH));
-    const int64_t total = (int64_t)k.units * k.m_tiles * k.n_tiles;
+    set_tiles(k, 256, 256 * NH);
+    const int64_t total = k.total;
     const int npairs = (int)(total < cap ? total : cap);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -1369,20 +1388,32 @@ bool pair_kernel_enabled() {
 // Pick the smaller estimate: waves x work per tile x that factor.
 // SHMM_TC_WIDE=0 / 1 forces 256- / 512-column tiles (tests compare them).
 int pair_halves(const TcK &k, int max_sms) {
-    if (k.fused && !k.accum && k.G > 1) return 1;  // the rank-order fold needs TMEM's second buffer
+    bool wide_ok = false;
+    for (int i = 0; i < k.nseg; ++i) {
+        const TcSeg &g = k.seg[i];
+        if (g.fused && !g.accum && g.G > 1) return 1;  // the rank-order fold needs TMEM's second buffer
+        if (g.N > 256) wide_ok = true;
+    }
     const char *env = getenv("SHMM_TC_WIDE");
     if (env && env[0] == '0') return 1;
     if (env && env[0] == '1') return 2;
-    if (k.N <= 256) return 1;
+    if (!wide_ok) return 1;
     int cap1 = 0, cap2 = 0;
     if (pair_capacity<1>(&cap1) != cudaSuccess || pair_capacity<2>(&cap2) != cudaSuccess || cap1 < 1 || cap2 < 1)
         return 1;
     cap1 = limit_pairs(cap1, max_sms);
     cap2 = limit_pairs(cap2, max_sms);
-    const int64_t m_t = (k.M + 255) / 256;
-    const int64_t t1 = (int64_t)k.units * m_t * ((k.N + 255) / 256);
-    const int64_t t2 = (int64_t)k.units * m_t * ((k.N + 511) / 512);
-    const double kb = (double)k.k_blocks * (k.fused && k.accum ? k.G : 1);  // k-blocks per tile
+    int64_t t1 = 0, t2 = 0;
+    double kb_sum = 0.0;  // k-blocks over the wide tiles (weights the per-tile estimate)
+    for (int i = 0; i < k.nseg; ++i) {
+        const TcSeg &g = k.seg[i];
+        const int64_t m_t = (g.M + 255) / 256;
+        const int64_t w = (int64_t)g.units * m_t * ((g.N + 511) / 512);
+        t1 += (int64_t)g.units * m_t * ((g.N + 255) / 256);
+        t2 += w;
+        kb_sum += (double)w * g.k_blocks * (g.fused && g.accum ? g.G : 1);
+    }
+    const double kb = t2 > 0 ? kb_sum / (double)t2 : 1.0;  // k-blocks per tile
     const double narrow = (double)((t1 + cap1 - 1) / cap1);
     const double wide = (double)((t2 + cap2 - 1) / cap2) * 2.0 * 0.88 * (1.0 + 4.0 / kb);
     return wide < narrow ? 2 : 1;
@@ -1399,118 +1430,155 @@ bool tcgen05_supported(const GemmArgs &a) {
            a.Kd <= ((int64_t)1 << 31);
 }
 
-int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::string *msg) {
+int launch_gemm_tcgen05(const GemmArgs *args, int nargs, int *status, void *stream, std::string *msg) {
     EncodeTiledFn fn = encode_fn(msg);
     if (!fn) return (int)cudaErrorNotSupported;
-    const int G = a.fused ? a.G : 1;
-    constexpr int bn = 256;
-    const int per_launch = kMaxMaps / G;  // units per launch
     cudaStream_t s = (cudaStream_t)stream;
-    for (int u0 = 0; u0 < a.units; u0 += per_launch) {
-        const int nu = (a.units - u0) < per_launch ? (a.units - u0) : per_launch;
-        TcK k;
-        memset(&k, 0, sizeof k);
-        // One tensor map per distinct operand buffer (a shard may serve
-        // every member of its all-gather group); per slot, a block table.
-        const void *ptrs_a[kMaxMaps], *ptrs_b[kMaxMaps];
-        int na = 0, nb = 0;
-        const bool gathered = a.A_src || a.B_src;
-        auto map_of = [&](const void *ptr, const void **ptrs, int *n, CUtensorMap *maps, int64_t rows,
-                          int64_t cols, uint32_t bx, uint32_t by) -> int {
-            if (gathered)  // a shard may serve several slots: one map each
-                for (int j = 0; j < *n; ++j)
-                    if (ptrs[j] == ptr) return j;
-            if (*n >= kMaxMaps) return -1;
-            if (!cached_map(fn, &maps[*n], ptr, rows, cols, bx, by)) return -2;
-            ptrs[*n] = ptr;
-            return (*n)++;
-        };
+    // Chunks of units (at most kMaxMaps operand slots each), grouped by the
+    // kernel they need: CTA pairs (local M above one 128-row tile) or single
+    // CTAs.  Each launch packs consecutive chunks of one group as segments.
+    struct Chunk {
+        const GemmArgs *a;
+        int u0, nu;
+    };
+    std::vector<Chunk> groups[2];  // [0] pair kernel, [1] single-CTA kernel
+    for (int i = 0; i < nargs; ++i) {
+        const GemmArgs &a = args[i];
+        const int G = a.fused ? a.G : 1;
         const int a_nb = a.A_src ? a.a_b0 * a.a_b1 : 1;
         const int b_nb = a.B_src ? a.b_b0 * a.b_b1 : 1;
-        const int64_t a_rows = a.A_src ? a.a_brows : a.M, a_cols = a.A_src ? a.a_bcols : a.Kd;
-        const int64_t b_rows = a.B_src ? a.b_brows : a.Kd, b_cols = a.B_src ? a.b_bcols : a.N;
         if (a_nb > kMaxMaps || b_nb > kMaxMaps) {
             if (msg) *msg = "all-gather group larger than one launch's operand maps";
             return (int)cudaErrorInvalidValue;
         }
-        for (int i = 0; i < nu * G; ++i) {
-            const int gi = u0 * G + i;
-            for (int p = 0; p < a_nb; ++p) {
-                const void *ptr = a.A_src ? a.A_src[(size_t)gi * a_nb + p] : a.A[gi];
-                const int m = map_of(ptr, ptrs_a, &na, k.tmA, a_rows, a_cols, BK, BM);
-                if (m < 0) {
-                    if (msg) *msg = m == -1 ? "more than 16 distinct A buffers in one launch"
-                                            : "cuTensorMapEncodeTiled rejected an A operand";
+        const int per_launch = kMaxMaps / G;  // units per launch
+        const int grp = (a.M > BM && pair_kernel_enabled()) ? 0 : 1;
+        for (int u0 = 0; u0 < a.units; u0 += per_launch)
+            groups[grp].push_back({&a, u0, (a.units - u0) < per_launch ? (a.units - u0) : per_launch});
+    }
+    for (int grp = 0; grp < 2; ++grp) {
+        const std::vector<Chunk> &chunks = groups[grp];
+        size_t ci = 0;
+        while (ci < chunks.size()) {
+            TcK k;
+            memset(&k, 0, sizeof k);
+            // One tensor map per distinct operand buffer (a shard may serve
+            // several slots, and plans may share buffers); per slot, a block
+            // table.
+            const void *ptrs_a[kMaxMaps], *ptrs_b[kMaxMaps];
+            int64_t dims_a[kMaxMaps][2], dims_b[kMaxMaps][2];
+            int na = 0, nb = 0, slots = 0, outs = 0;
+            bool limited = true;  // every segment carries an SM limit
+            int max_sms = 0;
+            auto map_of = [&](const void *ptr, const void **ptrs, int64_t (*dims)[2], int *n, CUtensorMap *maps,
+                              int64_t rows, int64_t cols, uint32_t bx, uint32_t by) -> int {
+                for (int j = 0; j < *n; ++j)
+                    if (ptrs[j] == ptr && dims[j][0] == rows && dims[j][1] == cols) return j;
+                if (*n >= kMaxMaps) return -1;
+                if (!cached_map(fn, &maps[*n], ptr, rows, cols, bx, by)) return -2;
+                ptrs[*n] = ptr;
+                dims[*n][0] = rows;
+                dims[*n][1] = cols;
+                return (*n)++;
+            };
+            while (ci < chunks.size() && k.nseg < kMaxSegs) {
+                const Chunk &c = chunks[ci];
+                const GemmArgs &a = *c.a;
+                const int G = a.fused ? a.G : 1;
+                const int nout = a.fused ? c.nu * G : c.nu;
+                if (slots + c.nu * G > kMaxMaps || outs + nout > kMaxMaps) break;
+                const int a_nb = a.A_src ? a.a_b0 * a.a_b1 : 1;
+                const int b_nb = a.B_src ? a.b_b0 * a.b_b1 : 1;
+                const int64_t a_rows = a.A_src ? a.a_brows : a.M, a_cols = a.A_src ? a.a_bcols : a.Kd;
+                const int64_t b_rows = a.B_src ? a.b_brows : a.Kd, b_cols = a.B_src ? a.b_bcols : a.N;
+                const int na0 = na, nb0 = nb;
+                int m = 0;
+                for (int i = 0; i < c.nu * G && m >= 0; ++i) {
+                    const int gi = c.u0 * G + i;
+                    for (int p = 0; p < a_nb && m >= 0; ++p) {
+                        const void *ptr = a.A_src ? a.A_src[(size_t)gi * a_nb + p] : a.A[gi];
+                        m = map_of(ptr, ptrs_a, dims_a, &na, k.tmA, a_rows, a_cols, BK, BM);
+                        if (m >= 0) k.a_idx[slots + i][p] = (uint8_t)m;
+                    }
+                    for (int p = 0; p < b_nb && m >= 0; ++p) {
+                        const void *ptr = a.B_src ? a.B_src[(size_t)gi * b_nb + p] : a.B[gi];
+                        m = map_of(ptr, ptrs_b, dims_b, &nb, k.tmB, b_rows, b_cols, 64, BK);
+                        if (m >= 0) k.b_idx[slots + i][p] = (uint8_t)m;
+                    }
+                }
+                if (m == -2) {
+                    if (msg) *msg = "cuTensorMapEncodeTiled rejected an operand";
                     return (int)cudaErrorInvalidValue;
                 }
-                k.a_idx[i][p] = (uint8_t)m;
-            }
-            for (int p = 0; p < b_nb; ++p) {
-                const void *ptr = a.B_src ? a.B_src[(size_t)gi * b_nb + p] : a.B[gi];
-                const int m = map_of(ptr, ptrs_b, &nb, k.tmB, b_rows, b_cols, 64, BK);
-                if (m < 0) {
-                    if (msg) *msg = m == -1 ? "more than 16 distinct B buffers in one launch"
-                                            : "cuTensorMapEncodeTiled rejected a B operand";
-                    return (int)cudaErrorInvalidValue;
+                if (m == -1) {  // out of maps: this chunk starts the next launch
+                    na = na0;
+                    nb = nb0;
+                    if (k.nseg == 0) {
+                        if (msg) *msg = "more than 16 distinct operand buffers in one chunk";
+                        return (int)cudaErrorInvalidValue;
+                    }
+                    break;
                 }
-                k.b_idx[i][p] = (uint8_t)m;
+                TcSeg &g = k.seg[k.nseg++];
+                g.units = c.nu;
+                g.G = G;
+                g.mode = a.mode;
+                g.fused = a.fused ? 1 : 0;
+                g.accum = a.fused && !a.rank_order ? 1 : 0;
+                g.gelu = a.gelu ? 1 : 0;
+                g.out_f32 = a.out_dt == SHMM_F32 ? 1 : 0;
+                g.M = a.M;
+                g.N = a.N;
+                g.Kd = a.Kd;
+                g.k_blocks = (int)((a.Kd + BK - 1) / BK);
+                g.slot_base = slots;
+                g.out_base = outs;
+                g.a_b0 = a.A_src ? a.a_b0 : 1;
+                g.a_b1 = a.A_src ? a.a_b1 : 1;
+                g.b_b0 = a.B_src ? a.b_b0 : 1;
+                g.b_b1 = a.B_src ? a.b_b1 : 1;
+                g.a_brows = a_rows;
+                g.a_bcols = a_cols;
+                g.b_brows = b_rows;
+                g.b_bcols = b_cols;
+                for (int i = 0; i < nout; ++i) k.out[outs + i] = a.out[(a.fused ? c.u0 * G : c.u0) + i];
+                // Output maps for the TMA-store epilogue: each destination block
+                // as rows x cols, 32 x 32 boxes.  A reduce-scatter's owner
+                // blocks must hold whole 32-row (32-column) boxes, else
+                // per-thread stores.
+                const bool out_f32 = a.out_dt == SHMM_F32;
+                int64_t c_rows = a.M, c_cols = a.N;
+                bool tma_store = true;
+                if (a.fused && a.mode == 0) {
+                    c_rows = a.M / G;
+                    tma_store = c_rows % 32 == 0;
+                } else if (a.fused && a.mode == 1) {
+                    c_cols = a.N / G;
+                    tma_store = c_cols % 32 == 0;
+                }
+                if ((c_cols * (out_f32 ? 4 : 2)) % 16) tma_store = false;
+                for (int i = 0; i < nout && tma_store; ++i)
+                    tma_store = cached_map(fn, &k.tmC[outs + i], k.out[outs + i], c_rows, c_cols, 32, 32, out_f32,
+                                           out_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                g.tma_store = tma_store ? 1 : 0;
+                g.out_n = c_rows * c_cols;  // an owner's block, or a whole copy
+                slots += c.nu * G;
+                outs += nout;
+                if (a.max_sms <= 0) limited = false;
+                else if (a.max_sms > max_sms) max_sms = a.max_sms;
+                ++ci;
             }
+            k.n_maps_a = na;
+            k.n_maps_b = nb;
+            k.status = status;
+            if (!limited) max_sms = 0;
+            // 256-row tiles on CTA pairs unless the local M fits one 128-row tile
+            cudaError_t e = cudaErrorNotSupported;
+            if (grp == 0)
+                e = pair_halves(k, max_sms) == 2 ? launch_pair<2>(k, s, max_sms) : launch_pair<1>(k, s, max_sms);
+            if (e == cudaErrorNotSupported) e = launch_bn<256>(k, s, max_sms);  // single CTAs when no pair fits
+            if (e != cudaSuccess) return (int)e;
         }
-        k.n_maps_a = na;
-        k.n_maps_b = nb;
-        k.gathered = gathered ? 1 : 0;
-        k.a_b0 = a.A_src ? a.a_b0 : 1;
-        k.a_b1 = a.A_src ? a.a_b1 : 1;
-        k.b_b0 = a.B_src ? a.b_b0 : 1;
-        k.b_b1 = a.B_src ? a.b_b1 : 1;
-        k.a_brows = a_rows;
-        k.a_bcols = a_cols;
-        k.b_brows = b_rows;
-        k.b_bcols = b_cols;
-        const int nout = a.fused ? nu * G : nu;
-        for (int i = 0; i < nout; ++i) k.out[i] = a.out[(a.fused ? u0 * G : u0) + i];
-        // Output maps for the TMA-store epilogue: each destination block as
-        // rows x cols, 32 x 32 boxes.  A reduce-scatter's owner blocks must
-        // hold whole 32-row (32-column) boxes, else per-thread stores.
-        const bool out_f32 = a.out_dt == SHMM_F32;
-        int64_t c_rows = a.M, c_cols = a.N;
-        bool tma_store = true;
-        if (a.fused && a.mode == 0) {
-            c_rows = a.M / G;
-            tma_store = c_rows % 32 == 0;
-        } else if (a.fused && a.mode == 1) {
-            c_cols = a.N / G;
-            tma_store = c_cols % 32 == 0;
-        }
-        if ((c_cols * (out_f32 ? 4 : 2)) % 16) tma_store = false;
-        for (int i = 0; i < nout && tma_store; ++i)
-            tma_store = cached_map(fn, &k.tmC[i], k.out[i], c_rows, c_cols, 32, 32, out_f32,
-                                   out_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-        k.tma_store = tma_store ? 1 : 0;
-        k.status = status;
-        k.units = nu;
-        k.G = G;
-        k.mode = a.mode;
-        k.fused = a.fused ? 1 : 0;
-        k.accum = a.fused && !a.rank_order ? 1 : 0;
-        k.gelu = a.gelu ? 1 : 0;
-        k.out_f32 = a.out_dt == SHMM_F32 ? 1 : 0;
-        k.M = a.M;
-        k.N = a.N;
-        k.Kd = a.Kd;
-        k.out_n = c_rows * c_cols;  // an owner's block, or a whole copy
-        k.m_tiles = (int)((a.M + BM - 1) / BM);
-        k.k_blocks = (int)((a.Kd + BK - 1) / BK);
-        // 256-row tiles on CTA pairs unless the local M fits one 128-row tile
-        cudaError_t e = cudaErrorNotSupported;
-        if (a.M > BM && pair_kernel_enabled())
-            e = pair_halves(k, a.max_sms) == 2 ? launch_pair<2>(k, s, a.max_sms) : launch_pair<1>(k, s, a.max_sms);
-        if (e == cudaErrorNotSupported) {
-            // single-CTA tiles when no CTA pair fits (or is wanted)
-            k.m_tiles = (int)((a.M + BM - 1) / BM);
-            e = launch_bn<bn>(k, s, a.max_sms);
-        }
-        if (e != cudaSuccess) return (int)e;
     }
     return 0;
 }

@@ -197,8 +197,10 @@ struct GemmArgs {
 };
 int launch_gemm_simt(const GemmArgs &a, int *status, void *stream);
 bool tcgen05_supported(const GemmArgs &a);
+// Local GEMMs of `n` independent products in as few launches as the
+// kernels' tables allow (several products share one persistent tile walk).
 // Returns a cudaError_t value; sets *msg on a failure outside CUDA.
-int launch_gemm_tcgen05(const GemmArgs &a, int *status, void *stream, std::string *msg);
+int launch_gemm_tcgen05(const GemmArgs *a, int n, int *status, void *stream, std::string *msg);
 
 // Count of kernels enqueued by this library since it was loaded.
 void count_launch(int n = 1);

@@ -84,7 +84,7 @@ EXPORTS = ["shmm_plan", "shmm_plan_destroy", "shmm_plan_query", "shmm_plan_rank_
            "shmm_all_reduce", "shmm_all_gather", "shmm_run", "shmm_sync_status", "shmm_last_error",
            "shmm_status_string", "shmm_version", "shmm_kernel_launches", "shmm_run_static_workspace",
            "shmm_selftest_wait_timeout", "shmm_choose_operand", "shmm_reshard", "shmm_layernorm",
-           "shmm_layernorm_all_gather", "shmm_run_host", "shmm_bounds_checked"]
+           "shmm_layernorm_all_gather", "shmm_run_host", "shmm_bounds_checked", "shmm_run_batch"]
 
 _lib = None
 
@@ -118,6 +118,8 @@ def lib():
         L.shmm_all_gather.argtypes = [P, ctypes.c_int, PP, PP, P]
         L.shmm_run.argtypes = [P, PP, PP, PP, P, ctypes.c_size_t, P]
         L.shmm_run_static_workspace.argtypes = [P, PP, PP, PP, P]
+        L.shmm_run_batch.argtypes = [ctypes.c_int, PP, ctypes.POINTER(PP), ctypes.POINTER(PP), ctypes.POINTER(PP),
+                                     PP, ctypes.POINTER(ctypes.c_size_t), P]
         L.shmm_run_host.argtypes = [P, P, P, P, PP, PP, PP, P, ctypes.c_size_t, P]
         L.shmm_sync_status.argtypes = [P]
         L.shmm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
@@ -415,6 +417,22 @@ def shmm_all_gather(plan: Plan, tensor: int, shard_r, full_r, stream=None):
 
 def shmm_run(plan: Plan, A_r, B_r, C_r, workspace=None, stream=None):
     plan.run(A_r, B_r, C_r, workspace, stream)
+
+
+def shmm_run_batch(plans: Sequence[Plan], A_r, B_r, C_r, workspaces=None, stream=None):
+    """Independent sharded matmuls whose local GEMMs share launches (see
+    include/shmm.h).  A_r, B_r, C_r: per plan, its list of per-rank tensors;
+    workspaces: per plan, a workspace tensor or None."""
+    n = len(plans)
+    keep = [[_ptr_array(t, w) for t in lists] for lists, w in ((A_r, "A"), (B_r, "B"), (C_r, "C"))]
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    tables = [(PP * n)(*[ctypes.cast(a, PP) for a in arrs]) for arrs in keep]
+    ws = list(workspaces) if workspaces is not None else [None] * n
+    ws_ptr = (ctypes.c_void_p * n)(*[None if w is None else w.data_ptr() for w in ws])
+    ws_bytes = (ctypes.c_size_t * n)(*[0 if w is None else w.numel() * w.element_size() for w in ws])
+    handles = (ctypes.c_void_p * n)(*[p.handle.value for p in plans])
+    _check(lib().shmm_run_batch(n, handles, tables[0], tables[1], tables[2], ws_ptr, ws_bytes,
+                                _stream_handle(stream)))
 
 
 def shmm_run_host(plan: Plan, A_host, B_host, C_host, A_r, B_r, C_r, workspace=None, stream=None):

@@ -358,3 +358,28 @@ def test_sm_limit_argument_checks(shmm):
         p.set_sm_limit(-1)
     assert e.value.status == shmm.shmm.ERR_SHAPE
     assert shmm.lib().shmm_plan_set_sm_limit(None, 4) == shmm.shmm.ERR_NULL
+
+
+def test_run_batch_argument_checks(shmm):
+    """Every plan and pointer is checked before anything is enqueued; the
+    message names the offending plan."""
+    L = shmm.lib()
+    import ctypes
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    assert L.shmm_run_batch(0, None, None, None, None, None, None, None) == shmm.shmm.OK
+    assert L.shmm_run_batch(-1, None, None, None, None, None, None, None) == shmm.shmm.ERR_SHAPE
+    assert L.shmm_run_batch(1, None, None, None, None, None, None, None) == shmm.shmm.ERR_NULL
+    p0 = shmm.Plan("{X:2,Y:2}", "I_X,J", "J,K_Y", "I_X,K_Y", 512, 256, 512, "bf16", "bf16")
+    p1 = shmm.Plan("{X:2,Y:2}", "I,J_Y", "J_Y,K", "I_Y,K", 512, 256, 512, "bf16", "bf16", shmm.FLAG_FUSED)
+    good = (ctypes.c_void_p * 4)(*([0x10000] * 4))
+    bad = (ctypes.c_void_p * 4)(*([0x10008] * 4))   # not 16-byte aligned
+    handles = (ctypes.c_void_p * 2)(p0.handle.value, p1.handle.value)
+    g = ctypes.cast(good, PP)
+    b = ctypes.cast(bad, PP)
+    A = (PP * 2)(g, g)
+    B = (PP * 2)(g, b)
+    C = (PP * 2)(g, g)
+    assert L.shmm_run_batch(2, handles, A, B, C, None, None, None) == shmm.shmm.ERR_ALIGN
+    assert b"plan 1" in L.shmm_last_error()
+    handles_null = (ctypes.c_void_p * 2)(p0.handle.value, None)
+    assert L.shmm_run_batch(2, handles_null, A, A, C, None, None, None) == shmm.shmm.ERR_NULL

@@ -781,6 +781,55 @@ def test_sm_limit_keeps_the_bits(s, case, sA, sB, sC, limit, monkeypatch):
             assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("wide", ["0", "1", None])
+def test_run_batch_equals_separate_runs(s, wide, monkeypatch):
+    """Independent plans through shmm_run_batch give the bits of their own
+    shmm_run calls: the four cases (in-place gathers, a fused reduce-scatter)
+    sharing one launch, a GeLU plan with fp32 output, a rank-order fused
+    all-reduce, a plan whose local M fits one 128-row tile (single-CTA
+    kernel), and an unfused reduction that runs through shmm_run; more
+    operand slots than one launch holds, so the joined plans take two."""
+    from partial_sum_reduction_gb300 import helpers as H
+    if wide is None:
+        monkeypatch.delenv("SHMM_TC_WIDE", raising=False)
+    else:
+        monkeypatch.setenv("SHMM_TC_WIDE", wide)
+    A, B = shmm_inputs.scaled_normal_pair(1024, 512, 768, "bf16", seed=50)
+    specs = [(XY22, sA, sB, sC, "bf16", s.FLAG_FUSED, A, B) for _, sA, sB, sC in FOUR]
+    A2, B2 = shmm_inputs.scaled_normal_pair(512, 256, 1024, "bf16", seed=51)
+    specs.append((X8, ((), ()), ((), ("X",)), ((), ("X",)), "f32", s.FLAG_GELU, A2, B2))
+    A3, B3 = shmm_inputs.scaled_normal_pair(1024, 1024, 512, "bf16", seed=52)
+    specs.append((XY42, (("X",), ("Y",)), (("Y",), ()), (("X",), ()), "bf16", s.FLAG_FUSED | s.FLAG_RANK_ORDER,
+                  A3, B3))
+    A4, B4 = shmm_inputs.scaled_normal_pair(256, 512, 320, "bf16", seed=53)
+    specs.append((XY22, (("X",), ()), ((), ("Y",)), (("X",), ("Y",)), "bf16", 0, A4, B4))   # local M = 128
+    specs.append((XY22, ((), ("Y",)), (("Y",), ()), (("Y",), ()), "bf16", 0, A, B))       # unfused reduction
+    plans, ins, refs, outs, wss = [], [], [], [], []
+    for mesh, sA, sB, sC, odt, fl, a, b in specs:
+        I, J = a.shape
+        K = b.shape[1]
+        p = s.Plan(mesh, sA, sB, sC, I, J, K, "bf16", odt, fl)
+        A_r, B_r = H.shard(p, s.TENSOR_A, a), H.shard(p, s.TENSOR_B, b)
+        ref = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+        p.run(A_r, B_r, ref, H.workspace(p))
+        plans.append(p)
+        ins.append((A_r, B_r))
+        refs.append(ref)
+        outs.append(H.alloc(p, s.TENSOR_C, fill=float("nan")))
+        wss.append(H.workspace(p))
+    launches = s.shmm_kernel_launches()
+    s.shmm_run_batch(plans, [x[0] for x in ins], [x[1] for x in ins], outs, wss)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    launched = s.shmm_kernel_launches() - launches
+    # eight plans, seven of them joined: no more kernels than one per plan
+    assert launched < len(plans)
+    for i, (o, r) in enumerate(zip(outs, refs)):
+        for q, (x, y) in enumerate(zip(o, r)):
+            assert not torch.isnan(x.float()).any(), "plan %d rank %d unwritten" % (i, q)
+            assert torch.equal(x, y), "plan %d rank %d differs from its own shmm_run" % (i, q)
+
+
 @pytest.mark.parametrize("flags", ["FUSED", "FUSED|RANK_ORDER", "0"])
 def test_repeated_runs_give_identical_bits(s, flags):
     """Every path is deterministic: one input gives one result, run after run
