@@ -65,6 +65,10 @@
  *   SHMM_TC_WIDE=0|1   CTA-pair tiles 256 columns wide (0) or 512 (1)
  *                      instead of the launcher's choice.  Both widths give
  *                      the same bits.
+ *   SHMM_LN_BULK=0     LayerNorm (+ all-gather) reads each row with
+ *                      per-thread loads instead of staging several rows
+ *                      in shared memory through the bulk-copy engine.
+ *                      Both give the same bits.
  *   SHMM_INJECT_FAIL=name[,name...]  the named entry points fail with
  *                      SHMM_ERR_INJECTED before enqueuing anything (tests
  *                      of error propagation).

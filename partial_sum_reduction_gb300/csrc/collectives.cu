@@ -19,10 +19,12 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 
 #include "checked.cuh"
+#include "device_wait.cuh"
 #include "shmm_internal.h"
 
 namespace {
@@ -632,6 +634,166 @@ __global__ void __launch_bounds__(256) ln_gather_reg_kernel(const __grid_constan
     }
 }
 
+// Bulk-copy path, same arithmetic per row as the register path (the same
+// vectors per thread, the same block sums): thread 0 keeps `stages` (2 to
+// kLnMaxStages, as many as kLnSmemBudget holds) rows of the
+// CTA's walk in flight through the bulk-copy engine (cp.async.bulk into
+// shared memory, completion counted on one mbarrier per stage), so the row a
+// CTA normalises has landed while the next ones stream in.  The register
+// path has one row in flight per CTA, which leaves a two- or four-rank
+// gather latency-bound (few stores per row to hide the load behind).
+// Thread 0 alone waits on a stage, bounded, and the CTA follows it through
+// __syncthreads, so every thread leaves the loop at the same row; before
+// exit thread 0 waits (bounded) for every copy it issued.
+constexpr int kLnMaxStages = 4;
+template <typename T, int NVT>
+__global__ void __launch_bounds__(256) ln_gather_bulk_kernel(const __grid_constant__ LnK k, int stages) {
+    constexpr int V = 16 / sizeof(T);
+    extern __shared__ __align__(128) uint8_t ln_rows[];  // `stages` rows of cols elements
+    __shared__ __align__(8) uint64_t bars[kLnMaxStages];
+    __shared__ float scratch[32];
+    __shared__ int abort_flag, go;
+    const int g = blockIdx.y;
+    const int64_t rows = (int64_t)k.G * k.brows;
+    const uint32_t row_bytes = (uint32_t)(k.cols * (int64_t)sizeof(T));
+    const float inv_n = 1.0f / (float)k.cols;
+    const int nvec = (int)(k.cols / V);
+    float ga[NVT][V], be[NVT][V];
+#pragma unroll
+    for (int j = 0; j < NVT; ++j) {
+        const int vi = threadIdx.x + j * blockDim.x;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const bool in = vi < nvec && in_bounds(k.status, (int64_t)vi * V + i, 1, k.gb_n);
+            ga[j][i] = in ? k.gamma[(int64_t)vi * V + i] : 0.0f;
+            be[j][i] = in ? k.beta[(int64_t)vi * V + i] : 0.0f;
+        }
+    }
+    auto bar = [&](int st) { return shmm_dev::smem_u32(&bars[st]); };
+    // Thread 0: start the copy of row t into stage st (a plain arrival when
+    // the bounds-checked build finds the row outside its block).
+    auto issue = [&](int st, int64_t t) {
+        const int p = (int)(t / k.brows);
+        const int64_t rr = t - (int64_t)p * k.brows;
+        if (!in_bounds(k.status, rr * k.cols, k.cols, k.src_n)) {
+            shmm_dev::mbar_arrive(bar(st));
+            return;
+        }
+        const char *src = (const char *)k.src[g * k.G + p] + rr * (int64_t)row_bytes;
+        shmm_dev::mbar_expect_tx(bar(st), row_bytes);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                shmm_dev::smem_u32(ln_rows + (size_t)st * row_bytes)),
+            "l"(src), "r"(row_bytes), "r"(bar(st))
+            : "memory");
+    };
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < stages; ++st) shmm_dev::mbar_init(bar(st), 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int st = 0; st < stages; ++st) {
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)st * gridDim.x;
+            if (t < rows) issue(st, t);
+        }
+    }
+    __syncthreads();
+    int it = 0;  // rows this CTA has taken
+    for (int64_t t = blockIdx.x; t < rows; t += gridDim.x, ++it) {
+        const int st = it % stages;
+        if (threadIdx.x == 0) go = shmm_dev::mbar_wait(bar(st), (uint32_t)(it / stages) & 1, &abort_flag, k.status);
+        __syncthreads();
+        if (!go) break;
+        const T *x = reinterpret_cast<const T *>(ln_rows + (size_t)st * row_bytes);
+        float v[NVT][V];
+#pragma unroll
+        for (int j = 0; j < NVT; ++j) {
+            const int vi = threadIdx.x + j * blockDim.x;
+            if (vi < nvec) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(x + (int64_t)vi * V);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                if constexpr (sizeof(T) == 4) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[j][i] = __uint_as_float(ws[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        v[j][2 * i] = __uint_as_float(ws[i] << 16);
+                        v[j][2 * i + 1] = __uint_as_float(ws[i] & 0xffff0000u);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i) v[j][i] = 0.0f;
+            }
+        }
+        const int p = (int)(t / k.brows);
+        const int64_t rr = t - (int64_t)p * k.brows;
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NVT; ++j)
+#pragma unroll
+            for (int i = 0; i < V; ++i) sum += v[j][i];
+        const float mean = block_sum(sum, scratch) * inv_n;
+        float sq = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NVT; ++j) {
+            const int vi = threadIdx.x + j * blockDim.x;
+            if (vi < nvec)
+#pragma unroll
+                for (int i = 0; i < V; ++i) sq += (v[j][i] - mean) * (v[j][i] - mean);
+        }
+        // block_sum's barriers also order every thread's reads of this stage
+        // before thread 0 refills it below
+        const float rstd = 1.0f / sqrtf(block_sum(sq, scratch) * inv_n + k.eps);
+        if (threadIdx.x == 0) {
+            const int64_t next = t + (int64_t)stages * gridDim.x;
+            if (next < rows) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(st, next);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NVT; ++j) {
+            const int vi = threadIdx.x + j * blockDim.x;
+            if (vi >= nvec) continue;
+            float y[V];
+#pragma unroll
+            for (int i = 0; i < V; ++i) y[i] = (v[j][i] - mean) * rstd * ga[j][i] + be[j][i];
+            const int64_t d0 = ((int64_t)p * k.brows + rr) * k.cols + (int64_t)vi * V;
+            if (!in_bounds(k.status, d0, V, k.dst_n)) continue;
+            for (int m = 0; m < k.G; ++m) store_n<T, V>((T *)k.dst[g * k.G + m] + d0, y);
+        }
+    }
+    // Never leave a copy into shared memory in flight at exit.  Row u of this
+    // CTA's walk was issued for u < it + stages and consumed for u < it;
+    // after an abort, wait (bounded) for the issued rows not consumed.
+    if (threadIdx.x == 0) {
+        const int64_t n = rows > (int64_t)blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        for (int64_t u = it; u < n && u < (int64_t)it + stages; ++u)
+            shmm_dev::mbar_wait(bar((int)(u % stages)), (uint32_t)(u / stages) & 1, &abort_flag, k.status, false);
+    }
+}
+
+// Dynamic shared memory the bulk-copy LayerNorm may take per CTA (above the
+// 48 KB default, so each instantiation opts in once per device).
+constexpr int kLnSmemBudget = 64 * 1024;
+template <typename T, int NVT>
+cudaError_t launch_ln_bulk(const LnK &k, dim3 grid, int stages, size_t smem, cudaStream_t s) {
+    static shmm::PerDevice<int> attr_set;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= shmm::kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set.get(dev)) {
+        e = cudaFuncSetAttribute(ln_gather_bulk_kernel<T, NVT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kLnSmemBudget);
+        if (e != cudaSuccess) return e;
+        attr_set.set(dev, 1);
+    }
+    ln_gather_bulk_kernel<T, NVT><<<grid, 256, smem, s>>>(k, stages);
+    return cudaGetLastError();
+}
+
 // ---- reshard: rectangles between rank buffers ------------------------------
 
 constexpr int kMaxRects = 256;  // one launch for a 16-rank all-to-all (16 x 16 rectangles)
@@ -724,6 +886,26 @@ int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream) {
     cudaStream_t s = (cudaStream_t)stream;
     count_launch();
     const int nvt = (int)((a.cols / V + 255) / 256);  // vectors per thread
+    // Rows staged through shared memory by the bulk-copy engine, up to 4 in
+    // flight per CTA within kLnSmemBudget, when at least two fit.
+    const int64_t row_bytes = a.cols * (a.dt == SHMM_F32 ? 4 : 2);
+    int64_t stages = kLnSmemBudget / (row_bytes > 0 ? row_bytes : 1);
+    if (stages > kLnMaxStages) stages = kLnMaxStages;
+    const char *env = getenv("SHMM_LN_BULK");
+    const bool bulk = env ? env[0] != '0' : true;
+    if (reg && bulk && stages >= 2) {
+        const size_t sm = (size_t)stages * (size_t)row_bytes;
+        const int st = (int)stages;
+        cudaError_t e;
+        if (a.dt == SHMM_F32)
+            e = nvt <= 1 ? launch_ln_bulk<float, 1>(k, grid, st, sm, s)
+                         : nvt == 2 ? launch_ln_bulk<float, 2>(k, grid, st, sm, s) : launch_ln_bulk<float, 4>(k, grid, st, sm, s);
+        else
+            e = nvt <= 1 ? launch_ln_bulk<__nv_bfloat16, 1>(k, grid, st, sm, s)
+                         : nvt == 2 ? launch_ln_bulk<__nv_bfloat16, 2>(k, grid, st, sm, s)
+                                    : launch_ln_bulk<__nv_bfloat16, 4>(k, grid, st, sm, s);
+        return (int)e;
+    }
     if (reg && a.dt == SHMM_F32) {
         if (nvt <= 1) ln_gather_reg_kernel<float, 1><<<grid, 256, 0, s>>>(k);
         else if (nvt == 2) ln_gather_reg_kernel<float, 2><<<grid, 256, 0, s>>>(k);

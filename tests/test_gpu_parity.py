@@ -682,6 +682,38 @@ def test_layernorm_rows(s, rows, cols, dtype):
     assert np.abs(got - ref).max() <= tol * np.abs(ref).max()
 
 
+@pytest.mark.parametrize("G,brows,cols,dtype", [(2, 96, 4096, "bf16"), (4, 33, 2048, "f32"), (8, 64, 8192, "bf16"),
+                                                 (2, 17, 8192, "f32"), (3, 40, 1001, "bf16")])
+def test_layernorm_gather_paths_agree(s, G, brows, cols, dtype, monkeypatch):
+    """LayerNorm + all-gather with rows staged through shared memory (the
+    bulk-copy path, several rows in flight per CTA) and with per-thread row
+    loads give the same bits: the same vectors per thread and the same block
+    sums.  Odd row counts leave CTAs with uneven walks; 8192 fp32 columns
+    leave room for two staged rows only; rows of 1001 columns are not whole
+    16-byte vectors (the element-wise path for both settings)."""
+    from partial_sum_reduction_gb300 import helpers as H
+    mesh = [("X", G)]
+    p = s.Plan(mesh, (("X",), ()), ((), ()), ((), ()), G * brows, 8, cols, dtype, dtype)
+    x = shmm_inputs.normal_matrix((G * brows, cols), 2.0, dtype, seed=G + brows)
+    shards = [x[q * brows:(q + 1) * brows].contiguous().cuda() for q in range(G)]
+    gamma = shmm_inputs.normal_matrix((1, cols), 1.0, "f32", seed=3)[0].cuda()
+    beta = shmm_inputs.normal_matrix((1, cols), 1.0, "f32", seed=4)[0].cuda()
+    outs = {}
+    for bulk in ("1", "0"):
+        monkeypatch.setenv("SHMM_LN_BULK", bulk)
+        out = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+        p.layernorm_all_gather(shards, gamma, beta, out)
+        s.shmm_sync_status()
+        torch.cuda.synchronize()
+        outs[bulk] = out
+    ref = oracle.layernorm(x.float().numpy(), gamma.cpu().numpy(), beta.cpu().numpy(), 1e-5, dtype)
+    tol = BF16_TOL if dtype == "bf16" else 1e-4
+    for a, b in zip(outs["1"], outs["0"]):
+        assert torch.equal(a, b)
+        got = a.float().cpu().numpy()
+        assert np.abs(got - ref).max() <= tol * np.abs(ref).max()
+
+
 @pytest.mark.parametrize("fused", [True, False])
 def test_sequence_parallel_mlp_block(s, fused):
     """X -> GeLU(X.W1) (column-parallel) -> .W2 reduce-scattered over tokens
