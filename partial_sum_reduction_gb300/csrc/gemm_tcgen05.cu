@@ -19,6 +19,10 @@
 // 256 x 256 (NH = 1) or 256 x 512 (NH = 2) tiles; gemm_tc_kernel<256> on
 // single CTAs with 128 x 256 tiles, for local M <= 128.
 // Work units are (rank, m-tile, n-tile) or, fused, (group, m-tile, n-tile).
+// A launch may carry several independent products (segments: their tiles
+// follow one another in one persistent walk), each with its own shapes,
+// group size and output mode; operands and outputs are reached through
+// per-launch tensor-map tables.
 // Fused, the G ranks' products of a reduction group accumulate in one fp32
 // TMEM accumulator, rank after rank in ascending order (one contraction over
 // the group's concatenated J); with the rank-order option each rank's
