@@ -92,7 +92,7 @@ def kernel_source_hash():
     import hashlib
     import re
     h = hashlib.sha256()
-    for name in ("gemm_tcgen05.cu", "device_wait.cuh", "checked.cuh"):
+    for name in ("gemm_tcgen05.cu", "device_wait.cuh", "checked.cuh", "gelu.cuh"):
         with open(os.path.join(ROOT, "partial_sum_reduction_gb300", "csrc", name)) as f:
             src = f.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)

@@ -25,6 +25,7 @@
 
 #include "checked.cuh"
 #include "device_wait.cuh"
+#include "gelu.cuh"
 #include "shmm_internal.h"
 
 namespace {
@@ -53,12 +54,6 @@ struct GatherK {
     int *status;                // device status word (bounds-checked build)
     int64_t src_n, dst_n;       // vectors (or elements) per shard / gathered box
 };
-
-__device__ __forceinline__ float gelu_tanh(float x) {
-    // tanh-form GeLU (Hendrycks & Gimpel 2016); sqrt(2/pi) = 0.7978845608...
-    const float inner = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-    return 0.5f * x * (1.0f + tanhf(inner));
-}
 
 // ---- 16-byte vectors of 4 fp32 or 8 bf16 values, widened to fp32 -------
 

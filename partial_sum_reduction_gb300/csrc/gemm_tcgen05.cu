@@ -48,6 +48,7 @@
 
 #include "checked.cuh"
 #include "device_wait.cuh"
+#include "gelu.cuh"
 #include "shmm_internal.h"
 
 namespace {
@@ -350,11 +351,6 @@ __device__ __forceinline__ void umma2_commit_both(uint32_t bar) {
 __host__ __device__ constexpr uint32_t instr_desc_pair(int bn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
            ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
-}
-
-__device__ __forceinline__ float gelu_tanh(float x) {
-    const float inner = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-    return 0.5f * x * (1.0f + tanhf(inner));
 }
 
 // Stores n (<= 32) consecutive values of one row starting at `p` (element

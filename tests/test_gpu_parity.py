@@ -813,6 +813,33 @@ def test_sm_limit_keeps_the_bits(s, case, sA, sB, sC, limit, monkeypatch):
             assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("pair", ["pair_wide", "single"])
+def test_gelu_epilogue_against_the_tanh_form(s, pair, monkeypatch):
+    """The epilogue's GeLU, x / (1 + exp(-2u)) (the tanh form through the
+    logistic identity, fast exponential), against torch's tanh-form GeLU
+    evaluated in fp32 on the same pre-activations: the GEMM's own fp32
+    output without GeLU.  Pre-activations span about +-12, so both tails
+    and the zero crossing are hit."""
+    from partial_sum_reduction_gb300 import helpers as H
+    use_kernel(monkeypatch, pair)
+    I, J, K = 512, 256, 8 * 512
+    A = shmm_inputs.normal_matrix((I, J), 1.0, "bf16", seed=60)
+    B = shmm_inputs.normal_matrix((J, K), 4.0 / J ** 0.5, "bf16", seed=61)
+    outs = []
+    for fl in (0, s.FLAG_GELU):
+        p = s.Plan(X8, ((), ()), ((), ("X",)), ((), ("X",)), I, J, K, "bf16", "f32", fl)
+        A_r, B_r = H.shard(p, s.TENSOR_A, A), H.shard(p, s.TENSOR_B, B)
+        C_r = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+        p.run(A_r, B_r, C_r, H.workspace(p))
+        torch.cuda.synchronize()
+        outs.append(C_r)
+    span = max(float(c.abs().max()) for c in outs[0])
+    assert span > 8.0
+    for pre, got in zip(*outs):
+        ref = torch.nn.functional.gelu(pre, approximate="tanh")
+        assert torch.all((got - ref).abs() <= 1e-5 * ref.abs() + 1e-6), float((got - ref).abs().max())
+
+
 @pytest.mark.parametrize("wide", ["0", "1", None])
 def test_run_batch_equals_separate_runs(s, wide, monkeypatch):
     """Independent plans through shmm_run_batch give the bits of their own
