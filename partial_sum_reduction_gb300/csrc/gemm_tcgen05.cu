@@ -120,11 +120,11 @@ __device__ __forceinline__ int shard_split(int blocks, int64_t extent, int64_t x
     return p;
 }
 
-// The in-place gather's walk along the contracted dim: the shard holding
-// k-block kb and the coordinate inside it, advanced one k-block at a time
-// (shard edges along K fall on k-block edges), so the producer divides only
-// once per tile.  Past the last shard the coordinate keeps growing, as in
-// shard_split.
+// An operand's walk along the contracted dim: the shard holding k-block kb
+// and the coordinate inside it (an operand read whole is one shard), advanced
+// one k-block at a time (an in-place gather's shard edges along K fall on
+// k-block edges), so the producer divides only once per tile.  Past the last
+// shard the coordinate keeps growing, as in shard_split.
 struct KWalk {
     int p;
     int32_t local;
