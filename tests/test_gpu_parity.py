@@ -889,6 +889,37 @@ def test_run_batch_equals_separate_runs(s, wide, monkeypatch):
             assert torch.equal(x, y), "plan %d rank %d differs from its own shmm_run" % (i, q)
 
 
+def test_run_batch_more_plans_than_one_launch_holds(s):
+    """Six joined plans: more segments than one launch carries, so the batch
+    takes two launches; the same plan appears twice with different outputs;
+    every plan carries an SM limit, so each launch takes the largest.  Each
+    output equals the plan's own shmm_run bit for bit."""
+    from partial_sum_reduction_gb300 import helpers as H
+    plans, ins, refs, outs = [], [], [], []
+    shapes = [(512, 256, 320), (768, 512, 256), (512, 128, 512), (1024, 256, 264), (512, 256, 320)]
+    for i, (I, J, K) in enumerate(shapes):
+        A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=70 + i)
+        p = s.Plan(Y2, ((), ("Y",)), (("Y",), ()), ((), ()), I, J, K, "bf16", "bf16", s.FLAG_FUSED)
+        p.set_sm_limit(40 + 8 * i)
+        A_r, B_r = H.shard(p, s.TENSOR_A, A), H.shard(p, s.TENSOR_B, B)
+        ref = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+        p.run(A_r, B_r, ref)
+        copies = 2 if i == 0 else 1   # plan 0 twice, each time into its own outputs
+        for _ in range(copies):
+            plans.append(p)
+            ins.append((A_r, B_r))
+            refs.append(ref)
+            outs.append(H.alloc(p, s.TENSOR_C, fill=float("nan")))
+    launches = s.shmm_kernel_launches()
+    s.shmm_run_batch(plans, [x[0] for x in ins], [x[1] for x in ins], outs)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    assert s.shmm_kernel_launches() - launches == 2
+    for i, (o, r) in enumerate(zip(outs, refs)):
+        for x, y in zip(o, r):
+            assert torch.equal(x, y), "plan %d" % i
+
+
 @pytest.mark.parametrize("flags", ["FUSED", "FUSED|RANK_ORDER", "0"])
 def test_repeated_runs_give_identical_bits(s, flags):
     """Every path is deterministic: one input gives one result, run after run
