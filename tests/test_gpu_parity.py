@@ -440,6 +440,26 @@ def test_fused_equals_unfused_bitwise(s, pair, monkeypatch):
             assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("pair", KERNELS)
+def test_gelu_after_the_reduction_fused_equals_unfused(s, pair, out, monkeypatch):
+    """GeLU of a reduced sum: applied by the standalone reduction kernel,
+    or by the GEMM epilogue after the rank-order fold.  Same sums, same
+    GeLU, so the same bits.  Pre-activations span about +-20: both tails
+    and the zero crossing."""
+    use_kernel(monkeypatch, pair)
+    A = shmm_inputs.normal_matrix((640, 1024), 1.0, "bf16", seed=14)
+    B = shmm_inputs.normal_matrix((1024, 512), 4.0 / 1024 ** 0.5, "bf16", seed=15)
+    for mesh, sA, sB, sC in ((Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ())),
+                             ([("X", 4)], ((), ("X",)), (("X",), ()), ((), ("X",)))):
+        _, g1 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", out, s.FLAG_GELU)
+        p2, g2 = run_gpu(mesh, sA, sB, sC, A, B, "bf16", out, s.FLAG_GELU | s.FLAG_FUSED | s.FLAG_RANK_ORDER)
+        assert p2.info.fused == 1
+        assert min(float(c.float().min()) for c in g1) < -0.1 and max(float(c.float().max()) for c in g1) > 8.0
+        for a, b in zip(g1, g2):
+            assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("pair", KERNELS)
 def test_accumulating_fusion_is_one_contraction(s, pair, monkeypatch):
     """Default fused path: a reduction group's products accumulate in one
@@ -815,8 +835,9 @@ def test_sm_limit_keeps_the_bits(s, case, sA, sB, sC, limit, monkeypatch):
 
 @pytest.mark.parametrize("pair", ["pair_wide", "single"])
 def test_gelu_epilogue_against_the_tanh_form(s, pair, monkeypatch):
-    """The epilogue's GeLU, x / (1 + exp(-2u)) (the tanh form through the
-    logistic identity, fast exponential), against torch's tanh-form GeLU
+    """The epilogue's GeLU, x s(2u) (the tanh form through the logistic
+    identity: one hardware exponential, the reciprocal by Newton-Raphson on
+    the FMA pipe), against torch's tanh-form GeLU
     evaluated in fp32 on the same pre-activations: the GEMM's own fp32
     output without GeLU.  Pre-activations span about +-12, so both tails
     and the zero crossing are hit."""
