@@ -286,6 +286,20 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrivals without release semantics, for the epilogue's hand-back of a
+// TMEM buffer: it publishes no memory writes.  Its TMEM reads have
+// finished (tcgen05.wait::ld) and are ordered before the MMAs that reuse
+// the buffer by the tcgen05 fences on both sides of the barrier.  Measured
+// at a tile boundary, right after a warp's last bulk store: about 1000
+// cycles for a release arrive at cluster scope, about 190 at CTA scope,
+// 11 relaxed; the MMA waits for the slowest of them.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Bounded wait whose success makes the releasing side's earlier writes
 // (from any CTA of the cluster) visible: for hand-offs between the pair.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int *status) {
@@ -546,7 +560,8 @@ __device__ __forceinline__ void store_tile_tma(const TcK &k, const TcSeg &g, int
 // Then GeLU if asked, one rounding and the stores (bulk tensor stores
 // through the staging buffers at cbuf, or per thread), and S is handed back.
 // full_bar(b): the barrier on which the MMA thread reports a finished
-// product in buffer b; release(b): hands buffer b back.
+// product in buffer b; release(b): hands buffer b back (every lane calls
+// it after its last TMEM read of the buffer; one arrival per warp).
 template <int NH, typename FullBar, typename Release>
 __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride, int tile_rows, int row_base,
                                             uint32_t lane_base, int c0, int c1, uint32_t cbuf, uint32_t share,
@@ -679,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(accf_bar(s), 1);
-            mbar_init(acce_bar(s), 4 * 32);
+            mbar_init(acce_bar(s), 4);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -831,7 +846,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     [&](int b) { return accf_bar(b); },
                     [&](int b) {
                         fence_before();
-                        mbar_arrive(acce_bar(b));
+                        __syncwarp();
+                        if (lane == 31) mbar_arrive_relaxed(acce_bar(b));
                     });
     }
 
@@ -925,7 +941,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(accf_bar(s), 1);
-            mbar_init(acce_bar(s), 2 * C::EPI_WARPS * 32);  // both CTAs' epilogue threads
+            mbar_init(acce_bar(s), 2 * C::EPI_WARPS);  // both CTAs' epilogue warps
         }
         mbar_init(drain_bar, 1);
         mbar_init(handoff_bar, 1);
@@ -1149,7 +1165,8 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                     [&](int b) { return accf_bar(b); },
                     [&](int b) {
                         fence_before();
-                        mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));  // the leader's barrier
+                        __syncwarp();
+                        if (lane == 31) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(b), 0));  // the leader's barrier
                     });
     }
 
