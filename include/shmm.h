@@ -65,6 +65,11 @@
  *   SHMM_TC_WIDE=0|1   CTA-pair tiles 256 columns wide (0) or 512 (1)
  *                      instead of the launcher's choice.  Both widths give
  *                      the same bits.
+ *   SHMM_PDL=0         CTA-pair GEMMs launch in plain stream order.  By
+ *                      default each is a programmatic dependent of the
+ *                      kernel before it in the stream: its set-up may run
+ *                      while that kernel finishes, and it touches no
+ *                      global memory until that kernel has completed.
  *   SHMM_LN_BULK=0     LayerNorm (+ all-gather) reads each row with
  *                      per-thread loads instead of staging several rows
  *                      in shared memory through the bulk-copy engine.

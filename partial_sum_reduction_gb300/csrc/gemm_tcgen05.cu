@@ -178,6 +178,16 @@ __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch.  wait: until the grids this one depends on
+// have completed and their memory is visible (returns at once for a grid
+// launched without the dependency).  launch_dependents: the next grid in
+// the stream may be scheduled, onto SMs this one leaves free, once every
+// CTA here has issued it; it runs up to its own wait.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -962,6 +972,10 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
     cluster_sync_all();  // both CTAs' barriers exist before any remote use
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // The prologue above (no global memory) may overlap the end of the
+    // previous kernel in the stream; the tiles wait for it.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     auto decode = [&](int t, int *si, int *unit, int *mt, int *nt) { tile_coords(k, t, si, unit, mt, nt); };
 
@@ -1371,17 +1385,24 @@ cudaError_t launch_pair(TcK &k, cudaStream_t s, int max_sms) {
     const int64_t total = k.total;
     const int npairs = (int)(total < cap ? total : cap);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // A programmatic dependent of the previous kernel in the stream: the
+    // prologue (barriers, TMEM, cluster sync) overlaps that kernel's last
+    // wave, and a pair GEMM launched next may start its own on the SMs this
+    // one frees.  SHMM_PDL=0 launches in plain stream order.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    const char *pdl = getenv("SHMM_PDL");
     cfg.gridDim = dim3((unsigned)(2 * npairs));
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = (pdl && pdl[0] == '0') ? 1 : 2;
     shmm::count_launch();
     return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<NH>, k);
 }
