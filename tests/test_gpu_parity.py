@@ -242,6 +242,46 @@ def test_mlp_pair_full_size_sampled(s, sY):
     _mlp(s, 8192, 4096, 16384, sY, True, rows=sorted(set(tile_rows(8192, salt=1) + [1023, 1024])))
 
 
+def test_chained_gemms_back_to_back(s, monkeypatch):
+    """The MLP pair's two GEMMs, ten times in a row on one stream with
+    nothing between the launches: each GEMM reads what the one before it
+    wrote (H), and the next first GEMM overwrites the H the second one
+    reads.  The pair kernel is a programmatic dependent launch (its set-up
+    may overlap the kernel before it); its results must be those of plain
+    stream order (SHMM_PDL=0, a synchronize after every launch), bit for
+    bit, for every link of the chain."""
+    from partial_sum_reduction_gb300 import helpers as H
+    T, D, F = 512, 256, 8192
+    X, W1, W2 = shmm_inputs.mlp_pair(T, D, F, seed=3)
+    X2 = shmm_inputs.normal_matrix((T, D), 1.0, "bf16", seed=4)
+    p1 = s.Plan(X8, ((), ()), ((), ("X",)), ((), ("X",)), T, D, F, "bf16", "bf16", s.FLAG_GELU)
+    p2 = s.Plan(X8, ((), ("X",)), (("X",), ()), ((), ()), T, F, D, "bf16", "bf16", s.FLAG_FUSED)
+    Xs = [H.shard(p1, s.TENSOR_A, X), H.shard(p1, s.TENSOR_A, X2)]
+    W1_r, W2_r = H.shard(p1, s.TENSOR_B, W1), H.shard(p2, s.TENSOR_B, W2)
+    H_r = H.alloc(p1, s.TENSOR_C, fill=float("nan"))
+    ws1, ws2 = H.workspace(p1), H.workspace(p2)
+    reps = 10
+    outs = {}
+    for pdl in ("1", "0"):
+        monkeypatch.setenv("SHMM_PDL", pdl)
+        Ys = [H.alloc(p2, s.TENSOR_C, fill=float("nan")) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for i in range(reps):
+            p1.run(Xs[i % 2], W1_r, H_r, ws1)
+            if pdl == "0":
+                torch.cuda.synchronize()
+            p2.run(H_r, W2_r, Ys[i], ws2)
+            if pdl == "0":
+                torch.cuda.synchronize()
+        s.shmm_sync_status()
+        torch.cuda.synchronize()
+        outs[pdl] = [[y.cpu() for y in Y] for Y in Ys]
+    for i in range(reps):
+        for a, b in zip(outs["1"][i], outs["0"][i]):
+            assert torch.equal(a, b), i
+    assert not torch.equal(outs["0"][0][0], outs["0"][1][0])  # the two inputs give different results
+
+
 # -------------------------------------------- collectives on given partials
 
 @pytest.mark.parametrize("G", [2, 3, 4, 5, 8, 12, 16, 24, 32])
