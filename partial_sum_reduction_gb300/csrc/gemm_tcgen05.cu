@@ -163,7 +163,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// At most one committed store group may still be reading shared memory.
 // At most `keep` (0, 1 or 3) committed store groups may still be reading
 // shared memory.
 __device__ __forceinline__ void bulk_wait_read(int keep) {
