@@ -65,6 +65,11 @@
  *   SHMM_TC_WIDE=0|1   CTA-pair tiles 256 columns wide (0) or 512 (1)
  *                      instead of the launcher's choice.  Both widths give
  *                      the same bits.
+ *   SHMM_TC_HALF_TAIL=0  no half tiles: by default, when the last wave of
+ *                      256 x 512 tiles would leave at least half the CTA
+ *                      pairs idle, its tiles run as 256-column halves, one
+ *                      round on twice as many pairs.  Both give the same
+ *                      bits.
  *   SHMM_PDL=0         CTA-pair GEMMs launch in plain stream order.  By
  *                      default each is a programmatic dependent of the
  *                      kernel before it in the stream: its set-up may run

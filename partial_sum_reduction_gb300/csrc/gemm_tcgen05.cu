@@ -93,6 +93,9 @@ struct TcK {
     uint8_t b_idx[kMaxMaps][kMaxMaps];
     int n_maps_a, n_maps_b;
     int nseg, total;  // segments; work items of all segments
+    // Work items from half_from on are half tiles: item half_from + 2 i + h
+    // is 256-column half h of tile half_from + i (half_from = total: none).
+    int half_from;
     TcSeg seg[kMaxSegs];
 };
 
@@ -470,6 +473,19 @@ __device__ __forceinline__ void tile_coords(const TcK &k, int t, int *si, int *u
     *nt = q / bm;
 }
 
+// Work item t -> its tile's coordinates, and *hh: which 256-column half a
+// half-tile item covers (0 or 1), or -1 for a whole tile.
+__device__ __forceinline__ void item_coords(const TcK &k, int t, int *si, int *unit, int *mt, int *nt, int *hh) {
+    if (t < k.half_from) {
+        *hh = -1;
+        tile_coords(k, t, si, unit, mt, nt);
+        return;
+    }
+    const int i = t - k.half_from;
+    *hh = i & 1;
+    tile_coords(k, k.half_from + (i >> 1), si, unit, mt, nt);
+}
+
 // Epilogue output staging: 32 KB per CTA, shared evenly by the epilogue
 // warps (8 KB each with four warps, 4 KB with eight).  A warp cycles
 // through its share in 32 x 32 boxes (4 KB at fp32, 2 KB at bf16), so it
@@ -593,13 +609,14 @@ __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride,
     int tile_iter = 0;
     bool ok = true;
     for (int t = first; t < k.total && ok; t += stride, ++tile_iter) {
-        int si, unit, mt, nt;
-        tile_coords(k, t, &si, &unit, &mt, &nt);
+        int si, unit, mt, nt, hh;
+        item_coords(k, t, &si, &unit, &mt, &nt, &hh);
         const TcSeg &g = k.seg[si];
         const int Gq = g.fused ? g.G : 1;
         const bool f32 = g.out_f32 != 0;
         const int64_t es = f32 ? 4 : 2;
-        for (int h = 0; h < NH && ok; ++h) {
+        const int nh = hh >= 0 ? 1 : NH;  // a half tile fills buffer 0 only
+        for (int h = 0; h < nh && ok; ++h) {
             const int bS = NH == 2 ? h : (tile_iter & 1), bW = bS ^ 1;
             const uint32_t s_base = lane_base + (uint32_t)(bS * BN);
             const uint32_t w_base = lane_base + (uint32_t)(bW * BN);
@@ -628,7 +645,7 @@ __device__ __forceinline__ void drain_tiles(const TcK &k, int first, int stride,
             }
             if (!ok) break;
             const int row0 = mt * tile_rows + row_base;
-            const int col_base = (nt * NH + h) * BN;
+            const int col_base = (nt * NH + (hh >= 0 ? hh : h)) * BN;
             if (g.tma_store) {
                 if (row0 < g.M)
                     store_tile_tma(k, g, unit, Gq, row0, col_base, c0, c1, s_base, cbuf, share, &staged, lane);
@@ -922,6 +939,9 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
     // handoff_bar (both used in the leader CTA only).
     volatile uint32_t *peer_issued = tmem_holder + 2;
     uint64_t *handoff = reinterpret_cast<uint64_t *>(tmem_holder + 4);
+    // ... and its bytes of each of its last S stages (slots 6 .. 6 + S - 1)
+    volatile uint32_t *peer_bytes = tmem_holder + 6;
+    static_assert(S <= 8, "the peer's stage bytes take slots 6..13 before the map tables at slot 16");
     // Operand slot -> map tables, copied once from the parameters into the
     // shared-memory tail (the producer looks a tile's maps up there).
     uint8_t *s_aidx = reinterpret_cast<uint8_t *>(tmem_holder + 16);
@@ -976,20 +996,23 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
     grid_dependency_wait();
     grid_launch_dependents();
 
-    auto decode = [&](int t, int *si, int *unit, int *mt, int *nt) { tile_coords(k, t, si, unit, mt, nt); };
-
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
         if (lane == 0) {
             for (int i = 0; i < k.n_maps_a; ++i) prefetch_map(&k.tmA[i]);
             for (int i = 0; i < k.n_maps_b; ++i) prefetch_map(&k.tmB[i]);
             uint32_t it = 0;  // stages loaded
+            uint32_t stage_bytes[S];  // this CTA's bytes of each stage it loaded last
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                int si, unit, mt, nt;
-                decode(t, &si, &unit, &mt, &nt);
+                int si, unit, mt, nt, hh;
+                item_coords(k, t, &si, &unit, &mt, &nt, &hh);
                 const TcSeg &g = k.seg[si];
                 const int Gq = g.fused ? g.G : 1;
+                // A half tile loads A and the two B boxes of its half, into the
+                // first half's slots.
+                const int nb = hh >= 0 ? 2 : 2 * NH;
+                const uint32_t bytes = hh >= 0 ? (uint32_t)(C::A_BYTES + C::B_BYTES / NH) : (uint32_t)C::STAGE;
                 for (int q = 0; q < Gq && ok; ++q) {
                     const int ri = g.slot_base + unit * Gq + q;
                     // The slot's maps are looked up once per tile: the row of A
@@ -1006,8 +1029,9 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                     const CUtensorMap *map_b[NB];
 #pragma unroll
                     for (int j = 0; j < NB; ++j) {
+                        const int jj = hh >= 0 ? 2 * hh + (j & 1) : j;  // the box's place in the whole tile
                         bp1[j] = shard_split(g.b_b1, g.b_bcols,
-                                             (int64_t)nt * TW + (j / 2) * BN + (int)cr * 128 + (j % 2) * 64, &bx[j]);
+                                             (int64_t)nt * TW + (jj / 2) * BN + (int)cr * 128 + (jj % 2) * 64, &bx[j]);
                         map_b[j] = &k.tmB[s_bidx[ri * kMaxMaps + wb.p * g.b_b1 + bp1[j]]];
                     }
                     for (int kb = 0; kb < g.k_blocks; ++kb, ++it) {
@@ -1017,13 +1041,15 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                             ok = false;
                             break;
                         }
-                        if (cr == 0) mbar_expect_tx(full_bar(s), 2 * C::STAGE);
+                        if (cr == 0) mbar_expect_tx(full_bar(s), 2 * bytes);
+                        stage_bytes[s] = bytes;
                         const uint32_t bar = mapa_shared(full_bar(s), 0);
                         const uint32_t a_dst = smem_u32(tiles + s * C::STAGE);
                         const uint32_t b_dst = a_dst + C::A_BYTES;
                         tma_load_2d_pair(a_dst, map_a, bar, wa.local, a_r);
 #pragma unroll
-                        for (int j = 0; j < NB; ++j) tma_load_2d_pair(b_dst + j * 8192, map_b[j], bar, bx[j], wb.local);
+                        for (int j = 0; j < NB; ++j)
+                            if (j < nb) tma_load_2d_pair(b_dst + j * 8192, map_b[j], bar, bx[j], wb.local);
                         if (wa.advance(g.a_b1, g.a_bcols, BK))
                             map_a = &k.tmA[s_aidx[ri * kMaxMaps + a_p0 * g.a_b1 + wa.p]];
                         if (wb.advance(g.b_b0, g.b_brows, BK))
@@ -1043,7 +1069,12 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
             // peer's half, and stands in for the half the peer never loaded,
             // so every stage's last phase completes once the loads that were
             // issued have landed.
+            // A stage's bytes depend on its work item (whole or half tile), so
+            // the peer hands over its bytes of its last S stages as well.
             if (cr == 1) {
+                for (int s = 0; s < S; ++s)
+                    if ((uint32_t)s < it)
+                        st_cluster_u32(mapa_shared(smem_u32((const void *)(peer_bytes + s)), 0), stage_bytes[s]);
                 st_cluster_u32(mapa_shared(smem_u32((const void *)peer_issued), 0), it);
                 mbar_arrive_cluster(mapa_shared(handoff_bar, 0));
             } else {
@@ -1052,8 +1083,8 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                 const uint32_t it_max = it_peer > it ? it_peer : it;
                 for (uint32_t i = it_peer < it ? it_peer : it; i < it_max; ++i) {
                     const int s = (int)(i % S);
-                    if (i >= it) mbar_expect_tx(full_bar(s), C::STAGE);  // the peer's half only
-                    else mbar_complete_tx(full_bar(s), C::STAGE);        // the half never loaded
+                    if (i >= it) mbar_expect_tx(full_bar(s), peer_bytes[s]);  // the peer's half only
+                    else mbar_complete_tx(full_bar(s), stage_bytes[s]);       // the half never loaded
                 }
                 for (uint32_t i = it_max > (uint32_t)S ? it_max - S : 0; i < it_max; ++i)
                     mbar_wait(full_bar((int)(i % S)), (i / S) & 1, abort_flag, k.status, false);
@@ -1068,7 +1099,9 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
             int tile_iter = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs, ++tile_iter) {
-                const TcSeg &g = k.seg[seg_of(k, t)];
+                const bool half = t >= k.half_from;  // a half tile: buffer 0 only
+                const int nh = half ? 1 : NH;
+                const TcSeg &g = k.seg[seg_of(k, half ? k.half_from + ((t - k.half_from) >> 1) : t)];
                 const int Gq = g.fused ? g.G : 1;
                 const bool accum = g.accum != 0;
                 const int k_blocks = g.k_blocks;
@@ -1120,15 +1153,19 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                             }
                             fence_after();
                             issue((int)(u % S), b, 0, kb == 0);
+                            if (half) umma2_commit_both(empty_bar((int)(u % S)));
                         }
-                        if (!ok || !wait_free(b + 1)) {
-                            ok = false;
-                            break;
-                        }
-                        for (kb = 0; kb < R; ++kb) {
-                            const int st = (int)((it + (uint32_t)kb) % S);
-                            issue(st, b + 1, 1, kb == 0);
-                            umma2_commit_both(empty_bar(st));
+                        if (!ok) break;
+                        if (!half) {
+                            if (!wait_free(b + 1)) {
+                                ok = false;
+                                break;
+                            }
+                            for (kb = 0; kb < R; ++kb) {
+                                const int st = (int)((it + (uint32_t)kb) % S);
+                                issue(st, b + 1, 1, kb == 0);
+                                umma2_commit_both(empty_bar(st));
+                            }
                         }
                         it += (uint32_t)R;
                     }
@@ -1142,6 +1179,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                         fence_after();
 #pragma unroll
                         for (int h = 0; h < NH; ++h) {
+                            if (h >= nh) break;
                             if (kb == 0 && fresh && !wait_free(b + h)) {  // 256x256 tiles only
                                 ok = false;
                                 break;
@@ -1155,6 +1193,7 @@ __global__ void __launch_bounds__(Cfg2<NH>::THREADS, 1) gemm_tc2_kernel(const __
                     if (accum && q < Gq - 1) continue;  // S is not finished
 #pragma unroll
                     for (int h = 0; h < NH; ++h) {
+                        if (h >= nh) break;
                         umma2_commit_both(accf_bar(b + h));
                         ++fills[b + h];
                     }
@@ -1297,6 +1336,23 @@ void set_tiles(TcK &k, int tile_rows, int tile_cols) {
         base += g.units * g.m_tiles * g.n_tiles;
     }
     k.total = base;
+    k.half_from = base;
+}
+
+// Tiles of a partial last wave of 256 x 512 tiles that run as 256-column
+// halves: when the wave would leave at least half the pairs idle, its r
+// tiles become 2 r half tiles, one round on 2 r pairs.  A half tile has
+// half the MMAs of a whole one for two thirds of its loads (A, and B of its
+// half), so it runs at the 256 x 256 kernel's load-bound rate: about 0.6
+// of a whole tile's time.  The halves add every output element's products
+// in the same order as the whole tile.  Returns r, or 0 for no split;
+// SHMM_TC_HALF_TAIL=0 turns it off.
+int tail_halves(int64_t tiles, int pairs) {
+    const char *e = getenv("SHMM_TC_HALF_TAIL");
+    if (e && e[0] == '0') return 0;
+    if (pairs < 1 || tiles < pairs) return 0;
+    const int64_t r = tiles % pairs;
+    return (r > 0 && 2 * r <= pairs) ? (int)r : 0;
 }
 
 template <int BN>
@@ -1383,6 +1439,13 @@ cudaError_t launch_pair(TcK &k, cudaStream_t s, int max_sms) {
     set_tiles(k, 256, 256 * NH);
     const int64_t total = k.total;
     const int npairs = (int)(total < cap ? total : cap);
+    if (NH == 2) {
+        const int r = tail_halves(total, npairs);
+        if (r) {
+            k.half_from = (int)(total - r);
+            k.total = (int)(total + r);
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1422,7 +1485,8 @@ bool pair_kernel_enabled() {
 // Measured on 8192^2 x K products (same wave counts), wide / narrow time =
 // 0.88 (1 + 4 / k-blocks per tile): 0.99 at K = 2048, 0.93 at 4096, 0.91 at
 // 16384 (the MLP's GeLU matmul, 64 k-blocks: 0.98 across 27 and 14 waves).
-// Pick the smaller estimate: waves x work per tile x that factor.
+// Pick the smaller estimate: waves x work per tile x that factor, where a
+// last wave split into half tiles (tail_halves) counts 0.6.
 // SHMM_TC_WIDE=0 / 1 forces 256- / 512-column tiles (tests compare them).
 int pair_halves(const TcK &k, int max_sms) {
     bool wide_ok = false;
@@ -1452,7 +1516,9 @@ int pair_halves(const TcK &k, int max_sms) {
     }
     const double kb = t2 > 0 ? kb_sum / (double)t2 : 1.0;  // k-blocks per tile
     const double narrow = (double)((t1 + cap1 - 1) / cap1);
-    const double wide = (double)((t2 + cap2 - 1) / cap2) * 2.0 * 0.88 * (1.0 + 4.0 / kb);
+    // a partial last wave split into half tiles takes about 0.6 of a round
+    const double rounds2 = (double)(t2 / cap2) + (t2 % cap2 == 0 ? 0.0 : tail_halves(t2, cap2) ? 0.6 : 1.0);
+    const double wide = rounds2 * 2.0 * 0.88 * (1.0 + 4.0 / kb);
     return wide < narrow ? 2 : 1;
 }
 

@@ -282,6 +282,36 @@ def test_chained_gemms_back_to_back(s, monkeypatch):
     assert not torch.equal(outs["0"][0][0], outs["0"][1][0])  # the two inputs give different results
 
 
+@pytest.mark.parametrize("case", ["gelu_ragged", "fused_all_reduce", "fused_reduce_scatter"])
+def test_half_tile_tail_keeps_the_bits(s, case, monkeypatch):
+    """96 tiles of 256x512 on 76 CTA pairs leave a last wave of 20 tiles,
+    which the launcher runs as 40 half tiles (256 columns each).  A half
+    tile adds its products in the whole tile's order, so every output has
+    the bits of the launch without the split (SHMM_TC_HALF_TAIL=0): GeLU
+    with a ragged last column tile, and a fused all-reduce and reduce-
+    scatter over 8 ranks (the accumulating mode)."""
+    monkeypatch.setenv("SHMM_TC_PAIR", "1")
+    monkeypatch.setenv("SHMM_TC_WIDE", "1")
+    if case == "gelu_ragged":   # 8 ranks x 6 x 2 tiles
+        spec = (((), ()), ((), ("X",)), ((), ("X",)))
+        I, J, K, fl = 1536, 256, 8 * 1000, s.FLAG_GELU
+    else:                       # one group of 8: 16 x 6 tiles
+        sC = ((), ()) if case == "fused_all_reduce" else (("X",), ())
+        spec = (((), ("X",)), (("X",), ()), sC)
+        I, J, K, fl = 4096, 8 * 128, 3072, s.FLAG_FUSED
+    A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=80)
+    outs = []
+    for split in ("1", "0"):
+        monkeypatch.setenv("SHMM_TC_HALF_TAIL", split)
+        p, g = run_gpu(X8, *spec, A, B, "bf16", "bf16", fl)
+        outs.append(g)
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    _, ores = oracle_run(X8, *spec, A, B, "bf16", gelu=case == "gelu_ragged",
+                         rows=sorted(set(tile_rows(I, salt=5))))
+    compare(p, outs[0], ores, exact=False, rows=sorted(set(tile_rows(I, salt=5))))
+
+
 # -------------------------------------------- collectives on given partials
 
 @pytest.mark.parametrize("G", [2, 3, 4, 5, 8, 12, 16, 24, 32])
