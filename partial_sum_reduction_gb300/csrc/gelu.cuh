@@ -1,6 +1,6 @@
 // GeLU of the column-parallel matmul's epilogue ("The simple maths behind
-// parallel training", MLP block), shared by the GEMM epilogue and the
-// reduction kernels.
+// parallel training", MLP block), shared by the tensor-core GEMM epilogue,
+// the CUDA-core GEMM and the reduction kernels.
 #pragma once
 
 // 2^v on the MUFU unit (PTX ex2.approx, subnormal results flushed to zero).

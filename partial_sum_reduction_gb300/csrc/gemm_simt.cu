@@ -15,6 +15,7 @@
 #include <cstdint>
 
 #include "checked.cuh"
+#include "gelu.cuh"
 #include "shmm_internal.h"
 
 namespace {
@@ -45,10 +46,6 @@ template <> __device__ __forceinline__ void put<__nv_bfloat16>(__nv_bfloat16 *p,
     *p = __float2bfloat16_rn(v);
 }
 
-__device__ __forceinline__ float gelu_tanh(float x) {
-    const float inner = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-    return 0.5f * x * (1.0f + tanhf(inner));
-}
 
 // One 64x64 output tile of one rank's product into acc (fp32, ascending k).
 // The k-tiles are software-pipelined: all of a tile's global loads are
