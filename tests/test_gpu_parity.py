@@ -282,34 +282,46 @@ def test_chained_gemms_back_to_back(s, monkeypatch):
     assert not torch.equal(outs["0"][0][0], outs["0"][1][0])  # the two inputs give different results
 
 
-@pytest.mark.parametrize("case", ["gelu_ragged", "fused_all_reduce", "fused_reduce_scatter"])
+@pytest.mark.parametrize("case", ["gelu_ragged", "fused_all_reduce", "fused_reduce_scatter",
+                                  "case2_in_place", "case4_in_place"])
 def test_half_tile_tail_keeps_the_bits(s, case, monkeypatch):
-    """96 tiles of 256x512 on 76 CTA pairs leave a last wave of 20 tiles,
-    which the launcher runs as 40 half tiles (256 columns each).  A half
-    tile adds its products in the whole tile's order, so every output has
-    the bits of the launch without the split (SHMM_TC_HALF_TAIL=0): GeLU
-    with a ragged last column tile, and a fused all-reduce and reduce-
-    scatter over 8 ranks (the accumulating mode)."""
+    """96 (or 256) tiles of 256x512 on 76 CTA pairs leave a last wave of 20
+    (or 28) tiles, which the launcher runs as 40 (56) half tiles of 256
+    columns.  A half tile adds its products in the whole tile's order, so
+    every output has the bits of the launch without the split
+    (SHMM_TC_HALF_TAIL=0): GeLU with a ragged last column tile, a fused
+    all-reduce and reduce-scatter over 8 ranks (the accumulating mode), and
+    operands read in place from their owners' shards (cases 2 and 4 on
+    {X:2,Y:2}; a half tile's B boxes are looked up by their own columns)."""
     monkeypatch.setenv("SHMM_TC_PAIR", "1")
     monkeypatch.setenv("SHMM_TC_WIDE", "1")
+    mesh = X8
     if case == "gelu_ragged":   # 8 ranks x 6 x 2 tiles
         spec = (((), ()), ((), ("X",)), ((), ("X",)))
         I, J, K, fl = 1536, 256, 8 * 1000, s.FLAG_GELU
-    else:                       # one group of 8: 16 x 6 tiles
+    elif case in ("fused_all_reduce", "fused_reduce_scatter"):  # one group of 8: 16 x 6 tiles
         sC = ((), ()) if case == "fused_all_reduce" else (("X",), ())
         spec = (((), ("X",)), (("X",), ()), sC)
         I, J, K, fl = 4096, 8 * 128, 3072, s.FLAG_FUSED
+    elif case == "case2_in_place":  # A gathered over X in place: 4 ranks x 6 x 4 tiles
+        mesh, spec = XY22, (((), ("X",)), ((), ()), ((), ()))
+        I, J, K, fl = 1536, 512, 2048, s.FLAG_FUSED
+    else:                           # B gathered over X in place: 4 ranks x 8 x 8 tiles
+        mesh, spec = XY22, ((("X",), ()), ((), ("X",)), (("X",), ()))
+        I, J, K, fl = 4096, 512, 4096, s.FLAG_FUSED
     A, B = shmm_inputs.scaled_normal_pair(I, J, K, "bf16", seed=80)
     outs = []
     for split in ("1", "0"):
         monkeypatch.setenv("SHMM_TC_HALF_TAIL", split)
-        p, g = run_gpu(X8, *spec, A, B, "bf16", "bf16", fl)
+        p, g = run_gpu(mesh, *spec, A, B, "bf16", "bf16", fl)
         outs.append(g)
+    if case.endswith("in_place"):
+        assert p.info.fused_gather == 1
     for a, b in zip(*outs):
         assert torch.equal(a, b)
-    _, ores = oracle_run(X8, *spec, A, B, "bf16", gelu=case == "gelu_ragged",
-                         rows=sorted(set(tile_rows(I, salt=5))))
-    compare(p, outs[0], ores, exact=False, rows=sorted(set(tile_rows(I, salt=5))))
+    rows = sorted(set(tile_rows(I, salt=5)))
+    _, ores = oracle_run(mesh, *spec, A, B, "bf16", gelu=case == "gelu_ragged", rows=rows)
+    compare(p, outs[0], ores, exact=False, rows=rows)
 
 
 # -------------------------------------------- collectives on given partials
