@@ -282,6 +282,52 @@ def test_chained_gemms_back_to_back(s, monkeypatch):
     assert not torch.equal(outs["0"][0][0], outs["0"][1][0])  # the two inputs give different results
 
 
+def test_cuda_graph_replay_matches_eager(s):
+    """The path captured into a CUDA graph and replayed gives the bits of
+    eager execution: the MLP pair's two GEMMs (the second a programmatic
+    dependent of the first, fused all-reduce) and an unfused case-3 product
+    (GEMM into partials, then the reduce-scatter kernel)."""
+    from partial_sum_reduction_gb300 import helpers as H
+    T, D, F = 512, 256, 8192
+    X, W1, W2 = shmm_inputs.mlp_pair(T, D, F, seed=5)
+    p1 = s.Plan(X8, ((), ()), ((), ("X",)), ((), ("X",)), T, D, F, "bf16", "bf16", s.FLAG_GELU)
+    p2 = s.Plan(X8, ((), ("X",)), (("X",), ()), ((), ()), T, F, D, "bf16", "bf16", s.FLAG_FUSED)
+    A, B = shmm_inputs.scaled_normal_pair(768, 1024, 640, "bf16", seed=6)
+    p3 = s.Plan(Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), 768, 1024, 640, "bf16", "bf16", 0)
+    X_r, W1_r, W2_r = H.shard(p1, s.TENSOR_A, X), H.shard(p1, s.TENSOR_B, W1), H.shard(p2, s.TENSOR_B, W2)
+    A_r, B_r = H.shard(p3, s.TENSOR_A, A), H.shard(p3, s.TENSOR_B, B)
+    H_r, Y_r, C_r = H.alloc(p1, s.TENSOR_C), H.alloc(p2, s.TENSOR_C), H.alloc(p3, s.TENSOR_C)
+    ws1, ws2, ws3 = H.workspace(p1), H.workspace(p2), H.workspace(p3)
+    assert p3.workspace_size() > 0
+
+    def chain():
+        p1.run(X_r, W1_r, H_r, ws1)
+        p2.run(H_r, W2_r, Y_r, ws2)
+        p3.run(A_r, B_r, C_r, ws3)
+
+    chain()
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in H_r + Y_r + C_r]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        chain()  # warm the capture stream once, outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        chain()
+    for _ in range(3):
+        for t in H_r + Y_r + C_r:
+            t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        s.shmm_sync_status()
+        for a, b in zip(eager, H_r + Y_r + C_r):
+            assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("case", ["gelu_ragged", "fused_all_reduce", "fused_reduce_scatter",
                                   "case2_in_place", "case4_in_place"])
 def test_half_tile_tail_keeps_the_bits(s, case, monkeypatch):
