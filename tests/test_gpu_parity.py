@@ -813,6 +813,37 @@ def test_reshard_bit_exact(s, mesh, sf, st, dtype, shape):
         np.testing.assert_array_equal(dst[r].float().cpu().numpy(), ref[r].astype(np.float32))
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("G,rows,cols", [(8, 8192, 16384), (2, 16384, 32768)])
+def test_all_to_all_at_sweep_sizes(s, G, rows, cols):
+    """The all-to-all of the collective sweep at its large end: a 256 MiB
+    bf16 array over 8 ranks and a 1 GiB one over 2, moved from row shards to
+    column shards through the benchmark's launcher, bit for bit against the
+    oracle's reshard."""
+    import oracle as orc
+    mesh, sf, st = [("X", G)], (("X",), ()), ((), ("X",))
+    full = shmm_inputs.uniform_matrix((rows, cols), -1.0, 1.0, "bf16", seed=G)
+    src, host_src = [], {}
+    for r in range(G):
+        (i0, j0), (n0, n1) = orc.shard_box(mesh, sf, (rows, cols), r)
+        blk = full[i0:i0 + n0, j0:j0 + n1].contiguous()
+        host_src[r] = blk.float().numpy()
+        src.append(blk.cuda())
+    del full
+    dst = []
+    for r in range(G):
+        _, (n0, n1) = orc.shard_box(mesh, st, (rows, cols), r)
+        dst.append(torch.full((n0, n1), float("nan"), dtype=torch.bfloat16, device="cuda"))
+    s.shmm_reshard(mesh, sf, st, rows, cols, "bf16", src, dst)
+    s.shmm_sync_status()
+    torch.cuda.synchronize()
+    del src
+    ref = orc.reshard(mesh, sf, st, host_src, (rows, cols))
+    del host_src
+    for r in range(G):
+        np.testing.assert_array_equal(dst[r].float().cpu().numpy(), ref[r].astype(np.float32))
+
+
 # --------------------------------------- sequence parallelism (f4)
 
 @pytest.mark.parametrize("rows,cols,dtype", [(64, 4096, "bf16"), (33, 1000, "f32"), (7, 12000, "bf16"),
@@ -860,6 +891,37 @@ def test_layernorm_gather_paths_agree(s, G, brows, cols, dtype, monkeypatch):
         assert torch.equal(a, b)
         got = a.float().cpu().numpy()
         assert np.abs(got - ref).max() <= tol * np.abs(ref).max()
+
+
+@pytest.mark.slow
+def test_layernorm_all_gather_full_size_sampled(s, monkeypatch):
+    """LayerNorm + all-gather at the sequence-parallel block's size: 8 ranks
+    x 1024 token rows x 4096 bf16 columns (64 MB in, 8 copies of 64 MB out).
+    Every copy holds every rank's normalised rows; one row in every 64 of
+    each copy is checked against the oracle, and the bulk-copy and register
+    paths agree bit for bit on all of it."""
+    from partial_sum_reduction_gb300 import helpers as H
+    G, brows, cols = 8, 1024, 4096
+    p = s.Plan(X8, (("X",), ()), ((), ()), ((), ()), G * brows, 8, cols, "bf16", "bf16")
+    x = shmm_inputs.normal_matrix((G * brows, cols), 2.0, "bf16", seed=21)
+    shards = [x[q * brows:(q + 1) * brows].contiguous().cuda() for q in range(G)]
+    gamma = (1.0 + 0.1 * shmm_inputs.normal_matrix((1, cols), 1.0, "f32", seed=22)[0]).cuda()
+    beta = (0.1 * shmm_inputs.normal_matrix((1, cols), 1.0, "f32", seed=23)[0]).cuda()
+    outs = {}
+    for bulk in ("1", "0"):
+        monkeypatch.setenv("SHMM_LN_BULK", bulk)
+        out = H.alloc(p, s.TENSOR_C, fill=float("nan"))
+        p.layernorm_all_gather(shards, gamma, beta, out)
+        s.shmm_sync_status()
+        torch.cuda.synchronize()
+        outs[bulk] = out
+    for a, b in zip(outs["1"], outs["0"]):
+        assert torch.equal(a, b)
+    rows = sorted(set(list(range(0, G * brows, 64)) + [q * brows - 1 for q in range(1, G + 1)]))
+    ref = oracle.layernorm(x[rows].float().numpy(), gamma.cpu().numpy(), beta.cpu().numpy(), 1e-5, "bf16")
+    for copy in outs["1"]:
+        got = copy[rows].float().cpu().numpy()
+        assert np.abs(got - ref).max() <= BF16_TOL * np.abs(ref).max()
 
 
 @pytest.mark.parametrize("fused", [True, False])
