@@ -675,10 +675,15 @@ def test_all_reduce_replicas_identical(s):
 
 # -------------------------------------------------------------- edge cases
 
-def test_empty_contraction_gives_zero(s):
-    A = torch.zeros(64, 0, dtype=torch.float32)
-    B = torch.zeros(0, 32, dtype=torch.float32)
-    plan, gpu = run_gpu(Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, "f32", "f32")
+@pytest.mark.parametrize("dtype,flags", [("f32", 0), ("bf16", 0), ("bf16", "FUSED"), ("bf16", "GELU")])
+def test_empty_contraction_gives_zero(s, dtype, flags):
+    """J = 0: every output element is the empty sum, 0 (GeLU(0) = 0), on
+    every path the plan can take, fused or not; nothing is left unwritten."""
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    fl = {0: 0, "FUSED": s.FLAG_FUSED, "GELU": s.FLAG_GELU}[flags]
+    A = torch.zeros(64, 0, dtype=tdt)
+    B = torch.zeros(0, 32, dtype=tdt)
+    plan, gpu = run_gpu(Y2, ((), ("Y",)), (("Y",), ()), (("Y",), ()), A, B, dtype, dtype, fl)
     for g in gpu:
         assert torch.equal(g, torch.zeros_like(g))
 
