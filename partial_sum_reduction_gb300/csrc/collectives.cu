@@ -30,6 +30,32 @@
 
 namespace {
 
+// Collective kernels launch as programmatic dependents of the kernel before
+// them in the stream: their CTAs may be placed on SMs that kernel frees and
+// wait in pdl_enter until it has completed and its writes are visible, so a
+// launch's set-up overlaps the end of the one before.  SHMM_PDL=0 launches
+// in plain stream order.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const char *e = getenv("SHMM_PDL");
+    cfg.attrs = attr;
+    cfg.numAttrs = (e && e[0] == '0') ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+
 using shmm_dev::in_bounds;
 
 constexpr int kMaxPtrs = SHMM_MAX_RANKS;
@@ -163,6 +189,7 @@ __device__ __forceinline__ void write_out(const ReduceK &k, int g, IT e, float *
 // memory rate of the sequential order.
 template <typename PT, typename OT, int GT, int UNROLL, typename IT, bool TREE = false>
 __global__ void __launch_bounds__(256) reduce_seq_kernel(const __grid_constant__ ReduceK k, bool gelu) {
+    pdl_enter();
     static_assert(!TREE || (GT > 0 && (GT & (GT - 1)) == 0), "register tree needs a power-of-two G");
     constexpr int V = Vec<PT>::N;
     const int G = GT > 0 ? GT : k.G;
@@ -232,6 +259,7 @@ __global__ void __launch_bounds__(256) reduce_seq_kernel(const __grid_constant__
 // Scalar fallback for shapes whose owner blocks are not whole vectors.
 template <typename PT, typename OT, bool TREE, typename IT>
 __global__ void __launch_bounds__(256) reduce_scalar_kernel(const __grid_constant__ ReduceK k, bool gelu) {
+    pdl_enter();
     const int g = blockIdx.y;
     const IT total = (IT)k.n;
     for (IT e = (IT)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (IT)gridDim.x * blockDim.x) {
@@ -261,6 +289,7 @@ __global__ void __launch_bounds__(256) reduce_scalar_kernel(const __grid_constan
 // addition is commutative bit for bit), so lane q writes destination q.
 template <typename PT, typename OT, int W, int UNROLL, typename IT>
 __global__ void __launch_bounds__(256) reduce_tree_kernel(const __grid_constant__ ReduceK k, bool gelu) {
+    pdl_enter();
     constexpr int V = Vec<PT>::N;
     constexpr int PER_WARP = 32 / W;  // vector positions per warp per step
     const int lane = threadIdx.x & 31;
@@ -352,8 +381,8 @@ template <typename PT, typename OT, typename IT>
 cudaError_t reduce_dispatch(const ReduceK &k, bool vec_ok, bool tree, bool gelu, cudaStream_t s) {
     if (!vec_ok) {
         const dim3 grid = grid_for(k.n, 256, k.ngroups);
-        if (tree) reduce_scalar_kernel<PT, OT, true, IT><<<grid, 256, 0, s>>>(k, gelu);
-        else reduce_scalar_kernel<PT, OT, false, IT><<<grid, 256, 0, s>>>(k, gelu);
+        if (tree) (void)launch_k(reduce_scalar_kernel<PT, OT, true, IT>, grid, 0, s, k, gelu);
+        else (void)launch_k(reduce_scalar_kernel<PT, OT, false, IT>, grid, 0, s, k, gelu);
         return cudaGetLastError();
     }
     if (tree && (k.G == 2 || k.G == 4 || k.G == 8 || k.G == 16)) {
@@ -365,17 +394,17 @@ cudaError_t reduce_dispatch(const ReduceK &k, bool vec_ok, bool tree, bool gelu,
                 const bool resident = sizeof(PT) == 2 || k.mode != 2;
                 const dim3 grid = resident ? grid_resident(kern, k.nvec, 256 * U2, k.ngroups)
                                            : grid_for(k.nvec, 256 * U2, k.ngroups);
-                kern<<<grid, 256, 0, s>>>(k, gelu);
+                (void)launch_k(kern, grid, 0, s, k, gelu);
                 break;
             }
-            case 4: reduce_seq_kernel<PT, OT, 4, 2, IT, true><<<grid_for(k.nvec, 256 * 2, k.ngroups), 256, 0, s>>>(k, gelu); break;
+            case 4: (void)launch_k(reduce_seq_kernel<PT, OT, 4, 2, IT, true>, grid_for(k.nvec, 256 * 2, k.ngroups), 0, s, k, gelu); break;
             case 8:  // as the sequential eight-rank case below
                 if (sizeof(PT) == 4 && k.mode == 2)
-                    reduce_seq_kernel<PT, OT, 8, 1, IT, true><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu);
+                    (void)launch_k(reduce_seq_kernel<PT, OT, 8, 1, IT, true>, grid_for(k.nvec, 256, k.ngroups), 0, s, k, gelu);
                 else
-                    reduce_seq_kernel<PT, OT, 8, 2, IT, true><<<grid_for(k.nvec, 512, k.ngroups), 256, 0, s>>>(k, gelu);
+                    (void)launch_k(reduce_seq_kernel<PT, OT, 8, 2, IT, true>, grid_for(k.nvec, 512, k.ngroups), 0, s, k, gelu);
                 break;
-            default: reduce_seq_kernel<PT, OT, 16, 1, IT, true><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
+            default: (void)launch_k(reduce_seq_kernel<PT, OT, 16, 1, IT, true>, grid_for(k.nvec, 256, k.ngroups), 0, s, k, gelu); break;
         }
         return cudaGetLastError();
     }
@@ -386,17 +415,17 @@ cudaError_t reduce_dispatch(const ReduceK &k, bool vec_ok, bool tree, bool gelu,
         constexpr int U = 4;  // vector positions per lane in flight
         const dim3 grid = grid_for(k.nvec, 8 * (32 / W) * U, k.ngroups);  // 8 warps per CTA
         switch (W) {
-            case 1: reduce_tree_kernel<PT, OT, 1, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
-            case 2: reduce_tree_kernel<PT, OT, 2, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
-            case 4: reduce_tree_kernel<PT, OT, 4, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
-            case 8: reduce_tree_kernel<PT, OT, 8, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
-            case 16: reduce_tree_kernel<PT, OT, 16, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
-            default: reduce_tree_kernel<PT, OT, 32, U, IT><<<grid, 256, 0, s>>>(k, gelu); break;
+            case 1: (void)launch_k(reduce_tree_kernel<PT, OT, 1, U, IT>, grid, 0, s, k, gelu); break;
+            case 2: (void)launch_k(reduce_tree_kernel<PT, OT, 2, U, IT>, grid, 0, s, k, gelu); break;
+            case 4: (void)launch_k(reduce_tree_kernel<PT, OT, 4, U, IT>, grid, 0, s, k, gelu); break;
+            case 8: (void)launch_k(reduce_tree_kernel<PT, OT, 8, U, IT>, grid, 0, s, k, gelu); break;
+            case 16: (void)launch_k(reduce_tree_kernel<PT, OT, 16, U, IT>, grid, 0, s, k, gelu); break;
+            default: (void)launch_k(reduce_tree_kernel<PT, OT, 32, U, IT>, grid, 0, s, k, gelu); break;
         }
         return cudaGetLastError();
     }
     switch (k.G) {
-        case 1: reduce_seq_kernel<PT, OT, 1, 4, IT><<<grid_for(k.nvec, 256 * 4, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        case 1: (void)launch_k(reduce_seq_kernel<PT, OT, 1, 4, IT>, grid_for(k.nvec, 256 * 4, k.ngroups), 0, s, k, gelu); break;
         case 2: {
             // Two ranks (measured at 64 and 256 MiB per rank): bf16 partials
             // with 2 vectors per thread and a grid of resident CTAs only,
@@ -408,10 +437,10 @@ cudaError_t reduce_dispatch(const ReduceK &k, bool vec_ok, bool tree, bool gelu,
             const bool resident = sizeof(PT) == 2 || k.mode != 2;
             const dim3 grid = resident ? grid_resident(kern, k.nvec, 256 * U2, k.ngroups)
                                        : grid_for(k.nvec, 256 * U2, k.ngroups);
-            kern<<<grid, 256, 0, s>>>(k, gelu);
+            (void)launch_k(kern, grid, 0, s, k, gelu);
             break;
         }
-        case 4: reduce_seq_kernel<PT, OT, 4, 2, IT><<<grid_for(k.nvec, 256 * 2, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        case 4: (void)launch_k(reduce_seq_kernel<PT, OT, 4, 2, IT>, grid_for(k.nvec, 256 * 2, k.ngroups), 0, s, k, gelu); break;
         case 8:
             // Eight ranks (256 MiB per rank): two vectors per thread, 16 loads
             // in flight, took the reduce-scatter from 0.965 to 0.973-0.976 of
@@ -419,12 +448,12 @@ cudaError_t reduce_dispatch(const ReduceK &k, bool vec_ok, bool tree, bool gelu,
             // all-reduce 0.948 -> 0.978; the fp32 all-reduce lost (0.972 ->
             // 0.945) and keeps one.
             if (sizeof(PT) == 4 && k.mode == 2)
-                reduce_seq_kernel<PT, OT, 8, 1, IT><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu);
+                (void)launch_k(reduce_seq_kernel<PT, OT, 8, 1, IT>, grid_for(k.nvec, 256, k.ngroups), 0, s, k, gelu);
             else
-                reduce_seq_kernel<PT, OT, 8, 2, IT><<<grid_for(k.nvec, 512, k.ngroups), 256, 0, s>>>(k, gelu);
+                (void)launch_k(reduce_seq_kernel<PT, OT, 8, 2, IT>, grid_for(k.nvec, 512, k.ngroups), 0, s, k, gelu);
             break;
-        case 16: reduce_seq_kernel<PT, OT, 16, 1, IT><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
-        default: reduce_seq_kernel<PT, OT, 0, 1, IT><<<grid_for(k.nvec, 256, k.ngroups), 256, 0, s>>>(k, gelu); break;
+        case 16: (void)launch_k(reduce_seq_kernel<PT, OT, 16, 1, IT>, grid_for(k.nvec, 256, k.ngroups), 0, s, k, gelu); break;
+        default: (void)launch_k(reduce_seq_kernel<PT, OT, 0, 1, IT>, grid_for(k.nvec, 256, k.ngroups), 0, s, k, gelu); break;
     }
     return cudaGetLastError();
 }
@@ -441,6 +470,7 @@ cudaError_t reduce_dispatch_idx(const ReduceK &k, bool vec_ok, bool tree, bool g
 // load in flight per thread left the gather at 0.88 of the copy rate).
 template <bool VEC16, typename IT>
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherK k, int elem) {
+    pdl_enter();
     const int g = blockIdx.y;
     const IT total = (IT)k.nvec;
     const IT bvecs = (IT)k.bvecs, brows = (IT)k.brows, per_block = brows * bvecs;
@@ -528,6 +558,7 @@ __device__ __forceinline__ float block_sum(float v, float *scratch) {
 // whole 16-byte vectors, cols <= 8192, take the register path below.
 template <typename T>
 __global__ void __launch_bounds__(256) ln_gather_scalar_kernel(const __grid_constant__ LnK k) {
+    pdl_enter();
     __shared__ float scratch[32];
     const int g = blockIdx.y;
     const int64_t rows = (int64_t)k.G * k.brows;
@@ -563,6 +594,7 @@ __global__ void __launch_bounds__(256) ln_gather_scalar_kernel(const __grid_cons
 // the plain all-gather).
 template <typename T, int NVT>
 __global__ void __launch_bounds__(256) ln_gather_reg_kernel(const __grid_constant__ LnK k) {
+    pdl_enter();
     constexpr int V = 16 / sizeof(T);
     __shared__ float scratch[32];
     const int g = blockIdx.y;
@@ -643,6 +675,7 @@ __global__ void __launch_bounds__(256) ln_gather_reg_kernel(const __grid_constan
 constexpr int kLnMaxStages = 4;
 template <typename T, int NVT>
 __global__ void __launch_bounds__(256) ln_gather_bulk_kernel(const __grid_constant__ LnK k, int stages) {
+    pdl_enter();
     constexpr int V = 16 / sizeof(T);
     extern __shared__ __align__(128) uint8_t ln_rows[];  // `stages` rows of cols elements
     __shared__ __align__(8) uint64_t bars[kLnMaxStages];
@@ -785,7 +818,7 @@ cudaError_t launch_ln_bulk(const LnK &k, dim3 grid, int stages, size_t smem, cud
         if (e != cudaSuccess) return e;
         attr_set.set(dev, 1);
     }
-    ln_gather_bulk_kernel<T, NVT><<<grid, 256, smem, s>>>(k, stages);
+    (void)launch_k(ln_gather_bulk_kernel<T, NVT>, grid, smem, s, k, stages);
     return cudaGetLastError();
 }
 
@@ -804,6 +837,7 @@ struct CopyK {
 // left a 16 MiB all-to-all at 0.47 of the copy rate, latency-bound).
 template <bool VEC, typename IT>
 __global__ void __launch_bounds__(256) copy_rects_kernel(const __grid_constant__ CopyK k, int elem) {
+    pdl_enter();
     const shmm::CopyRect &R = k.r[blockIdx.y];
     const IT per_row = VEC ? (IT)(R.w * elem / 16) : (IT)R.w;
     const IT total = per_row * (IT)R.h;
@@ -902,17 +936,17 @@ int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream) {
         return (int)e;
     }
     if (reg && a.dt == SHMM_F32) {
-        if (nvt <= 1) ln_gather_reg_kernel<float, 1><<<grid, 256, 0, s>>>(k);
-        else if (nvt == 2) ln_gather_reg_kernel<float, 2><<<grid, 256, 0, s>>>(k);
-        else ln_gather_reg_kernel<float, 4><<<grid, 256, 0, s>>>(k);
+        if (nvt <= 1) (void)launch_k(ln_gather_reg_kernel<float, 1>, grid, 0, s, k);
+        else if (nvt == 2) (void)launch_k(ln_gather_reg_kernel<float, 2>, grid, 0, s, k);
+        else (void)launch_k(ln_gather_reg_kernel<float, 4>, grid, 0, s, k);
     } else if (reg) {
-        if (nvt <= 1) ln_gather_reg_kernel<__nv_bfloat16, 1><<<grid, 256, 0, s>>>(k);
-        else if (nvt == 2) ln_gather_reg_kernel<__nv_bfloat16, 2><<<grid, 256, 0, s>>>(k);
-        else ln_gather_reg_kernel<__nv_bfloat16, 4><<<grid, 256, 0, s>>>(k);
+        if (nvt <= 1) (void)launch_k(ln_gather_reg_kernel<__nv_bfloat16, 1>, grid, 0, s, k);
+        else if (nvt == 2) (void)launch_k(ln_gather_reg_kernel<__nv_bfloat16, 2>, grid, 0, s, k);
+        else (void)launch_k(ln_gather_reg_kernel<__nv_bfloat16, 4>, grid, 0, s, k);
     } else if (a.dt == SHMM_F32) {
-        ln_gather_scalar_kernel<float><<<grid, 256, 0, s>>>(k);
+        (void)launch_k(ln_gather_scalar_kernel<float>, grid, 0, s, k);
     } else {
-        ln_gather_scalar_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(k);
+        (void)launch_k(ln_gather_scalar_kernel<__nv_bfloat16>, grid, 0, s, k);
     }
     return (int)cudaGetLastError();
 }
@@ -943,11 +977,11 @@ int launch_copy_rects(const CopyRect *rects, int n, int elem, int *status, void 
         const dim3 grid((unsigned)want, (unsigned)m, 1);
         count_launch();
         if (vec) {
-            if (small) copy_rects_kernel<true, uint32_t><<<grid, 256, 0, s>>>(k, elem);
-            else copy_rects_kernel<true, uint64_t><<<grid, 256, 0, s>>>(k, elem);
+            if (small) (void)launch_k(copy_rects_kernel<true, uint32_t>, grid, 0, s, k, elem);
+            else (void)launch_k(copy_rects_kernel<true, uint64_t>, grid, 0, s, k, elem);
         } else {
-            if (small) copy_rects_kernel<false, uint32_t><<<grid, 256, 0, s>>>(k, elem);
-            else copy_rects_kernel<false, uint64_t><<<grid, 256, 0, s>>>(k, elem);
+            if (small) (void)launch_k(copy_rects_kernel<false, uint32_t>, grid, 0, s, k, elem);
+            else (void)launch_k(copy_rects_kernel<false, uint64_t>, grid, 0, s, k, elem);
         }
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return (int)e;
@@ -1020,11 +1054,11 @@ int launch_gather(const GatherArgs &a, int *status, void *stream) {
                        (int64_t)a.blocks0 * a.brows * k.full_vecs < ((int64_t)1 << 32) - 64;
     count_launch();
     if (vec) {
-        if (small) gather_kernel<true, uint32_t><<<grid, 256, 0, s>>>(k, elem);
-        else gather_kernel<true, uint64_t><<<grid, 256, 0, s>>>(k, elem);
+        if (small) (void)launch_k(gather_kernel<true, uint32_t>, grid, 0, s, k, elem);
+        else (void)launch_k(gather_kernel<true, uint64_t>, grid, 0, s, k, elem);
     } else {
-        if (small) gather_kernel<false, uint32_t><<<grid, 256, 0, s>>>(k, elem);
-        else gather_kernel<false, uint64_t><<<grid, 256, 0, s>>>(k, elem);
+        if (small) (void)launch_k(gather_kernel<false, uint32_t>, grid, 0, s, k, elem);
+        else (void)launch_k(gather_kernel<false, uint64_t>, grid, 0, s, k, elem);
     }
     return (int)cudaGetLastError();
 }
