@@ -26,33 +26,17 @@
 #include "checked.cuh"
 #include "device_wait.cuh"
 #include "gelu.cuh"
+#include "pdl.cuh"
 #include "shmm_internal.h"
 
 namespace {
 
-// Collective kernels launch as programmatic dependents of the kernel before
-// them in the stream: their CTAs may be placed on SMs that kernel frees and
-// wait in pdl_enter until it has completed and its writes are visible, so a
-// launch's set-up overlaps the end of the one before.  SHMM_PDL=0 launches
-// in plain stream order.
-__device__ __forceinline__ void pdl_enter() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+using shmm_pdl::pdl_enter;
+// Every collective kernel runs 256 threads and is a programmatic dependent
+// launch (pdl.cuh).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, size_t smem, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    const char *e = getenv("SHMM_PDL");
-    cfg.attrs = attr;
-    cfg.numAttrs = (e && e[0] == '0') ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
+    return shmm_pdl::launch_pdl(kern, grid, dim3(256), smem, s, args...);
 }
 
 

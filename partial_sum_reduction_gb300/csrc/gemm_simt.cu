@@ -16,6 +16,7 @@
 
 #include "checked.cuh"
 #include "gelu.cuh"
+#include "pdl.cuh"
 #include "shmm_internal.h"
 
 namespace {
@@ -113,6 +114,7 @@ __device__ __forceinline__ void tile_product(const SimtK &k, const IT *__restric
 
 template <typename IT, typename OT>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ SimtK k) {
+    shmm_pdl::pdl_enter();
     __shared__ float As[BK][BM];
     __shared__ float Bs[BK][BN];
     const int unit = blockIdx.z;
@@ -188,11 +190,13 @@ int launch_gemm_simt(const GemmArgs &a, int *status, void *stream) {
     dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)a.units);
     cudaStream_t s = (cudaStream_t)stream;
     count_launch();
-    if (a.in_dt == SHMM_F32 && a.out_dt == SHMM_F32) gemm_simt_kernel<float, float><<<grid, 256, 0, s>>>(k);
-    else if (a.in_dt == SHMM_F32) gemm_simt_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(k);
-    else if (a.out_dt == SHMM_F32) gemm_simt_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(k);
-    else gemm_simt_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(k);
-    return (int)cudaGetLastError();
+    using shmm_pdl::launch_pdl;
+    cudaError_t e;
+    if (a.in_dt == SHMM_F32 && a.out_dt == SHMM_F32) e = launch_pdl(gemm_simt_kernel<float, float>, grid, dim3(256), 0, s, k);
+    else if (a.in_dt == SHMM_F32) e = launch_pdl(gemm_simt_kernel<float, __nv_bfloat16>, grid, dim3(256), 0, s, k);
+    else if (a.out_dt == SHMM_F32) e = launch_pdl(gemm_simt_kernel<__nv_bfloat16, float>, grid, dim3(256), 0, s, k);
+    else e = launch_pdl(gemm_simt_kernel<__nv_bfloat16, __nv_bfloat16>, grid, dim3(256), 0, s, k);
+    return (int)e;
 }
 
 }  // namespace shmm
