@@ -39,7 +39,6 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, size_t smem, cudaStream_
     return shmm_pdl::launch_pdl(kern, grid, dim3(256), smem, s, args...);
 }
 
-
 using shmm_dev::in_bounds;
 
 constexpr int kMaxPtrs = SHMM_MAX_RANKS;
