@@ -657,8 +657,7 @@ __global__ void __launch_bounds__(256) ln_gather_reg_kernel(const __grid_constan
 // exit thread 0 waits (bounded) for every copy it issued.
 constexpr int kLnMaxStages = 4;
 template <typename T, int NVT>
-__global__ void __launch_bounds__(256) ln_gather_bulk_kernel(const __grid_constant__ LnK k, int stages) {
-    pdl_enter();
+__device__ __forceinline__ void ln_gather_bulk(const LnK &k, int stages) {
     constexpr int V = 16 / sizeof(T);
     extern __shared__ __align__(128) uint8_t ln_rows[];  // `stages` rows of cols elements
     __shared__ __align__(8) uint64_t bars[kLnMaxStages];
@@ -785,23 +784,45 @@ __global__ void __launch_bounds__(256) ln_gather_bulk_kernel(const __grid_consta
     }
 }
 
+// The bulk path's kernels: the compiler's own register budget (three CTAs
+// per SM for rows of up to 4096 bf16 columns), and a 64-register cap for
+// four CTAs per SM.  With two members a row has few stores to hide its two
+// block reductions behind, so more rows in flight pay: four CTAs took bf16
+// rows of 4096 from 0.76 to 0.81 of the copy rate at 256 MiB; with 8
+// members, and for fp32, the cap cost more than the extra rows gave.
+template <typename T, int NVT>
+__global__ void __launch_bounds__(256) ln_gather_bulk_kernel(const __grid_constant__ LnK k, int stages) {
+    pdl_enter();
+    ln_gather_bulk<T, NVT>(k, stages);
+}
+template <typename T, int NVT>
+__global__ void __launch_bounds__(256, 4) ln_gather_bulk4_kernel(const __grid_constant__ LnK k, int stages) {
+    pdl_enter();
+    ln_gather_bulk<T, NVT>(k, stages);
+}
+
 // Dynamic shared memory the bulk-copy LayerNorm may take per CTA (above the
 // 48 KB default, so each instantiation opts in once per device).
 constexpr int kLnSmemBudget = 64 * 1024;
-template <typename T, int NVT>
+template <typename T, int NVT, bool FOUR = false>
 cudaError_t launch_ln_bulk(const LnK &k, dim3 grid, int stages, size_t smem, cudaStream_t s) {
+    void (*kern)(LnK, int);
+    if constexpr (FOUR)
+        kern = ln_gather_bulk4_kernel<T, NVT>;
+    else
+        kern = ln_gather_bulk_kernel<T, NVT>;
     static shmm::PerDevice<int> attr_set;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= shmm::kMaxDevices) return cudaErrorInvalidDevice;
     if (!attr_set.get(dev)) {
-        e = cudaFuncSetAttribute(ln_gather_bulk_kernel<T, NVT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kLnSmemBudget);
         if (e != cudaSuccess) return e;
         attr_set.set(dev, 1);
     }
-    (void)launch_k(ln_gather_bulk_kernel<T, NVT>, grid, smem, s, k, stages);
+    (void)launch_k(kern, grid, smem, s, k, stages);
     return cudaGetLastError();
 }
 
@@ -912,6 +933,9 @@ int launch_layernorm_gather(const LayerNormArgs &a, int *status, void *stream) {
         if (a.dt == SHMM_F32)
             e = nvt <= 1 ? launch_ln_bulk<float, 1>(k, grid, st, sm, s)
                          : nvt == 2 ? launch_ln_bulk<float, 2>(k, grid, st, sm, s) : launch_ln_bulk<float, 4>(k, grid, st, sm, s);
+        else if (a.G <= 2 && nvt <= 2)  // four CTAs per SM (see the kernels)
+            e = nvt <= 1 ? launch_ln_bulk<__nv_bfloat16, 1, true>(k, grid, st, sm, s)
+                         : launch_ln_bulk<__nv_bfloat16, 2, true>(k, grid, st, sm, s);
         else
             e = nvt <= 1 ? launch_ln_bulk<__nv_bfloat16, 1>(k, grid, st, sm, s)
                          : nvt == 2 ? launch_ln_bulk<__nv_bfloat16, 2>(k, grid, st, sm, s)
