@@ -70,13 +70,12 @@
  *                      pairs idle, its tiles run as 256-column halves, one
  *                      round on twice as many pairs.  Both give the same
  *                      bits.
- *   SHMM_PDL=0         CTA-pair GEMMs, the CUDA-core GEMM and the
- *                      collective kernels launch in plain stream order
- *                      (single-CTA tensor-core GEMMs always do).  By
- *                      default each is a programmatic dependent of the
- *                      kernel before it in the stream: its set-up may run
- *                      while that kernel finishes, and it touches no
- *                      global memory until that kernel has completed.
+ *   SHMM_PDL=0         the GEMMs and the collective kernels launch in
+ *                      plain stream order.  By default each is a
+ *                      programmatic dependent of the kernel before it in
+ *                      the stream: its set-up may run while that kernel
+ *                      finishes, and it touches no global memory until
+ *                      that kernel has completed.
  *   SHMM_LN_BULK=0     LayerNorm (+ all-gather) reads each row with
  *                      per-thread loads instead of staging several rows
  *                      in shared memory through the bulk-copy engine.

@@ -737,6 +737,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // The prologue above (no global memory) may overlap the end of the
+    // previous kernel in the stream; the tiles wait for it.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     auto decode = [&](int t, int *si, int *unit, int *mt, int *nt) { tile_coords(k, t, si, unit, mt, nt); };
 
@@ -1373,9 +1377,20 @@ cudaError_t launch_bn(TcK &k, cudaStream_t s, int max_sms) {
     int ctas = num_sms();
     if (max_sms > 0 && max_sms < ctas) ctas = max_sms;
     const int grid = (int)(total < ctas ? total : ctas);
+    // a programmatic dependent of the kernel before it, as the pair kernel
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const char *pdl = getenv("SHMM_PDL");
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = (pdl && pdl[0] == '0') ? 0 : 1;
     shmm::count_launch();
-    gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, s>>>(k);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, k);
 }
 
 // CTA pairs of gemm_tc2_kernel<NH> that can be resident at once (one CTA
